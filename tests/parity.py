@@ -1,0 +1,55 @@
+"""Comparison helpers shared by the parity tests (no attention arithmetic).
+
+Acceptance, per tensor and per packed segment: for 16-bit inputs, cosine
+similarity >= 0.9999 and max|gpu - ref| <= 2e-2 * max|ref|; for fp32 inputs,
+max|gpu - ref| <= 1e-4 * max|ref|.  Comparisons are made in fp64.
+"""
+from __future__ import annotations
+
+import torch
+
+BF16_TOL_REL = 2e-2
+BF16_MIN_COS = 0.9999
+FP32_TOL_REL = 1e-4
+
+
+def tolerances(dtype):
+    if dtype == torch.float32:
+        return FP32_TOL_REL, 0.0
+    return BF16_TOL_REL, BF16_MIN_COS
+
+
+def compare(got, ref, tol_rel, min_cos):
+    got = got.detach().to("cpu", torch.float64).reshape(-1)
+    ref = ref.detach().to("cpu", torch.float64).reshape(-1)
+    max_ref = float(ref.abs().max()) if ref.numel() else 0.0
+    err = float((got - ref).abs().max()) if ref.numel() else 0.0
+    finite = bool(torch.isfinite(got).all())
+    ng, nr = float(got.norm()), float(ref.norm())
+    if nr == 0.0 and ng == 0.0:
+        cos = 1.0
+    elif nr == 0.0 or ng == 0.0:
+        cos = 0.0
+    else:
+        cos = float((got @ ref) / (ng * nr))
+    ok = finite and err <= tol_rel * max_ref + 1e-30 and (min_cos <= 0.0 or cos >= min_cos
+                                                           or max_ref == 0.0)
+    if max_ref == 0.0:
+        ok = finite and err == 0.0
+    return dict(ok=ok, cos=cos, max_err=err, max_ref=max_ref, finite=finite)
+
+
+def per_segment_report(got, ref, cu, name, tol_rel, min_cos):
+    """One comparison per packed segment of a [T, H, D] tensor."""
+    out = []
+    cu = [int(x) for x in cu]
+    for b in range(len(cu) - 1):
+        r = compare(got[cu[b]:cu[b + 1]], ref[cu[b]:cu[b + 1]], tol_rel, min_cos)
+        r.update(tensor=name, segment=b, length=cu[b + 1] - cu[b])
+        out.append(r)
+    return out
+
+
+def assert_all_ok(reports, what=""):
+    bad = [r for r in reports if not r["ok"]]
+    assert not bad, f"{what}: {len(bad)} failing comparisons, first: {bad[:3]}"
