@@ -5,4 +5,4 @@ The compute path is a C-ABI shared library of hand-written CUDA kernels
 this package does not load the library; ``binding.load()`` does, and raises if
 the library is missing.
 """
-__all__ = ["binding", "workloads", "flops"]
+__all__ = ["binding", "build", "workloads", "flops"]

@@ -1,0 +1,223 @@
+"""ctypes binding of the C ABI in include/attn_bwd.h (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of ``libattn_bwd.so``;
+this module only fills the parameter structs from torch tensors, allocates
+outputs / workspace with torch (the library itself allocates nothing) and
+passes the caller's current CUDA stream.  ``load()`` raises if the library has
+not been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_bwd.so")
+
+ATTN_BF16, ATTN_FP16, ATTN_FP32 = 0, 1, 2
+MASK_NONE, MASK_CAUSAL_TOP_LEFT, MASK_CAUSAL_BOTTOM_RIGHT, MASK_WINDOW = 0, 1, 2, 3
+STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED_HEADDIM",
+          -3: "ATTN_ERR_WORKSPACE_TOO_SMALL", -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_DEVICE_FLAG",
+          -6: "ATTN_ERR_TIMEOUT", -7: "ATTN_ERR_BAD_SEQLENS"}
+
+_DTYPES = {torch.bfloat16: ATTN_BF16, torch.float16: ATTN_FP16, torch.float32: ATTN_FP32}
+
+_i32, _vp, _f32 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+
+
+class AttnBwdParams(ctypes.Structure):
+    _fields_ = [("dtype", _i32), ("batch", _i32), ("nhead_q", _i32), ("nhead_kv", _i32),
+                ("seqlen_q", _i32), ("seqlen_k", _i32), ("total_q", _i32), ("total_k", _i32),
+                ("d_qk", _i32), ("d_v", _i32), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
+                ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
+                ("softmax_scale", _f32), ("deterministic", _i32),
+                ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("dout", _vp), ("lse", _vp),
+                ("dq", _vp), ("dk", _vp), ("dv", _vp)]
+
+
+class AttnFwdParams(ctypes.Structure):
+    _fields_ = [("dtype", _i32), ("batch", _i32), ("nhead_q", _i32), ("nhead_kv", _i32),
+                ("seqlen_q", _i32), ("seqlen_k", _i32), ("total_q", _i32), ("total_k", _i32),
+                ("d_qk", _i32), ("d_v", _i32), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
+                ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
+                ("softmax_scale", _f32), ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp)]
+
+
+EXPORTS = ["attn_bwd_workspace_size", "attn_bwd", "attn_bwd_timed", "attn_bwd_read_status",
+           "attn_fwd", "attn_status_string"]
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libattn_bwd.so and declare its signatures.  Raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (python -m head_attention_backward_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    lib.attn_bwd_workspace_size.argtypes = [P(AttnBwdParams), P(ctypes.c_size_t)]
+    lib.attn_bwd_workspace_size.restype = ctypes.c_int
+    lib.attn_bwd.argtypes = [P(AttnBwdParams), _vp, ctypes.c_size_t, _vp]
+    lib.attn_bwd.restype = ctypes.c_int
+    lib.attn_bwd_timed.argtypes = [P(AttnBwdParams), _vp, ctypes.c_size_t, _vp, P(ctypes.c_float)]
+    lib.attn_bwd_timed.restype = ctypes.c_int
+    lib.attn_bwd_read_status.argtypes = [_vp, _vp, P(ctypes.c_int)]
+    lib.attn_bwd_read_status.restype = ctypes.c_int
+    lib.attn_fwd.argtypes = [P(AttnFwdParams), _vp]
+    lib.attn_fwd.restype = ctypes.c_int
+    lib.attn_status_string.argtypes = [ctypes.c_int]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({attn_status_string(status)})")
+
+
+# ------------------------------------------------------------ raw entry points
+
+def attn_bwd_workspace_size(p: AttnBwdParams):
+    n = ctypes.c_size_t(0)
+    st = load().attn_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n))
+    return st, n.value
+
+
+def attn_bwd(p: AttnBwdParams, workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    return load().attn_bwd(ctypes.byref(p), workspace, workspace_bytes, stream)
+
+
+def attn_bwd_timed(p: AttnBwdParams, workspace: int, workspace_bytes: int, stream: int = 0):
+    ms = (ctypes.c_float * 4)()
+    st = load().attn_bwd_timed(ctypes.byref(p), workspace, workspace_bytes, stream, ms)
+    return st, list(ms)
+
+
+def attn_bwd_read_status(workspace: int, stream: int = 0):
+    s = ctypes.c_int(0)
+    st = load().attn_bwd_read_status(workspace, stream, ctypes.byref(s))
+    return st, s.value
+
+
+def attn_fwd(p: AttnFwdParams, stream: int = 0) -> int:
+    return load().attn_fwd(ctypes.byref(p), stream)
+
+
+def attn_status_string(st: int) -> str:
+    return load().attn_status_string(st).decode()
+
+
+# ------------------------------------------------------- tensor marshalling
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k):
+    if cu_seqlens_q is None:
+        b, sq, hq, dqk = q.shape
+        sk, hkv, dv = k.shape[1], k.shape[2], v.shape[3]
+        return dict(batch=b, nhead_q=hq, nhead_kv=hkv, seqlen_q=sq, seqlen_k=sk, total_q=0,
+                    total_k=0, d_qk=dqk, d_v=dv)
+    tq, hq, dqk = q.shape
+    tk, hkv, dv = k.shape[0], k.shape[1], v.shape[2]
+    return dict(batch=cu_seqlens_q.numel() - 1, nhead_q=hq, nhead_kv=hkv, seqlen_q=max_seqlen_q,
+                seqlen_k=max_seqlen_k, total_q=tq, total_k=tk, d_qk=dqk, d_v=dv)
+
+
+def bwd_params(q, k, v, o, do, lse, dq, dk, dv, *, scale, mask=MASK_NONE, left=-1, right=-1,
+               deterministic=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0,
+               max_seqlen_k=0) -> AttnBwdParams:
+    p = AttnBwdParams()
+    p.dtype = _DTYPES[q.dtype]
+    for name, val in _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k).items():
+        setattr(p, name, val)
+    p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    p.mask, p.window_left, p.window_right = mask, left, right
+    p.softmax_scale = scale
+    p.deterministic = 1 if deterministic else 0
+    p.q, p.k, p.v, p.o, p.dout, p.lse = (_ptr(t) for t in (q, k, v, o, do, lse))
+    p.dq, p.dk, p.dv = _ptr(dq), _ptr(dk), _ptr(dv)
+    return p
+
+
+def fwd_params(q, k, v, o, lse, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlens_q=None,
+               cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0) -> AttnFwdParams:
+    p = AttnFwdParams()
+    p.dtype = _DTYPES[q.dtype]
+    for name, val in _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k).items():
+        setattr(p, name, val)
+    p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    p.mask, p.window_left, p.window_right = mask, left, right
+    p.softmax_scale = scale
+    p.q, p.k, p.v, p.o, p.lse = (_ptr(t) for t in (q, k, v, o, lse))
+    return p
+
+
+def workspace_bytes(p: AttnBwdParams) -> int:
+    st, n = attn_bwd_workspace_size(p)
+    if st != 0:
+        raise AttnError(st, "attn_bwd_workspace_size")
+    return n
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def attn_forward(q, k, v, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlens_q=None,
+                 cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, stream=None):
+    """O and LSE from the library's forward helper (outputs allocated here)."""
+    if cu_seqlens_q is None:
+        o = torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+        lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
+    else:
+        o = torch.empty(q.shape[:2] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    p = fwd_params(q, k, v, o, lse, scale=scale, mask=mask, left=left, right=right,
+                   cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                   max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
+    st = attn_fwd(p, _stream(stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd")
+    return o, lse
+
+
+def attn_backward(q, k, v, o, do, lse, *, scale, mask=MASK_NONE, left=-1, right=-1,
+                  deterministic=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0,
+                  max_seqlen_k=0, workspace=None, out=None, stream=None, check_status=True):
+    """dQ, dK, dV through attn_bwd (outputs and workspace allocated here unless given)."""
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    p = bwd_params(q, k, v, o, do, lse, dq, dk, dv, scale=scale, mask=mask, left=left, right=right,
+                   deterministic=deterministic, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                   max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
+    n = workspace_bytes(p)
+    if workspace is None or workspace.numel() < n:
+        workspace = alloc_workspace(n, q.device)
+    s = _stream(stream)
+    st = attn_bwd(p, workspace.data_ptr(), workspace.numel(), s)
+    if st != 0:
+        raise AttnError(st, "attn_bwd")
+    if check_status:
+        st, dev = attn_bwd_read_status(workspace.data_ptr(), s)
+        if st != 0:
+            raise AttnError(st, "attn_bwd_read_status")
+        if dev != 0:
+            raise AttnError(dev, "attn_bwd (device status)")
+    return dq, dk, dv

@@ -1,0 +1,214 @@
+// Host side of the C ABI declared in include/attn_bwd.h: argument validation,
+// workspace layout and the launch sequence
+//   schedule -> preprocess -> main (tensor-core or fp32 SIMT) -> reduce/convert
+// on the caller's stream.  Every check runs before the first CUDA call, so an
+// invalid configuration is reported without touching the device (the
+// "return -1" / loud-check convention of aiter PR #2216's follow-up commit
+// and TransformerEngine PR #671's head-dim check).
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+
+#include "common.cuh"
+
+namespace attn {
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool tc_headdims(int dqk, int dv) {
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
+}
+
+static bool simt_headdims(int dqk, int dv) {
+  return dqk >= 4 && dqk <= 64 && dv >= 1 && dv <= 64 && dqk % 4 == 0;
+}
+
+template <typename Prm>
+static int validate_common(const Prm* p) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (p->dtype < ATTN_BF16 || p->dtype > ATTN_FP32) return ATTN_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->nhead_q < 1 || p->nhead_kv < 1) return ATTN_ERR_INVALID_ARG;
+  if (p->nhead_q % p->nhead_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (p->seqlen_q < 0 || p->seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+  const bool gq = p->cu_seqlens_q != nullptr, gk = p->cu_seqlens_k != nullptr;
+  if (gq != gk) return ATTN_ERR_INVALID_ARG;   // group mode needs both seqstart arrays
+  if (gq && (p->total_q < 0 || p->total_k < 0)) return ATTN_ERR_INVALID_ARG;
+  if (p->mask < ATTN_MASK_NONE || p->mask > ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;
+  if (p->mask == ATTN_MASK_WINDOW && (p->window_left < -1 || p->window_right < -1))
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(p->softmax_scale) || p->softmax_scale == 0.f) return ATTN_ERR_INVALID_ARG;
+  if (p->d_qk < 1 || p->d_v < 1) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  // element counts must fit the 32-bit TMA / row coordinates
+  const long long rows_q = gq ? (long long)p->total_q : (long long)p->batch * p->seqlen_q;
+  const long long rows_k = gq ? (long long)p->total_k : (long long)p->batch * p->seqlen_k;
+  if (rows_q > (1LL << 30) || rows_k > (1LL << 30)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+static int validate_bwd(const attn_bwd_params* p) {
+  int st = validate_common(p);
+  if (st != ATTN_OK) return st;
+  if (p->dtype == ATTN_FP32) {
+    if (!simt_headdims(p->d_qk, p->d_v)) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  } else if (!tc_headdims(p->d_qk, p->d_v)) {
+    return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  }
+  const void* ptrs[] = {p->q, p->k, p->v, p->o, p->dout, p->lse, p->dq, p->dk, p->dv};
+  for (const void* x : ptrs)
+    if (!x || !aligned16(x)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+static int validate_fwd(const attn_fwd_params* p) {
+  int st = validate_common(p);
+  if (st != ATTN_OK) return st;
+  if (p->d_qk > 192 || p->d_v > 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  const void* ptrs[] = {p->q, p->k, p->v, p->o, p->lse};
+  for (const void* x : ptrs)
+    if (!x) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+static Problem make_problem(const attn_bwd_params& p, void* ws) {
+  const WsLayout L = ws_layout(p);
+  Problem P{};
+  P.dtype = p.dtype;
+  P.nseg = p.batch;
+  P.hq = p.nhead_q;
+  P.hkv = p.nhead_kv;
+  P.g = p.nhead_q / p.nhead_kv;
+  P.sq = p.seqlen_q;
+  P.sk = p.seqlen_k;
+  P.group = p.cu_seqlens_q != nullptr;
+  P.tq = P.group ? p.total_q : p.batch * p.seqlen_q;
+  P.tk = P.group ? p.total_k : p.batch * p.seqlen_k;
+  P.dqk = p.d_qk;
+  P.dv = p.d_v;
+  P.cu_q = p.cu_seqlens_q;
+  P.cu_k = p.cu_seqlens_k;
+  P.mask = p.mask;
+  P.left = p.mask == ATTN_MASK_WINDOW ? p.window_left : -1;
+  P.right = p.mask == ATTN_MASK_WINDOW ? p.window_right : -1;
+  P.scale = p.softmax_scale;
+  P.scale_log2 = p.softmax_scale * 1.4426950408889634f;
+  P.det = p.deterministic ? 1 : 0;
+  P.nsplits = L.nsplits;
+  P.q = p.q; P.k = p.k; P.v = p.v; P.o = p.o; P.dout = p.dout; P.lse = p.lse;
+  P.dq = p.dq; P.dk = p.dk; P.dv_out = p.dv;
+  char* w = static_cast<char*>(ws);
+  P.hdr = reinterpret_cast<int*>(w + L.off_hdr);
+  P.lse2 = reinterpret_cast<float*>(w + L.off_lse2);
+  P.dvec = reinterpret_cast<float*>(w + L.off_dvec);
+  P.items = reinterpret_cast<int4*>(w + L.off_items);
+  P.max_items = L.max_items;
+  P.dq_acc = reinterpret_cast<float*>(w + L.off_dqacc);
+  P.n_lse = L.n_lse;
+  return P;
+}
+
+static bool log_enabled() {
+  const char* e = std::getenv("ATTN_BWD_LOG");
+  return e && e[0] == '1';
+}
+
+static void log_config(const attn_bwd_params& p, const WsLayout& L) {
+  std::fprintf(stderr,
+               "[attn_bwd] dtype=%d mode=%s batch=%d hq=%d hkv=%d sq=%d sk=%d tq=%d tk=%d d_qk=%d d_v=%d "
+               "mask=%d window=(%d,%d) scale=%g det=%d nsplits=%d items<=%d workspace=%zu\n",
+               p.dtype, p.cu_seqlens_q ? "group" : "batch", p.batch, p.nhead_q, p.nhead_kv, p.seqlen_q,
+               p.seqlen_k, p.total_q, p.total_k, p.d_qk, p.d_v, p.mask, p.window_left, p.window_right,
+               p.softmax_scale, p.deterministic, L.nsplits, L.max_items, L.total);
+}
+
+static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t s,
+               cudaEvent_t* ev /* 4 events or null */) {
+  int st = validate_bwd(p);
+  if (st != ATTN_OK) return st;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*p);
+  if (ws_bytes < L.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (log_enabled()) log_config(*p, L);
+  const Problem P = make_problem(*p, ws);
+  if (ev) cudaEventRecord(ev[0], s);
+  launch_schedule(P, s);
+  launch_preprocess(P, s);
+  if (ev) cudaEventRecord(ev[1], s);
+  if (P.dtype == ATTN_FP32) {
+    launch_bwd_simt(P, s);
+  } else {
+    st = launch_bwd_tc(P, s);
+    if (st != ATTN_OK) return st;
+  }
+  if (ev) cudaEventRecord(ev[2], s);
+  launch_reduce_convert(P, s);
+  if (ev) cudaEventRecord(ev[3], s);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes) {
+  if (!bytes) return ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  const int st = validate_common(p);
+  if (st != ATTN_OK) return st;
+  *bytes = ws_layout(*p).total;
+  return ATTN_OK;
+}
+
+extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  return run(p, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int attn_bwd_timed(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream, float stage_ms[4]) {
+  if (!stage_ms) return ATTN_ERR_INVALID_ARG;
+  int st = validate_bwd(p);
+  if (st != ATTN_OK) return st;
+  cudaEvent_t ev[4];
+  for (int i = 0; i < 4; ++i)
+    if (cudaEventCreate(&ev[i]) != cudaSuccess) return ATTN_ERR_CUDA;
+  st = run(p, workspace, workspace_bytes, stream, ev);
+  if (st == ATTN_OK) {
+    if (cudaEventSynchronize(ev[3]) != cudaSuccess) st = ATTN_ERR_CUDA;
+    cudaEventElapsedTime(&stage_ms[0], ev[0], ev[1]);
+    cudaEventElapsedTime(&stage_ms[1], ev[1], ev[2]);
+    cudaEventElapsedTime(&stage_ms[2], ev[2], ev[3]);
+    cudaEventElapsedTime(&stage_ms[3], ev[0], ev[3]);
+  }
+  for (int i = 0; i < 4; ++i) cudaEventDestroy(ev[i]);
+  return st;
+}
+
+extern "C" int attn_bwd_read_status(const void* workspace, cudaStream_t stream, int* status) {
+  if (!workspace || !status) return ATTN_ERR_INVALID_ARG;
+  int h[HDR_WORDS];
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpy(h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  *status = h[HDR_STATUS];
+  return ATTN_OK;
+}
+
+extern "C" int attn_fwd(const attn_fwd_params* p, cudaStream_t stream) {
+  const int st = validate_fwd(p);
+  if (st != ATTN_OK) return st;
+  launch_fwd(*p, stream);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED_HEADDIM: return "unsupported head dimension for this dtype";
+    case ATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_DEVICE_FLAG: return "device reported an error";
+    case ATTN_ERR_TIMEOUT: return "bounded device wait expired";
+    case ATTN_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with declared bounds";
+    default: return "unknown status";
+  }
+}

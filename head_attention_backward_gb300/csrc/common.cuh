@@ -1,0 +1,220 @@
+// Internal definitions shared by the host launcher and every kernel of the
+// FMHA backward library: the problem descriptor, the workspace layout, the
+// mask / tile-range arithmetic and the index helpers.  One definition of each
+// layout serves the producer and the consumer of every buffer (the THD dQ bug
+// of TransformerEngine PR #671, Root cause, came from two disagreeing ones).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/attn_bwd.h"
+
+namespace attn {
+
+// Tile shape of the backward pass: KV tiles of BN keys own a CTA; query tiles
+// of BM rows stream through it.  nsplits of the deterministic dq_acc
+// workspace is ceil(Sk / BN): one slice per KV tile.
+constexpr int BN = 128;
+constexpr int BM = 64;
+
+// Workspace header words.
+enum HeaderWord : int {
+  HDR_STATUS = 0,     // attn_status_t of the last run (0 = ok)
+  HDR_NITEMS = 1,     // number of work items written by the scheduler
+  HDR_NEXT = 2,       // dynamic work counter of the persistent kernel
+  HDR_DIAG = 3,       // diagnostic word (where a bounded wait expired)
+  HDR_WORDS = 64
+};
+
+struct Problem {
+  // shapes
+  int dtype;
+  int nseg;          // B (batch) or number of segments (group)
+  int hq, hkv, g;    // g = hq / hkv
+  int sq, sk;        // batch: lengths; group: upper bounds
+  int tq, tk;        // group: packed totals
+  int dqk, dv;
+  int group;         // 1 = THD group mode
+  const int* cu_q;
+  const int* cu_k;
+  int mask, left, right;
+  float scale;
+  float scale_log2;  // scale * log2(e)
+  int det;
+  int nsplits;       // dq_acc slices (1 in atomic mode)
+  // tensors
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv_out;
+  // workspace
+  int* hdr;
+  float* lse2;       // LSE * log2(e), +inf for rows without a visible key
+  float* dvec;       // D = rowsum(dO * O)
+  int4* items;       // (segment, kv head, kv tile, unused)
+  int max_items;
+  float* dq_acc;     // [nsplits][rows(lse layout)][dqk]
+  long long n_lse;   // rows of the LSE layout = B*Hq*Sq or Hq*Tq
+};
+
+struct WsLayout {
+  size_t off_hdr, off_lse2, off_dvec, off_items, off_dqacc, total;
+  int max_items, nsplits;
+  long long n_lse;
+};
+
+__host__ __device__ inline long long cdiv_ll(long long a, long long b) { return (a + b - 1) / b; }
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Workspace layout: pure function of the scalar problem fields, used by both
+// attn_bwd_workspace_size and attn_bwd.
+inline WsLayout ws_layout(const attn_bwd_params& p) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  WsLayout L{};
+  const bool group = p.cu_seqlens_q != nullptr;
+  L.n_lse = group ? (long long)p.nhead_q * p.total_q : (long long)p.batch * p.nhead_q * p.seqlen_q;
+  L.nsplits = p.deterministic ? cdiv(p.seqlen_k > 0 ? p.seqlen_k : 1, BN) : 1;
+  long long nkv_tiles;
+  if (group) {
+    long long a = (long long)p.total_k / BN + p.batch;
+    long long b = (long long)p.batch * cdiv(p.seqlen_k > 0 ? p.seqlen_k : 1, BN);
+    nkv_tiles = a < b ? a : b;
+  } else {
+    nkv_tiles = (long long)p.batch * cdiv(p.seqlen_k > 0 ? p.seqlen_k : 1, BN);
+  }
+  L.max_items = (int)(nkv_tiles * p.nhead_kv);
+  size_t o = 0;
+  L.off_hdr = o;   o = up(o + HDR_WORDS * sizeof(int));
+  L.off_lse2 = o;  o = up(o + (size_t)L.n_lse * sizeof(float));
+  L.off_dvec = o;  o = up(o + (size_t)L.n_lse * sizeof(float));
+  L.off_items = o; o = up(o + (size_t)(L.max_items > 0 ? L.max_items : 1) * sizeof(int4));
+  L.off_dqacc = o; o = up(o + (size_t)L.nsplits * (size_t)L.n_lse * p.d_qk * sizeof(float));
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ segments
+
+struct Seg {
+  int q0, lq;   // first packed row and length of the query segment
+  int k0, lk;   // same for keys
+};
+
+__device__ __forceinline__ Seg segment(const Problem& P, int b) {
+  Seg s;
+  if (P.group) {
+    s.q0 = __ldg(P.cu_q + b);
+    s.lq = __ldg(P.cu_q + b + 1) - s.q0;
+    s.k0 = __ldg(P.cu_k + b);
+    s.lk = __ldg(P.cu_k + b + 1) - s.k0;
+  } else {
+    s.q0 = b * P.sq;
+    s.lq = P.sq;
+    s.k0 = b * P.sk;
+    s.lk = P.sk;
+  }
+  return s;
+}
+
+// Row index of (segment b, head h, segment-local query q) in the LSE layout:
+// batch [B][Hq][Sq], group [Hq][Tq].  dq_acc slices use the same row order.
+__device__ __forceinline__ long long lse_row(const Problem& P, int b, int h, const Seg& s, int q) {
+  return P.group ? (long long)h * P.tq + s.q0 + q : ((long long)b * P.hq + h) * P.sq + q;
+}
+
+// ---------------------------------------------------------------------- mask
+// Visibility of segment-local key j to query i (same reading as the header):
+// off = 0 for top-left causal, Lk - Lq for bottom-right causal and window.
+
+struct MaskArgs {
+  int off;     // diagonal offset
+  int left;    // < 0: unbounded
+  int right;   // < 0: unbounded
+};
+
+__host__ __device__ inline MaskArgs mask_args(int mask, int left, int right, int lq, int lk) {
+  MaskArgs m;
+  switch (mask) {
+    case ATTN_MASK_CAUSAL_TOP_LEFT: m.off = 0; m.left = -1; m.right = 0; break;
+    case ATTN_MASK_CAUSAL_BOTTOM_RIGHT: m.off = lk - lq; m.left = -1; m.right = 0; break;
+    case ATTN_MASK_WINDOW: m.off = lk - lq; m.left = left; m.right = right; break;
+    default: m.off = 0; m.left = -1; m.right = -1; break;
+  }
+  return m;
+}
+
+__host__ __device__ inline bool visible(const MaskArgs& m, int i, int j) {
+  const int c = i + m.off;
+  return (m.left < 0 || j >= c - m.left) && (m.right < 0 || j <= c + m.right);
+}
+
+// Range [qt_lo, qt_hi) of BM-row query tiles holding at least one query that
+// sees a key of the BN-key tile kt.  Used by the main kernels (which tiles to
+// visit) and by the dQ reduction (which dq_acc slices were written).
+__host__ __device__ inline void qtile_range(const MaskArgs& m, int lq, int lk, int kt, int& lo, int& hi) {
+  lo = 0;
+  hi = 0;
+  const int k_first = kt * BN;
+  if (lq <= 0 || k_first >= lk) return;
+  int k_last = k_first + BN - 1;
+  if (k_last > lk - 1) k_last = lk - 1;
+  // query i sees key j iff j - off - right <= i (right bounded) and
+  // i <= j - off + left (left bounded)
+  long long qlo = 0, qhi = lq - 1;
+  if (m.right >= 0) {
+    long long v = (long long)k_first - m.off - m.right;
+    if (v > qlo) qlo = v;
+  }
+  if (m.left >= 0) {
+    long long v = (long long)k_last - m.off + m.left;
+    if (v < qhi) qhi = v;
+  }
+  if (qlo > qhi) return;
+  lo = (int)(qlo / BM);
+  hi = (int)(qhi / BM) + 1;
+}
+
+// ------------------------------------------------------------------- types
+
+template <typename T> struct TypeOps;
+template <> struct TypeOps<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+template <> struct TypeOps<__half> {
+  static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+template <> struct TypeOps<float> {
+  static __device__ __forceinline__ float to_f(float x) { return x; }
+  static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+
+__device__ __forceinline__ void set_status(const Problem& P, int code) {
+  atomicCAS(P.hdr + HDR_STATUS, 0, code);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------- kernel entry points
+
+void launch_schedule(const Problem& P, cudaStream_t st);
+void launch_preprocess(const Problem& P, cudaStream_t st);
+void launch_reduce_convert(const Problem& P, cudaStream_t st);
+void launch_bwd_simt(const Problem& P, cudaStream_t st);
+int launch_bwd_tc(const Problem& P, cudaStream_t st);   // returns ATTN_* status
+void launch_fwd(const attn_fwd_params& p, cudaStream_t st);
+
+}  // namespace attn

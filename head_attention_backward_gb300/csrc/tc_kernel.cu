@@ -1,0 +1,632 @@
+// Persistent KV-tile-major FMHA backward on tcgen05 tensor cores (sm_103a).
+//
+// Each CTA (one per SM) takes work items (segment b, kv head, KV tile of
+// BN = 128 keys) from the scheduler's list, keeps that K and V tile in shared
+// memory, and streams the BM = 64-row query tiles of all G query heads of the
+// kv head through it.  Per (query tile, KV tile) pair it recomputes the
+// scores from the stored LSE and runs the five dense products of the
+// softmax-attention gradient, all with the KV tile on the 128 TMEM lanes:
+//
+//   S^T  = K Q^T                 (M = keys,  N = queries, K = d_qk)
+//   dP^T = V dO^T                (M = keys,  N = queries, K = d_v)
+//   P^T  = exp(s S^T - LSE),  dS^T = P^T o (dP^T - D)      (CUDA cores)
+//   dQ^T = K^T dS^T              (M = d_qk,  N = queries, K = keys)
+//   dV  += P^T dO                (M = keys,  N = d_v,     K = queries)
+//   dK  += dS^T Q                (M = keys,  N = d_qk,    K = queries)
+//
+// dK and dV accumulate in TMEM across the item and are written once, scaled;
+// each dQ^T partial is written to the item's slice of the fp32 dq_acc
+// workspace (deterministic mode) or added to the single slice with fp32
+// reductions.  This is the persistent, deterministic split-dQ design of
+// aiter PR #2216 (Motivation) re-derived for TMA + tcgen05 + TMEM.
+//
+// Warp roles (320 threads): warp 0 loads (TMA for Q/dO/K/V plus the LSE/D
+// rows of each query tile) and fetches work items; warp 1 allocates TMEM and
+// one lane issues every MMA; warps 2-5 turn S/dP into P/dS (one key row per
+// thread); warps 6-9 drain dQ partials and the final dK/dV.  Every mbarrier
+// wait is bounded by %globaltimer: on expiry the CTA records ATTN_ERR_TIMEOUT
+// in the workspace header and all roles unwind to a clean TMEM release.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace tc {
+
+using namespace ptx;
+
+constexpr int NUM_THREADS = 320;
+constexpr int NI = 2;                       // work-item ring slots
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct TmaMaps {
+  CUtensorMap q, k, v, dout;
+};
+
+template <int DQK, int DV>
+struct Cfg {
+  static constexpr int NCK = DQK / 64;                  // 64-wide chunks of q/k rows
+  static constexpr int NCV = DV / 64;                   // chunks of v/o rows
+  static constexpr int DQK_PAD = (DQK + 127) / 128 * 128;
+  static constexpr int NCK_PAD = DQK_PAD / 64;          // k chunks incl. zero padding
+  static constexpr int NMB = DQK_PAD / 128;             // M blocks of dQ^T
+  static constexpr int ST = DQK <= 128 ? 3 : 2;         // Q/dO pipeline stages
+  static constexpr int KCH = BN * 128;                  // bytes of one 64-wide k/v chunk
+  static constexpr int QCH = BM * 128;                  // bytes of one 64-wide q/dO chunk
+  // shared memory map (1024-byte aligned regions)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NCK_PAD * KCH;
+  static constexpr int OFF_Q = OFF_V + NCV * KCH;
+  static constexpr int OFF_DO = OFF_Q + ST * NCK * QCH;
+  static constexpr int OFF_P = OFF_DO + ST * NCV * QCH;
+  static constexpr int OFF_DS = OFF_P + BN * BM * 2;
+  static constexpr int OFF_L = OFF_DS + BN * BM * 2;    // [ST][BM] log2 LSE
+  static constexpr int OFF_D = OFF_L + ST * BM * 4;     // [ST][BM] D
+  static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
+  static constexpr int NBAR = 16 + 2 * ST + 2 * NI;
+  static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_MISC = OFF_RING + NI * 16;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  // TMEM column map
+  static constexpr int T_DK = 0;
+  static constexpr int T_DV = DQK;
+  static constexpr int T_S = DQK + DV;
+  static constexpr int T_DP = T_S + BM;
+  static constexpr bool ALIAS = T_DP + BM + NMB * BM > (int)TMEM_COLS;
+  static constexpr int T_DQ = ALIAS ? T_S : T_DP + BM;
+  static_assert(T_DQ + NMB * BM <= (int)TMEM_COLS, "TMEM overflow");
+  static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+  static constexpr uint32_t KV_BYTES = (NCK + NCV) * KCH;
+  static constexpr uint32_t QDO_BYTES = (NCK + NCV) * QCH;
+};
+
+// barrier indices
+enum {
+  B_KV_FULL = 0, B_KV_EMPTY, B_SDP_FULL, B_SDP_EMPTY, B_PDS_FULL, B_PDS_EMPTY,
+  B_DQ_FULL, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_FIXED_END = 16
+};
+
+struct Ctx {
+  uint64_t* bar;
+  int* abort_flag;
+  int* hdr;
+};
+
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity, int where) {
+  const uint32_t a = smem_u32(c.bar + idx);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((++n & 31u) == 0) {
+      if (*(volatile int*)c.abort_flag) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        *(volatile int*)c.abort_flag = 1;
+        atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
+        atomicExch(c.hdr + HDR_DIAG, where);
+        return false;
+      }
+    }
+  }
+}
+
+// Work item and the per-item quantities every role derives identically.
+struct ItemInfo {
+  int b, hk, kt;
+  Seg sg;
+  MaskArgs m;
+  int qlo, nq, nsteps, klen;
+};
+
+__device__ __forceinline__ ItemInfo item_info(const Problem& P, int4 it) {
+  ItemInfo I;
+  I.b = it.x; I.hk = it.y; I.kt = it.z;
+  I.sg = segment(P, I.b);
+  I.m = mask_args(P.mask, P.left, P.right, I.sg.lq, I.sg.lk);
+  int lo, hi;
+  qtile_range(I.m, I.sg.lq, I.sg.lk, I.kt, lo, hi);
+  I.qlo = lo;
+  I.nq = hi - lo;
+  I.nsteps = I.nq * P.g;
+  I.klen = min(BN, I.sg.lk - I.kt * BN);
+  return I;
+}
+
+template <typename T> struct IsHalf { static constexpr bool value = false; };
+template <> struct IsHalf<__half> { static constexpr bool value = true; };
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16*) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int DQK, int DV, typename T>
+__global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_constant__ TmaMaps maps, const Problem P) {
+  using C = Cfg<DQK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  int4* ring = reinterpret_cast<int4*>(smem + C::OFF_RING);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::OFF_MISC + 4);
+  float* sL = reinterpret_cast<float*>(smem + C::OFF_L);
+  float* sD = reinterpret_cast<float*>(smem + C::OFF_D);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Ctx ctx{bar, abort_flag, P.hdr};
+  const int B_Q_FULL = B_FIXED_END, B_Q_EMPTY = B_FIXED_END + C::ST;
+  const int B_IT_FULL = B_FIXED_END + 2 * C::ST, B_IT_EMPTY = B_IT_FULL + NI;
+
+  // zero the k padding chunks read by the dQ^T MMA of padded head dims
+  if (C::NCK_PAD > C::NCK) {
+    uint4* z = reinterpret_cast<uint4*>(smem + C::OFF_K + C::NCK * C::KCH);
+    for (int i = threadIdx.x; i < (C::NCK_PAD - C::NCK) * C::KCH / 16; i += NUM_THREADS)
+      z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar + B_KV_FULL, 1);
+    mbar_init(bar + B_KV_EMPTY, 1);
+    mbar_init(bar + B_SDP_FULL, 1);
+    mbar_init(bar + B_SDP_EMPTY, 4);
+    mbar_init(bar + B_PDS_FULL, 4);
+    mbar_init(bar + B_PDS_EMPTY, 1);
+    mbar_init(bar + B_DQ_FULL, 1);
+    mbar_init(bar + B_DQ_EMPTY, 4);
+    mbar_init(bar + B_DKV_FULL, 1);
+    mbar_init(bar + B_DKV_EMPTY, 4);
+    mbar_init(bar + B_DRAIN, 1);
+    for (int s = 0; s < C::ST; ++s) {
+      mbar_init(bar + B_Q_FULL + s, 32);
+      mbar_init(bar + B_Q_EMPTY + s, 1);
+    }
+    for (int s = 0; s < NI; ++s) {
+      mbar_init(bar + B_IT_FULL + s, 1);
+      mbar_init(bar + B_IT_EMPTY + s, 1 + 4 + 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int nitems = P.hdr[HDR_NITEMS];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.dout);
+    }
+    uint32_t g = 0, it = 0, n_item = 0;
+    while (true) {
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(P.hdr + HDR_NEXT, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const int4 item = idx < nitems ? P.items[idx] : make_int4(-1, 0, 0, 0);
+      const int slot = n_item % NI;
+      if (!wait_bar(ctx, B_IT_EMPTY + slot, ((n_item / NI) & 1) ^ 1, 1)) break;
+      if (lane == 0) {
+        ring[slot] = item;
+        mbar_arrive(bar + B_IT_FULL + slot);
+      }
+      ++n_item;
+      if (item.x < 0) break;
+      const ItemInfo I = item_info(P, item);
+      if (I.nsteps == 0) continue;
+      if (!wait_bar(ctx, B_KV_EMPTY, (it & 1) ^ 1, 2)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar + B_KV_FULL, C::KV_BYTES);
+        const int krow = I.sg.k0 + I.kt * BN;
+        for (int c = 0; c < C::NCK; ++c)
+          tma_load_3d(smem + C::OFF_K + c * C::KCH, &maps.k, bar + B_KV_FULL, c * 64, I.hk, krow);
+        for (int c = 0; c < C::NCV; ++c)
+          tma_load_3d(smem + C::OFF_V + c * C::KCH, &maps.v, bar + B_KV_FULL, c * 64, I.hk, krow);
+      }
+      bool ok = true;
+      for (int s = 0; s < I.nsteps; ++s) {
+        const uint32_t gs = g + s, st = gs % C::ST;
+        const int h = I.hk * P.g + s / I.nq, qt = I.qlo + s % I.nq;
+        if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
+        for (int c = lane; c < BM; c += 32) {
+          const int q = qt * BM + c;
+          float l = INFINITY, d = 0.f;
+          if (q < I.sg.lq) {
+            const long long li = lse_row(P, I.b, h, I.sg, q);
+            l = P.lse2[li];
+            d = P.dvec[li];
+          }
+          sL[st * BM + c] = l;
+          sD[st * BM + c] = d;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar + B_Q_FULL + st, C::QDO_BYTES);
+          const int qrow = I.sg.q0 + qt * BM;
+          for (int c = 0; c < C::NCK; ++c)
+            tma_load_3d(smem + C::OFF_Q + (st * C::NCK + c) * C::QCH, &maps.q, bar + B_Q_FULL + st, c * 64, h, qrow);
+          for (int c = 0; c < C::NCV; ++c)
+            tma_load_3d(smem + C::OFF_DO + (st * C::NCV + c) * C::QCH, &maps.dout, bar + B_Q_FULL + st, c * 64, h,
+                        qrow);
+        } else {
+          mbar_arrive(bar + B_Q_FULL + st);
+        }
+      }
+      if (!ok) break;
+      g += I.nsteps;
+      ++it;
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr bool F16 = IsHalf<T>::value;
+      constexpr uint32_t ID_SDP = idesc_f16(128, BM, false, false, F16);
+      constexpr uint32_t ID_DQ = idesc_f16(128, BM, true, true, F16);
+      constexpr uint32_t ID_DV = idesc_f16(128, DV, false, true, F16);
+      constexpr uint32_t ID_DK = idesc_f16(128, DQK, false, true, F16);
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
+      const uint32_t sP = smem_u32(smem + C::OFF_P), sdS = smem_u32(smem + C::OFF_DS);
+      uint32_t g = 0, it = 0, n_item = 0;
+      bool ok = true;
+      // S^T and dP^T of global step gs (stage st) into TMEM.
+      auto issue_sdp = [&](uint32_t gs) -> bool {
+        const uint32_t st = gs % C::ST;
+        if (!wait_bar(ctx, B_Q_FULL + st, (gs / C::ST) & 1, 10)) return false;
+        if (!wait_bar(ctx, B_SDP_EMPTY, (gs & 1) ^ 1, 11)) return false;
+        if (C::ALIAS && !wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 12)) return false;
+        tc_fence_after();
+        const uint32_t q = sQ + st * C::NCK * C::QCH, d = sdO + st * C::NCV * C::QCH;
+#pragma unroll
+        for (int ks = 0; ks < DQK / 16; ++ks) {
+          const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
+          umma_ss(tmem + C::T_S, sdesc_sw128(sK + off_a, 16, 1024), sdesc_sw128(q + off_b, 16, 1024), ID_SDP, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < DV / 16; ++ks) {
+          const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
+          umma_ss(tmem + C::T_DP, sdesc_sw128(sV + off_a, 16, 1024), sdesc_sw128(d + off_b, 16, 1024), ID_SDP,
+                  ks > 0);
+        }
+        umma_commit(bar + B_SDP_FULL);
+        return true;
+      };
+      while (ok) {
+        const int slot = n_item % NI;
+        if (!wait_bar(ctx, B_IT_FULL + slot, (n_item / NI) & 1, 13)) break;
+        const int4 item = ring[slot];
+        mbar_arrive(bar + B_IT_EMPTY + slot);
+        ++n_item;
+        if (item.x < 0) break;
+        const ItemInfo I = item_info(P, item);
+        if (I.nsteps == 0) continue;
+        if (!wait_bar(ctx, B_KV_FULL, it & 1, 14)) break;
+        if (!(ok = issue_sdp(g))) break;
+        for (int s = 0; s < I.nsteps; ++s) {
+          const uint32_t gs = g + s, st = gs % C::ST;
+          if (!C::ALIAS && s + 1 < I.nsteps && !(ok = issue_sdp(gs + 1))) break;
+          if (!(ok = wait_bar(ctx, B_PDS_FULL, gs & 1, 15))) break;
+          if (!C::ALIAS && !(ok = wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16))) break;
+          tc_fence_after();
+          // dQ^T = K^T dS^T: A = K tile read MN-major, B = dS^T read MN-major
+#pragma unroll
+          for (int mb = 0; mb < C::NMB; ++mb) {
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks) {
+              umma_ss(tmem + C::T_DQ + mb * BM, sdesc_sw128(sK + mb * 2 * C::KCH + ks * 2048, C::KCH, 1024),
+                      sdesc_sw128(sdS + ks * 2048, C::KCH, 1024), ID_DQ, ks > 0);
+            }
+          }
+          umma_commit(bar + B_DQ_FULL);
+          if (s == 0) {
+            if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17))) break;
+            tc_fence_after();
+          }
+          const uint32_t q = sQ + st * C::NCK * C::QCH, d = sdO + st * C::NCV * C::QCH;
+#pragma unroll
+          for (int ks = 0; ks < BM / 16; ++ks)   // dV += P^T dO
+            umma_ss(tmem + C::T_DV, sdesc_sw128(sP + ks * 32, 16, 1024), sdesc_sw128(d + ks * 2048, C::QCH, 1024),
+                    ID_DV, (s > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < BM / 16; ++ks)   // dK += dS^T Q
+            umma_ss(tmem + C::T_DK, sdesc_sw128(sdS + ks * 32, 16, 1024), sdesc_sw128(q + ks * 2048, C::QCH, 1024),
+                    ID_DK, (s > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(bar + B_PDS_EMPTY);
+          umma_commit(bar + B_Q_EMPTY + st);
+          if (C::ALIAS && s + 1 < I.nsteps && !(ok = issue_sdp(gs + 1))) break;
+        }
+        if (!ok) break;
+        g += I.nsteps;
+        umma_commit(bar + B_KV_EMPTY);
+        umma_commit(bar + B_DKV_FULL);
+        ++it;
+      }
+      // make sure no MMA is in flight before TMEM is released
+      umma_commit(bar + B_DRAIN);
+      wait_bar(ctx, B_DRAIN, 0, 18);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------- softmax / dS
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                 // key row = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* pRow = smem + C::OFF_P + r * 128;
+    uint8_t* dsRow = smem + C::OFF_DS + r * 128;
+    uint32_t g = 0, n_item = 0;
+    while (true) {
+      const int slot = n_item % NI;
+      if (!wait_bar(ctx, B_IT_FULL + slot, (n_item / NI) & 1, 20)) break;
+      const int4 item = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + B_IT_EMPTY + slot);
+      ++n_item;
+      if (item.x < 0) break;
+      const ItemInfo I = item_info(P, item);
+      if (I.nsteps == 0) continue;
+      const int kk = I.kt * BN + r;                    // segment-local key index
+      const bool key_ok = r < I.klen;
+      bool ok = true;
+      for (int s = 0; s < I.nsteps; ++s) {
+        const uint32_t gs = g + s, st = gs % C::ST;
+        const int qt = I.qlo + s % I.nq;
+        if (!(ok = wait_bar(ctx, B_SDP_FULL, gs & 1, 21))) break;
+        tc_fence_after();
+        uint32_t sv[BM], dpv[BM];
+        tmem_ld32(lane_addr + C::T_S, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(lane_addr + C::T_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(lane_addr + C::T_DP, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
+        tmem_ld32(lane_addr + C::T_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar + B_SDP_EMPTY);
+        if (!(ok = wait_bar(ctx, B_Q_FULL + st, (gs / C::ST) & 1, 22))) break;
+        const float* lrow = sL + st * BM;
+        const float* drow = sD + st * BM;
+        // whole tile visible and in range: skip the per-element predicate
+        const int q_first = qt * BM, q_last = qt * BM + BM - 1;
+        const int k_first = I.kt * BN, k_last = I.kt * BN + BN - 1;
+        const bool full = I.klen == BN && q_last < I.sg.lq &&
+                          (I.m.right < 0 || k_last <= q_first + I.m.off + I.m.right) &&
+                          (I.m.left < 0 || k_first >= q_last + I.m.off - I.m.left);
+        float pv[BM], dsv[BM];
+#pragma unroll
+        for (int c = 0; c < BM; ++c) {
+          const float l = lrow[c];
+          float p = fast_exp2(fmaf(__uint_as_float(sv[c]), P.scale_log2, -l));
+          if (!full) {
+            const int q = q_first + c;
+            const bool vis = key_ok && q < I.sg.lq && visible(I.m, q, kk);
+            p = vis ? p : 0.f;
+          }
+          pv[c] = p;
+          dsv[c] = p * (__uint_as_float(dpv[c]) - drow[c]);
+        }
+        if (!(ok = wait_bar(ctx, B_PDS_EMPTY, (gs & 1) ^ 1, 23))) break;
+#pragma unroll
+        for (int ch = 0; ch < BM / 8; ++ch) {
+          const int sw = ((ch ^ (r & 7)) << 4);
+          uint4 a, b;
+          a.x = pack2(pv[8 * ch + 0], pv[8 * ch + 1], (T*)nullptr);
+          a.y = pack2(pv[8 * ch + 2], pv[8 * ch + 3], (T*)nullptr);
+          a.z = pack2(pv[8 * ch + 4], pv[8 * ch + 5], (T*)nullptr);
+          a.w = pack2(pv[8 * ch + 6], pv[8 * ch + 7], (T*)nullptr);
+          b.x = pack2(dsv[8 * ch + 0], dsv[8 * ch + 1], (T*)nullptr);
+          b.y = pack2(dsv[8 * ch + 2], dsv[8 * ch + 3], (T*)nullptr);
+          b.z = pack2(dsv[8 * ch + 4], dsv[8 * ch + 5], (T*)nullptr);
+          b.w = pack2(dsv[8 * ch + 6], dsv[8 * ch + 7], (T*)nullptr);
+          *reinterpret_cast<uint4*>(pRow + sw) = a;
+          *reinterpret_cast<uint4*>(dsRow + sw) = b;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar + B_PDS_FULL);
+      }
+      if (!ok) break;
+      g += I.nsteps;
+    }
+  } else {
+    // ------------------------------------------------------ dQ / dK / dV out
+    const int quarter = warp & 3;
+    const int L = quarter * 32 + lane;                 // TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    T* dKg = static_cast<T*>(P.dk);
+    T* dVg = static_cast<T*>(P.dv_out);
+    const long long slice = P.n_lse * DQK;
+    uint32_t g = 0, it = 0, n_item = 0;
+    while (true) {
+      const int slot = n_item % NI;
+      if (!wait_bar(ctx, B_IT_FULL + slot, (n_item / NI) & 1, 30)) break;
+      const int4 item = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + B_IT_EMPTY + slot);
+      ++n_item;
+      if (item.x < 0) break;
+      const ItemInfo I = item_info(P, item);
+      const long long krow = (long long)(I.sg.k0 + I.kt * BN + L) * P.hkv + I.hk;
+      if (I.nsteps == 0) {
+        if (L < I.klen) {
+          for (int e = 0; e < DQK; ++e) dKg[krow * DQK + e] = TypeOps<T>::from_f(0.f);
+          for (int e = 0; e < DV; ++e) dVg[krow * DV + e] = TypeOps<T>::from_f(0.f);
+        }
+        continue;
+      }
+      float* acc = P.dq_acc + (P.det ? (long long)I.kt * slice : 0);
+      bool ok = true;
+      for (int s = 0; s < I.nsteps; ++s) {
+        const uint32_t gs = g + s;
+        const int h = I.hk * P.g + s / I.nq, qt = I.qlo + s % I.nq;
+        if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
+        tc_fence_after();
+        uint32_t v[C::NMB][BM];
+#pragma unroll
+        for (int mb = 0; mb < C::NMB; ++mb) {
+          tmem_ld32(lane_addr + C::T_DQ + mb * BM, *reinterpret_cast<uint32_t(*)[32]>(&v[mb][0]));
+          tmem_ld32(lane_addr + C::T_DQ + mb * BM + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[mb][32]));
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
+        const int nvalid = min(BM, I.sg.lq - qt * BM);
+        const long long row0 = lse_row(P, I.b, h, I.sg, qt * BM);
+#pragma unroll
+        for (int mb = 0; mb < C::NMB; ++mb) {
+          const int e = mb * 128 + L;
+          if (e >= DQK) continue;
+          float* dst = acc + row0 * DQK + e;
+#pragma unroll
+          for (int c = 0; c < BM; ++c) {
+            if (c < nvalid) {
+              if (P.det) dst[(long long)c * DQK] = __uint_as_float(v[mb][c]);
+              else atomicAdd(dst + (long long)c * DQK, __uint_as_float(v[mb][c]));
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      g += I.nsteps;
+      if (!wait_bar(ctx, B_DKV_FULL, it & 1, 32)) break;
+      tc_fence_after();
+      const bool row_ok = L < I.klen;
+#pragma unroll 1
+      for (int ch = 0; ch < DQK / 32; ++ch) {
+        uint32_t x[32];
+        tmem_ld32(lane_addr + C::T_DK + ch * 32, x);
+        tmem_wait_ld();
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dKg + krow * DQK + ch * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(x[8 * j + 0]) * P.scale, __uint_as_float(x[8 * j + 1]) * P.scale, (T*)nullptr);
+            w.y = pack2(__uint_as_float(x[8 * j + 2]) * P.scale, __uint_as_float(x[8 * j + 3]) * P.scale, (T*)nullptr);
+            w.z = pack2(__uint_as_float(x[8 * j + 4]) * P.scale, __uint_as_float(x[8 * j + 5]) * P.scale, (T*)nullptr);
+            w.w = pack2(__uint_as_float(x[8 * j + 6]) * P.scale, __uint_as_float(x[8 * j + 7]) * P.scale, (T*)nullptr);
+            dst[j] = w;
+          }
+        }
+      }
+#pragma unroll 1
+      for (int ch = 0; ch < DV / 32; ++ch) {
+        uint32_t x[32];
+        tmem_ld32(lane_addr + C::T_DV + ch * 32, x);
+        tmem_wait_ld();
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dVg + krow * DV + ch * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(x[8 * j + 0]), __uint_as_float(x[8 * j + 1]), (T*)nullptr);
+            w.y = pack2(__uint_as_float(x[8 * j + 2]), __uint_as_float(x[8 * j + 3]), (T*)nullptr);
+            w.z = pack2(__uint_as_float(x[8 * j + 4]), __uint_as_float(x[8 * j + 5]), (T*)nullptr);
+            w.w = pack2(__uint_as_float(x[8 * j + 6]), __uint_as_float(x[8 * j + 7]), (T*)nullptr);
+            dst[j] = w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + B_DKV_EMPTY);
+      ++it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D view (dim, heads, rows) of a contiguous [rows, heads, dim] 16-bit
+// tensor; boxes of 64 x 1 x box_rows with 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, bool fp16, int dim, int heads, long long rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int DQK, int DV, typename T>
+static int launch_typed(const Problem& P, cudaStream_t st) {
+  using C = Cfg<DQK, DV>;
+  const bool fp16 = IsHalf<T>::value;
+  TmaMaps maps;
+  const long long rq = P.group ? P.tq : (long long)P.nseg * P.sq;
+  const long long rk = P.group ? P.tk : (long long)P.nseg * P.sk;
+  if (!make_map(&maps.q, P.q, fp16, DQK, P.hq, rq, BM) || !make_map(&maps.dout, P.dout, fp16, DV, P.hq, rq, BM) ||
+      !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, BN) || !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, BN))
+    return ATTN_ERR_CUDA;
+  auto kern = bwd_tc_kernel<DQK, DV, T>;
+  // at least 120 KB so that two CTAs never share an SM (each holds all 512 TMEM columns)
+  const int smem = C::SMEM_BYTES > 120 * 1024 ? C::SMEM_BYTES : 120 * 1024;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int grid = sms > 0 ? sms : 1;
+  if (P.max_items < grid) grid = P.max_items;
+  if (grid <= 0) return ATTN_OK;
+  kern<<<grid, NUM_THREADS, smem, st>>>(maps, P);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <typename T>
+static int launch_dims(const Problem& P, cudaStream_t st) {
+  if (P.dqk == 128 && P.dv == 128) return launch_typed<128, 128, T>(P, st);
+  if (P.dqk == 64 && P.dv == 64) return launch_typed<64, 64, T>(P, st);
+  if (P.dqk == 192 && P.dv == 128) return launch_typed<192, 128, T>(P, st);
+  return ATTN_ERR_UNSUPPORTED_HEADDIM;
+}
+
+}  // namespace tc
+
+int launch_bwd_tc(const Problem& P, cudaStream_t st) {
+  if (P.dtype == ATTN_FP16) return tc::launch_dims<__half>(P, st);
+  return tc::launch_dims<__nv_bfloat16>(P, st);
+}
+
+}  // namespace attn

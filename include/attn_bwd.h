@@ -1,0 +1,177 @@
+/*
+ * attn_bwd.h - C ABI of the GB300 (sm_103a) fused multi-head attention
+ * backward pass.
+ *
+ * Given Q, K, V, the forward output O, the upstream gradient dO and the
+ * forward log-sum-exp LSE, attn_bwd computes dQ, dK and dV of softmax
+ * attention.  The operation is the FMHA backward whose deterministic,
+ * split-dQ persistent-kernel path is described in ROCm/aiter PR #2216
+ * ("[CK_TILE] FMHA BWD Use Persistent Kernels in Deterministic Mode",
+ * Motivation), behind a sizing call plus an execute call on one opaque
+ * workspace as in that PR's follow-up commit "[CK_TILE] mha bwd: adapt to CK
+ * #6152 unified workspace API".  Batch and group (THD, packed ragged) modes
+ * follow ROCm/TransformerEngine PR #446 (the batch/group seqstart setup in
+ * ck_fused_attn_bwd.cpp) and PR #671 (Summary, Root cause).
+ *
+ * Conventions
+ * -----------
+ * - Every pointer named "device" is a CUDA device pointer owned by the
+ *   caller; the library allocates nothing and keeps no per-device state.
+ * - All work is enqueued on the caller's stream; no call synchronises the
+ *   host except attn_bwd_read_status and attn_bwd_timed.
+ * - Return value: ATTN_OK (0) on success, a negative attn_status_t otherwise.
+ *   Arguments are validated before anything is launched; an unsupported or
+ *   inconsistent configuration is rejected, never computed silently
+ *   (aiter PR #2216 follow-up: "LOG_ERROR + return -1" on missing group
+ *   pointers; TransformerEngine PR #671: a hard head-dim check instead of a
+ *   silent hard-coded size).
+ * - Tensors are contiguous.  Batch mode (cu_seqlens_q == cu_seqlens_k ==
+ *   NULL): q [B,Sq,Hq,d_qk], k [B,Sk,Hkv,d_qk], v [B,Sk,Hkv,d_v],
+ *   o/dout/dq [B,Sq,Hq,·], dk/dv like k/v, lse [B,Hq,Sq].  Group mode:
+ *   q [Tq,Hq,d_qk], k [Tk,Hkv,d_qk], v [Tk,Hkv,d_v], lse [Hq,Tq]; segment b
+ *   owns rows cu_seqlens_q[b]..cu_seqlens_q[b+1] and keys
+ *   cu_seqlens_k[b]..cu_seqlens_k[b+1] and attends only within itself.
+ * - Query head h reads kv head h / (Hq / Hkv) (GQA, contiguous groups).
+ * - LSE is the natural-log log-sum-exp of the scaled scores, fp32; -inf
+ *   marks a row with no visible key (its gradients are zero).
+ */
+#ifndef ATTN_BWD_H_
+#define ATTN_BWD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1,         /* null pointer, bad size, bad enum, misaligned */
+  ATTN_ERR_UNSUPPORTED_HEADDIM = -2, /* (d_qk, d_v) not built for this dtype       */
+  ATTN_ERR_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < attn_bwd_workspace_size   */
+  ATTN_ERR_CUDA = -4,                /* a CUDA runtime/driver call failed           */
+  ATTN_ERR_DEVICE_FLAG = -5,         /* kernels reported an error (see read_status) */
+  ATTN_ERR_TIMEOUT = -6,             /* a bounded in-kernel wait expired            */
+  ATTN_ERR_BAD_SEQLENS = -7          /* cu_seqlens not monotone / exceed the bounds */
+} attn_status_t;
+
+/* Mask kinds: the AITER mask enum reviewed in TransformerEngine PR #446
+ * (ck_to_aiter_mask_type).  With off = 0 for TOP_LEFT and off = Lk - Lq for
+ * BOTTOM_RIGHT and WINDOW (per segment), key j is visible to query i iff
+ *   CAUSAL_*: j <= i + off
+ *   WINDOW:   i + off - window_left <= j <= i + off + window_right
+ * (inclusive; a negative bound means unbounded on that side). */
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL_TOP_LEFT = 1,
+  ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2,
+  ATTN_MASK_WINDOW = 3
+} attn_mask_t;
+
+/* Element type of q, k, v, o, dout, dq, dk, dv (lse is always fp32).
+ * Supported head dims: BF16/FP16 (d_qk, d_v) in {(64,64), (128,128),
+ * (192,128)} on the tensor-core kernel; FP32 any d_qk, d_v in [1, 128]
+ * on the fp32 SIMT kernel. */
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1, ATTN_FP32 = 2 } attn_dtype_t;
+
+typedef struct {
+  int32_t dtype;          /* attn_dtype_t                                          */
+  int32_t batch;          /* batch mode: B; group mode: number of segments         */
+  int32_t nhead_q;        /* Hq                                                    */
+  int32_t nhead_kv;       /* Hkv, Hq % Hkv == 0                                    */
+  int32_t seqlen_q;       /* batch: Sq; group: upper bound on every query segment  */
+  int32_t seqlen_k;       /* batch: Sk; group: upper bound on every key segment    */
+  int32_t total_q;        /* group mode: Tq = cu_seqlens_q[batch]; ignored in batch */
+  int32_t total_k;        /* group mode: Tk = cu_seqlens_k[batch]; ignored in batch */
+  int32_t d_qk;           /* head dim of q and k                                   */
+  int32_t d_v;            /* head dim of v and o                                   */
+  const int32_t* cu_seqlens_q; /* device, [batch+1], or NULL (batch mode)          */
+  const int32_t* cu_seqlens_k; /* device, [batch+1], or NULL (batch mode)          */
+  int32_t mask;           /* attn_mask_t                                           */
+  int32_t window_left;    /* ATTN_MASK_WINDOW only; -1 = unbounded                 */
+  int32_t window_right;   /* ATTN_MASK_WINDOW only; -1 = unbounded                 */
+  float softmax_scale;    /* s in S = s * Q K^T                                    */
+  int32_t deterministic;  /* 1: split dq_acc + fixed-order reduction (bitwise
+                             repeatable); 0: fp32 atomic accumulation           */
+  const void* q;          /* device inputs, layouts above                          */
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;       /* device, fp32 natural log                              */
+  void* dq;               /* device outputs, same dtype as q; fully overwritten    */
+  void* dk;
+  void* dv;
+} attn_bwd_params;
+
+/* Forward helper that produces O and LSE for benchmark and test inputs
+ * (the forward pass implied by TransformerEngine PR #446's ck_attn_fwd).
+ * Same field meanings as attn_bwd_params; o and lse are outputs. */
+typedef struct {
+  int32_t dtype;
+  int32_t batch;
+  int32_t nhead_q;
+  int32_t nhead_kv;
+  int32_t seqlen_q;
+  int32_t seqlen_k;
+  int32_t total_q;
+  int32_t total_k;
+  int32_t d_qk;
+  int32_t d_v;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int32_t mask;
+  int32_t window_left;
+  int32_t window_right;
+  float softmax_scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;                /* device output [.., Hq, d_v], dtype                    */
+  float* lse;             /* device output, fp32 natural log                       */
+} attn_fwd_params;
+
+/* Workspace bytes attn_bwd needs for *p.  Pure host arithmetic on the scalar
+ * fields (no device access, no GPU probe), using the same layout function as
+ * attn_bwd, so the sizing and the launch cannot disagree (the sizing-pass
+ * lesson of TransformerEngine PR #671, review reply on is_v3_api_check).
+ * In deterministic mode the workspace holds nsplits = ceil(seqlen_k / 128)
+ * fp32 dq_acc slices of [B][Hq][Sq][d_qk] (group mode: [Hq][Tq][d_qk], row =
+ * packed token, the fp32-packed layout of PR #671, Root cause), otherwise one.
+ * Writes the size to *bytes.  Returns ATTN_OK or an error code. */
+int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes);
+
+/* Enqueue the backward pass on `stream`.  `workspace` is a device buffer of
+ * at least attn_bwd_workspace_size bytes, 256-byte aligned; its contents on
+ * entry are irrelevant (the library initialises what it needs) and it must
+ * not be used by another attn_bwd call in flight.  dq, dk, dv are fully
+ * overwritten.  Invalid arguments return an error before any launch;
+ * problems found on the device (cu_seqlens inconsistent with the declared
+ * bounds, an expired wait) are recorded in the workspace and returned by
+ * attn_bwd_read_status. */
+int attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+             cudaStream_t stream);
+
+/* attn_bwd plus CUDA-event timing of its stages; synchronises `stream`
+ * before returning.  stage_ms[0] = schedule + preprocess, [1] = main kernel,
+ * [2] = dQ reduce/convert, [3] = the whole call. */
+int attn_bwd_timed(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream, float stage_ms[4]);
+
+/* Synchronise `stream` and return the device status word of the last
+ * attn_bwd run on `workspace` (ATTN_OK or an attn_status_t) in *status. */
+int attn_bwd_read_status(const void* workspace, cudaStream_t stream, int* status);
+
+/* Enqueue the forward helper on `stream`. */
+int attn_fwd(const attn_fwd_params* p, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTN_BWD_H_ */

@@ -1,0 +1,180 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/attn_bwd.h declares, its ctypes mirrors match the C structs, the
+workspace sizing is right, and every invalid configuration is rejected with
+its error code before anything touches the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from head_attention_backward_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_bwd.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(attn_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(B.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _c_layout():
+    """sizeof / offsetof of the header's structs, from the C compiler."""
+    prog = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "attn_bwd.h"
+#define F(S, m) printf(#S "." #m " %zu\n", offsetof(S, m));
+int main(void) {
+  printf("attn_bwd_params.size %zu\n", sizeof(attn_bwd_params));
+  printf("attn_fwd_params.size %zu\n", sizeof(attn_fwd_params));
+  F(attn_bwd_params, cu_seqlens_q) F(attn_bwd_params, mask) F(attn_bwd_params, softmax_scale)
+  F(attn_bwd_params, deterministic) F(attn_bwd_params, q) F(attn_bwd_params, lse) F(attn_bwd_params, dv)
+  F(attn_fwd_params, cu_seqlens_k) F(attn_fwd_params, softmax_scale) F(attn_fwd_params, q) F(attn_fwd_params, lse)
+  return 0;
+}
+"""
+    tmp = os.path.join(ROOT, "head_attention_backward_gb300", "_build")
+    os.makedirs(tmp, exist_ok=True)
+    c = os.path.join(tmp, "layout.c")
+    exe = os.path.join(tmp, "layout")
+    open(c, "w").write(prog)
+    cuda_inc = "/usr/local/cuda/include"
+    r = subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, c, "-o", exe],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("gcc/CUDA headers unavailable: " + r.stderr[:200])
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    return {k: int(v) for k, v in (line.split() for line in out.strip().splitlines())}
+
+
+def test_ctypes_structs_match_c_layout():
+    lay = _c_layout()
+    assert lay["attn_bwd_params.size"] == ctypes.sizeof(B.AttnBwdParams)
+    assert lay["attn_fwd_params.size"] == ctypes.sizeof(B.AttnFwdParams)
+    for key, off in lay.items():
+        s, m = key.split(".")
+        if m == "size":
+            continue
+        cls = B.AttnBwdParams if s == "attn_bwd_params" else B.AttnFwdParams
+        assert getattr(cls, m).offset == off, key
+
+
+def make(**kw):
+    p = B.AttnBwdParams()
+    base = dict(dtype=B.ATTN_BF16, batch=2, nhead_q=32, nhead_kv=8, seqlen_q=4096, seqlen_k=4096,
+                total_q=0, total_k=0, d_qk=128, d_v=128, mask=1, window_left=-1, window_right=-1,
+                softmax_scale=0.088, deterministic=1)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    # fake, 16-byte aligned addresses: validation never dereferences them
+    for i, name in enumerate(["q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv"]):
+        if getattr(p, name) is None and name not in kw:
+            setattr(p, name, 0x10000 * (i + 1))
+    return p
+
+
+def test_workspace_size_deterministic_holds_all_splits(lib):
+    st, n = B.attn_bwd_workspace_size(make())
+    assert st == 0
+    nsplits = 4096 // 128
+    dq_acc = nsplits * 2 * 32 * 4096 * 128 * 4
+    assert dq_acc <= n < dq_acc + 16 * 2**20
+
+
+def test_workspace_size_atomic_one_slice(lib):
+    st, n = B.attn_bwd_workspace_size(make(deterministic=0))
+    assert st == 0
+    one = 2 * 32 * 4096 * 128 * 4
+    assert one <= n < one + 16 * 2**20
+
+
+def test_workspace_size_group_mode(lib):
+    p = make(deterministic=1, batch=3, seqlen_q=300, seqlen_k=300, total_q=700, total_k=700)
+    p.cu_seqlens_q = 0x1000
+    p.cu_seqlens_k = 0x2000
+    st, n = B.attn_bwd_workspace_size(p)
+    assert st == 0
+    nsplits = (300 + 127) // 128
+    assert n >= nsplits * 32 * 700 * 128 * 4
+
+
+def test_workspace_size_is_pure_host_arithmetic(lib):
+    # same answer twice and for null tensor pointers: no device access involved
+    p = make()
+    for name in ["q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv"]:
+        setattr(p, name, None)
+    a = B.attn_bwd_workspace_size(p)
+    b = B.attn_bwd_workspace_size(make())
+    assert a == b and a[0] == 0
+
+
+ERR = dict(inv=-1, hd=-2, ws=-3)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nhead_q=30, nhead_kv=8), "inv"),
+    (dict(batch=0), "inv"),
+    (dict(dtype=7), "inv"),
+    (dict(mask=9), "inv"),
+    (dict(mask=3, window_left=-2), "inv"),
+    (dict(softmax_scale=float("nan")), "inv"),
+    (dict(seqlen_q=-1), "inv"),
+    (dict(d_qk=96, d_v=96), "hd"),
+    (dict(d_qk=128, d_v=64), "hd"),
+    (dict(dtype=B.ATTN_FP32, d_qk=128, d_v=128), "hd"),
+    (dict(q=None), "inv"),
+    (dict(dq=0x10008), "inv"),          # not 16-byte aligned
+])
+def test_invalid_arguments_rejected_before_launch(lib, kw, code):
+    p = make(**kw)
+    st = B.attn_bwd(p, 0x100000, 1 << 40, 0)
+    assert st == ERR[code], (kw, st)
+
+
+def test_group_mode_needs_both_seqstart_arrays(lib):
+    p = make(total_q=100, total_k=100)
+    p.cu_seqlens_q = 0x1000           # cu_seqlens_k left NULL
+    assert B.attn_bwd_workspace_size(p)[0] == -1
+    assert B.attn_bwd(p, 0x100000, 1 << 40, 0) == -1
+
+
+def test_workspace_too_small_and_misaligned(lib):
+    p = make()
+    _, need = B.attn_bwd_workspace_size(p)
+    assert B.attn_bwd(p, 0x100000, need - 1, 0) == -3
+    assert B.attn_bwd(p, 0x100010, need, 0) == -1      # not 256-byte aligned
+    assert B.attn_bwd(p, None, need, 0) == -1
+
+
+def test_null_params_and_status_strings(lib):
+    assert lib.attn_bwd(None, None, 0, None) == -1
+    n = ctypes.c_size_t(1)
+    assert lib.attn_bwd_workspace_size(None, ctypes.byref(n)) == -1 and n.value == 0
+    for code in [0, -1, -2, -3, -4, -5, -6, -7]:
+        s = B.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert B.attn_status_string(-99) == "unknown status"
+
+
+def test_fwd_rejects_bad_args(lib):
+    p = B.AttnFwdParams()
+    p.dtype, p.batch, p.nhead_q, p.nhead_kv, p.seqlen_q, p.seqlen_k = 0, 1, 4, 3, 16, 16
+    p.d_qk, p.d_v, p.softmax_scale = 64, 64, 0.1
+    assert B.attn_fwd(p, 0) == -1          # 4 % 3 != 0
+    p.nhead_kv = 2
+    assert B.attn_fwd(p, 0) == -1          # null pointers
+    p.q, p.k, p.v, p.o, p.lse = 0x1000, 0x2000, 0x3000, 0x4000, 0x5000
+    p.d_qk = 256
+    assert B.attn_fwd(p, 0) == -2

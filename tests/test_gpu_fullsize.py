@@ -1,0 +1,107 @@
+"""The benchmark workloads at full size, in the benchmark's launch
+configuration (GPU forward, then attn_bwd through the C ABI), checked on
+sampled rows that the fp64 oracle recomputes from Q, K, V and dO alone.
+Packed THD workloads are checked segment by segment, every segment."""
+import numpy as np
+import pytest
+import torch
+
+from head_attention_backward_gb300 import workloads as W
+from oracle import attn_ref as R
+from tests.parity import assert_all_ok, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from head_attention_backward_gb300 import build, binding
+    build.build_library()
+    binding.load()
+    return binding
+
+
+def _rows(n, rng, k=6):
+    base = {0, 1, 63, 64, 127, 128, n // 2, n - 1}
+    base |= set(int(v) for v in rng.integers(0, n, size=k))
+    return sorted(r for r in base if 0 <= r < n)
+
+
+def _run(B, wl, det):
+    x = wl.inputs()
+    cu = wl.cu_seqlens()
+    d = {k: v.cuda() for k, v in x.items()}
+    cu_d = None if cu is None else cu.cuda()
+    kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
+              cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+    o, lse = B.attn_forward(d["q"], d["k"], d["v"], **kw)
+    got = B.attn_backward(d["q"], d["k"], d["v"], o, d["do"], lse, deterministic=det, **kw)
+    torch.cuda.synchronize()
+    return x, cu, [t.cpu() for t in got]
+
+
+def _check_batch(wl, x, got, heads, kv_heads, seed):
+    rng = np.random.default_rng(seed)
+    okw = dict(mask=wl.mask, left=wl.left, right=wl.right)
+    dq, dk, dv = got
+    gq, rq, gk, rk, gv, rv = [], [], [], [], [], []
+    for b, h in heads:
+        rows = _rows(wl.sq, rng)
+        rq.append(R.dq_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, h, rows, **okw))
+        gq.append(dq[b, rows, h])
+    for b, hk in kv_heads:
+        rows = _rows(wl.sk, rng)
+        ek, ev = R.dkv_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, hk, rows, **okw)
+        rk.append(ek); rv.append(ev)
+        gk.append(dk[b, rows, hk]); gv.append(dv[b, rows, hk])
+    reps = []
+    for name, g, r in (("dq", gq, rq), ("dk", gk, rk), ("dv", gv, rv)):
+        rep = compare(torch.cat(g), torch.cat(r), 2e-2, 0.9999)
+        rep["tensor"] = name
+        reps.append(rep)
+    return reps
+
+
+def test_mha_causal_B4_H16_S2048(B):
+    wl = W.mha_causal()
+    for det in (False, True):
+        x, _, got = _run(B, wl, det)
+        assert_all_ok(_check_batch(wl, x, got, [(0, 0), (3, 15), (1, 7)], [(0, 0), (3, 15)], 1), f"det={det}")
+
+
+def test_gqa_causal_det_B2_Hq32_Hkv8_S4096(B):
+    wl = W.gqa_causal_det()
+    x, _, got = _run(B, wl, True)
+    assert_all_ok(_check_batch(wl, x, got, [(0, 0), (1, 31), (0, 13)], [(0, 0), (1, 7)], 2), "gqa det")
+
+
+@pytest.mark.parametrize("det", [True, False], ids=["det", "atomic"])
+def test_window_dqk192_dv128_S8192(B, det):
+    wl = W.window_192(deterministic=det)
+    x, _, got = _run(B, wl, det)
+    assert_all_ok(_check_batch(wl, x, got, [(0, 0), (0, 15)], [(0, 5)], 5), f"window det={det}")
+
+
+@pytest.mark.parametrize("det", [False, True], ids=["atomic", "det"])
+def test_thd_packed_T16384_every_segment(B, det):
+    wl = W.thd_packed(deterministic=det)
+    x, cu, (dq, dk, dv) = _run(B, wl, det)
+    cu = cu.tolist()
+    rng = np.random.default_rng(4)
+    okw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cu)
+    reps = []
+    for b in range(len(cu) - 1):
+        n = cu[b + 1] - cu[b]
+        rows = _rows(n, rng, k=4)
+        h = int(rng.integers(0, wl.hq))
+        hk = int(rng.integers(0, wl.hkv))
+        rq = R.dq_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, h, rows, **okw)
+        ek, ev = R.dkv_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, hk, rows, **okw)
+        idx = torch.tensor(rows) + cu[b]
+        for name, g, r in (("dq", dq[idx, h], rq), ("dk", dk[idx, hk], ek), ("dv", dv[idx, hk], ev)):
+            rep = compare(g, r, 2e-2, 0.9999)
+            rep.update(tensor=name, segment=b, length=n)
+            reps.append(rep)
+    assert_all_ok(reps, f"thd det={det}")

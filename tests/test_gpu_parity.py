@@ -1,0 +1,202 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every element; they span several KV and query tiles with
+ragged tails.  Packed THD cases are compared segment by segment (the failure
+mode of TransformerEngine PR #671: first segment right, later ones garbage).
+Full-size workloads are checked on sampled rows the oracle recomputes from
+Q, K, V and dO alone (tests/test_gpu_fullsize.py).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from head_attention_backward_gb300 import workloads as W
+from oracle import attn_ref as R
+from tests.parity import assert_all_ok, compare, per_segment_report, tolerances
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from head_attention_backward_gb300 import build, binding
+    build.build_library()
+    binding.load()
+    return binding
+
+
+def _wl(name, dtype, b, hq, hkv, s_q, s_k, dqk, dv, mask, left=-1, right=-1, seed=0, seqlens=None):
+    return W.Workload(name, dtype, b, hq, hkv, s_q, s_k, dqk, dv, mask, left, right, False, seed,
+                      seqlens)
+
+
+def run_backward_vs_oracle(B, wl, deterministic, ref_fwd=True):
+    """Oracle forward -> rounded O / fp32 LSE -> GPU backward and oracle backward
+    on identical inputs; returns reports per tensor (and per segment)."""
+    x = wl.inputs()
+    cu = wl.cu_seqlens()
+    kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cu)
+    o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, **kw)
+    o_in, lse_in = o64.to(wl.dtype), lse64.to(torch.float32)
+    ref = R.attn_backward(x["q"], x["k"], x["v"], o_in, x["do"], lse_in, wl.scale, **kw)
+    dev = {k: v.cuda() for k, v in x.items()}
+    cu_d = None if cu is None else cu.cuda()
+    got = B.attn_backward(dev["q"], dev["k"], dev["v"], o_in.cuda(), dev["do"], lse_in.cuda(),
+                          scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right,
+                          deterministic=deterministic, cu_seqlens_q=cu_d, cu_seqlens_k=cu_d,
+                          max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+    torch.cuda.synchronize()
+    tol, mcos = tolerances(wl.dtype)
+    reps = []
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        g = g.cpu()
+        rep = compare(g, r, tol, mcos)
+        rep["tensor"] = name
+        reps.append(rep)
+        if cu is not None:
+            reps.extend(per_segment_report(g, r, cu.tolist(), name, tol, mcos))
+    return reps
+
+
+SMALL = [
+    _wl("fp32_tiny", torch.float32, 1, 2, 2, 64, 64, 32, 32, W.MASK_NONE, seed=0),
+    _wl("fp32_causal_ragged", torch.float32, 2, 2, 1, 150, 150, 64, 64, W.MASK_CAUSAL_TOP_LEFT, seed=1),
+    _wl("bf16_causal_ragged", torch.bfloat16, 2, 2, 2, 300, 300, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=2),
+    _wl("bf16_gqa_causal", torch.bfloat16, 1, 4, 2, 257, 257, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=3),
+    _wl("bf16_nomask_sq_ne_sk", torch.bfloat16, 1, 2, 1, 200, 333, 128, 128, W.MASK_NONE, seed=4),
+    _wl("bf16_causal_br_long_k", torch.bfloat16, 1, 2, 2, 100, 300, 128, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, seed=5),
+    _wl("bf16_causal_br_short_k", torch.bfloat16, 1, 2, 2, 300, 100, 128, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, seed=6),
+    _wl("bf16_causal_tl_long_k", torch.bfloat16, 1, 2, 2, 100, 300, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=7),
+    _wl("bf16_window_left", torch.bfloat16, 1, 2, 2, 520, 520, 128, 128, W.MASK_WINDOW, 100, 0, seed=8),
+    _wl("bf16_window_lr", torch.bfloat16, 1, 2, 1, 300, 350, 128, 128, W.MASK_WINDOW, 30, 20, seed=9),
+    _wl("bf16_d64_causal", torch.bfloat16, 2, 2, 1, 200, 200, 64, 64, W.MASK_CAUSAL_TOP_LEFT, seed=10),
+    _wl("bf16_d192_window", torch.bfloat16, 1, 2, 2, 400, 400, 192, 128, W.MASK_WINDOW, 150, 0, seed=11),
+    _wl("fp16_causal", torch.float16, 1, 2, 2, 200, 200, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=12),
+]
+
+
+@pytest.mark.parametrize("det", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_small_backward(B, wl, det):
+    assert_all_ok(run_backward_vs_oracle(B, wl, det), wl.name)
+
+
+@pytest.mark.parametrize("det", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("segs", W.PAGE_SPLITS + [[1, 1, 130, 1], [5, 0, 7], [2048]], ids=str)
+def test_thd_splits_per_segment(B, segs, det):
+    """Packed THD, padding-causal within segments, llama3-shaped GQA heads
+    (TransformerEngine PR #671, Tests / Verification)."""
+    wl = W.thd("thd", segs, hq=8, hkv=2, seed=sum(segs))
+    reps = run_backward_vs_oracle(B, wl, det)
+    assert_all_ok(reps, f"segments {segs}")
+
+
+def test_thd_window_and_d192(B):
+    wl = W.thd("thd_win", [100, 300, 37], hq=4, hkv=4, d_qk=192, d_v=128, mask=W.MASK_WINDOW,
+               left=64, right=0, seed=77)
+    assert_all_ok(run_backward_vs_oracle(B, wl, True), "thd window d192")
+
+
+def test_forward_helper_matches_oracle(B):
+    for wl in (SMALL[0], SMALL[2], SMALL[3], SMALL[8], SMALL[11], W.thd("t", [100, 80, 76], hq=4, hkv=2, seed=3)):
+        x = wl.inputs()
+        cu = wl.cu_seqlens()
+        kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cu)
+        o_ref, lse_ref = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, **kw)
+        cu_d = None if cu is None else cu.cuda()
+        o, lse = B.attn_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), scale=wl.scale, mask=wl.mask,
+                                left=wl.left, right=wl.right, cu_seqlens_q=cu_d, cu_seqlens_k=cu_d,
+                                max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+        torch.cuda.synchronize()
+        tol, mcos = tolerances(wl.dtype)
+        assert compare(o.cpu(), o_ref, tol, mcos)["ok"], wl.name
+        fin = torch.isfinite(lse_ref)
+        assert torch.equal(torch.isfinite(lse.cpu()), fin)
+        assert float((lse.cpu().double()[fin] - lse_ref[fin]).abs().max()) < 1e-3
+
+
+def test_fully_masked_rows_give_zero_and_finite(B):
+    wl = _wl("br_dead_rows", torch.bfloat16, 1, 2, 2, 300, 100, 128, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, seed=21)
+    x = wl.inputs()
+    o, lse = B.attn_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), scale=wl.scale, mask=wl.mask)
+    dq, dk, dv = B.attn_backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), o, x["do"].cuda(), lse,
+                                 scale=wl.scale, mask=wl.mask, deterministic=True)
+    torch.cuda.synchronize()
+    dead = ~R.visible(300, 100, wl.mask).any(dim=1)
+    assert int(dead.sum()) == 200
+    assert torch.isinf(lse.cpu()[0, :, dead]).all()
+    assert (dq.cpu()[0, dead] == 0).all()
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+
+
+def test_gpu_forward_then_backward_end_to_end(B):
+    """GPU forward -> GPU backward against the oracle's forward+backward."""
+    wl = _wl("e2e", torch.bfloat16, 2, 4, 2, 300, 300, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=31)
+    x = wl.inputs()
+    d = {k: v.cuda() for k, v in x.items()}
+    o, lse = B.attn_forward(d["q"], d["k"], d["v"], scale=wl.scale, mask=wl.mask)
+    got = B.attn_backward(d["q"], d["k"], d["v"], o, d["do"], lse, scale=wl.scale, mask=wl.mask,
+                          deterministic=True)
+    o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, mask=wl.mask)
+    ref = R.attn_backward(x["q"], x["k"], x["v"], o64, x["do"], lse64, wl.scale, mask=wl.mask)
+    reps = [compare(g.cpu(), r, 2e-2, 0.9999) for g, r in zip(got, ref)]
+    assert_all_ok(reps, "e2e")
+
+
+def test_deterministic_bitwise_repeatable(B):
+    wl = _wl("det_rep", torch.bfloat16, 2, 8, 2, 1000, 1000, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=41)
+    x = {k: v.cuda() for k, v in wl.inputs().items()}
+    o, lse = B.attn_forward(x["q"], x["k"], x["v"], scale=wl.scale, mask=wl.mask)
+    first = B.attn_backward(x["q"], x["k"], x["v"], o, x["do"], lse, scale=wl.scale, mask=wl.mask,
+                            deterministic=True)
+    first = [t.clone() for t in first]
+    for _ in range(9):
+        again = B.attn_backward(x["q"], x["k"], x["v"], o, x["do"], lse, scale=wl.scale, mask=wl.mask,
+                                deterministic=True)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+
+
+def test_bad_cu_seqlens_reported_by_device(B):
+    wl = W.thd("bad", [100, 80, 76], hq=4, hkv=2)
+    x = {k: v.cuda() for k, v in wl.inputs().items()}
+    bad = torch.tensor([0, 100, 90, 256], dtype=torch.int32, device="cuda")   # not monotone
+    lse = torch.zeros(4, 256, device="cuda")
+    with pytest.raises(B.AttnError) as e:
+        B.attn_backward(x["q"], x["k"], x["v"], x["do"], x["do"], lse, scale=wl.scale, mask=1,
+                        cu_seqlens_q=bad, cu_seqlens_k=bad, max_seqlen_q=100, max_seqlen_k=100)
+    assert e.value.status == -7
+    too_long = torch.tensor([0, 200, 230, 256], dtype=torch.int32, device="cuda")  # 200 > declared 100
+    with pytest.raises(B.AttnError) as e:
+        B.attn_backward(x["q"], x["k"], x["v"], x["do"], x["do"], lse, scale=wl.scale, mask=1,
+                        cu_seqlens_q=too_long, cu_seqlens_k=too_long, max_seqlen_q=100, max_seqlen_k=100)
+    assert e.value.status == -7
+
+
+def test_outputs_and_workspace_guard_bands(B):
+    """Nothing is written outside dq/dk/dv or past the sized workspace."""
+    wl = _wl("guard", torch.bfloat16, 1, 2, 2, 300, 300, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=51)
+    x = {k: v.cuda() for k, v in wl.inputs().items()}
+    o, lse = B.attn_forward(x["q"], x["k"], x["v"], scale=wl.scale, mask=wl.mask)
+    g = 4096
+    bufs = []
+    for t in (x["q"], x["k"], x["v"]):
+        big = torch.full((t.numel() + 2 * g,), float("nan"), dtype=t.dtype, device="cuda")
+        bufs.append(big)
+    outs = tuple(b[g:g + t.numel()].view(t.shape) for b, t in zip(bufs, (x["q"], x["k"], x["v"])))
+    for det in (True, False):
+        p = B.bwd_params(x["q"], x["k"], x["v"], o, x["do"], lse, *outs, scale=wl.scale, mask=wl.mask,
+                         deterministic=det)
+        need = B.workspace_bytes(p)
+        ws = torch.full((need + 65536,), 0xAB, dtype=torch.uint8, device="cuda")
+        assert B.attn_bwd(p, ws.data_ptr(), need, torch.cuda.current_stream().cuda_stream) == 0
+        torch.cuda.synchronize()
+        assert (ws[need:] == 0xAB).all()
+        for b, t in zip(bufs, outs):
+            assert torch.isnan(b[:g]).all() and torch.isnan(b[-g:]).all()
+            assert torch.isfinite(t).all()
