@@ -1,0 +1,318 @@
+"""Benchmark of the FMHA backward on the Llama-3-8B-shaped GQA workload.
+
+Default workload: B=2, Hq=32, Hkv=8, S=4096, d=128, causal, deterministic
+(nsplits = 32 dq_acc slices), bf16 inputs ~ N(0, 1), O/LSE from the forward
+helper.  One step = one whole attn_bwd call (schedule, preprocess, main
+kernel, dQ reduce/convert) on inputs resident in HBM; L2 is flushed (256 MB
+write) before every timed step.  Metric: mask-adjusted TFLOP/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica on its own GPU (the
+method has no cross-GPU exchange); the value is the whole-job throughput,
+timed as the max over ranks.  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from head_attention_backward_gb300 import flops as FL  # noqa: E402
+from head_attention_backward_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attn-bwd TFLOP/s (mask-adjusted, bf16) and % of GB300 dense BF16 peak"
+WORKLOADS = {"gqa_causal_det": W.gqa_causal_det, "mha_causal": W.mha_causal,
+             "thd_packed": W.thd_packed, "window_192": W.window_192}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops", 1900.0), d.get("hbm_gbs", 6800.0), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def config_of(wl):
+    c = {"workload": wl.name, "batch": wl.batch, "nhead_q": wl.hq, "nhead_kv": wl.hkv,
+         "seqlen": wl.sq, "d_qk": wl.d_qk, "d_v": wl.d_v, "mask": wl.mask,
+         "window": [wl.left, wl.right], "deterministic": wl.deterministic,
+         "l2": "flushed (256 MB write) before every timed step"}
+    if wl.group_mode:
+        c["segments"] = len(wl.seqlens)
+        c["total_tokens"] = wl.total
+    return c
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        target = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", target], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r.split(",") for r in self.tmp.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        loaded = [s for s in sm if s > 0.5 * mx] or sm
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].strip() not in ("", "[N/A]"))}
+
+
+def cpu_sample(wl, x, groups, budget_s):
+    """fp64 oracle backward on whole (batch, kv-head) groups of the workload;
+    returns (mask-adjusted FLOPs done, seconds, description)."""
+    from oracle import attn_ref as R
+    g = wl.hq // wl.hkv
+    per_pair = 2.0 * (3 * wl.d_qk + 2 * wl.d_v)
+    pairs = FL.visible_pairs(wl.sq, wl.sk, wl.mask, wl.left, wl.right)
+    done_flops, secs, n = 0.0, 0.0, 0
+    for b, hk in groups:
+        hs = slice(hk * g, (hk + 1) * g)
+        q, k, v, do = (x["q"][b:b + 1, :, hs], x["k"][b:b + 1, :, hk:hk + 1], x["v"][b:b + 1, :, hk:hk + 1],
+                       x["do"][b:b + 1, :, hs])
+        kw = dict(mask=wl.mask, left=wl.left, right=wl.right)
+        o, lse = R.attn_forward(q, k, v, wl.scale, **kw)
+        t0 = time.perf_counter()
+        R.attn_backward(q, k, v, o, do, lse, wl.scale, **kw)
+        secs += time.perf_counter() - t0
+        done_flops += per_pair * pairs * g
+        n += 1
+        if secs >= budget_s:
+            break
+    return done_flops, secs, f"{n} (batch, kv-head) group(s) x {g} query heads of {wl.name}, full S={wl.sq}"
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    x = wl.inputs()
+    steps = []
+    for i in range(args.warmup + args.steps):
+        f, s, desc = cpu_sample(wl, x, [(0, i % wl.hkv)], 0.0)
+        if i >= args.warmup:
+            steps.append((f, s))
+    tot_f = sum(f for f, _ in steps)
+    tot_s = sum(s for _, s in steps)
+    value = tot_f / tot_s / 1e12
+    cores = torch.get_num_threads()
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / len(steps),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": config_of(wl),
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                            "sample": "per step: " + desc},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_ours(args, wl):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    from head_attention_backward_gb300 import build as BLD
+    if rank == 0:
+        BLD.build_library()
+    if pg:
+        pg.barrier()
+    BLD.build_library()
+    from head_attention_backward_gb300 import binding as B
+    B.load()
+
+    x = wl.inputs()
+    d = {k: v.to(dev) for k, v in x.items()}
+    cu = wl.cu_seqlens()
+    cu_d = None if cu is None else cu.to(dev)
+    kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
+              cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+    o, lse = B.attn_forward(d["q"], d["k"], d["v"], **kw)
+    outs = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]))
+    p = B.bwd_params(d["q"], d["k"], d["v"], o, d["do"], lse, *outs, deterministic=wl.deterministic, **kw)
+    nbytes = B.workspace_bytes(p)
+    ws = B.alloc_workspace(nbytes, dev)
+    flush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    fl = FL.bwd_flops(wl)
+
+    def step():
+        flush.fill_(1.0)
+        st, ms = B.attn_bwd_timed(p, ws.data_ptr(), nbytes, stream)
+        if st != 0:
+            raise B.AttnError(st, "attn_bwd_timed")
+        return ms
+
+    for _ in range(args.warmup):
+        step()
+    st, dev_status = B.attn_bwd_read_status(ws.data_ptr(), stream)
+    if st != 0 or dev_status != 0:
+        raise B.AttnError(dev_status or st, "device status after warm-up")
+    clocks = ClockSampler(local)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    stage = [step() for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    step_ms = [s[3] for s in stage]
+    main_ms = [s[1] for s in stage]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    main_avg = sum(main_ms) / len(main_ms)
+    if pg:
+        t = torch.tensor([ms_per_step, main_avg], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_per_step, main_avg = t.tolist()
+
+    # end to end through the C ABI: pinned host inputs in, results back out
+    e2e_avg, h2d, d2h = float("nan"), 0, 0
+    if not args.no_e2e:
+        host = {k: v.to(dev).cpu().pin_memory() for k, v in (("q", d["q"]), ("k", d["k"]), ("v", d["v"]),
+                                                               ("o", o), ("do", d["do"]), ("lse", lse))}
+        host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs)
+        dev_in = {"q": d["q"], "k": d["k"], "v": d["v"], "o": o, "do": d["do"], "lse": lse}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+        e2e_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for k2, t in host.items():
+                dev_in[k2].copy_(t, non_blocking=True)
+            rc = B.attn_bwd(p, ws.data_ptr(), nbytes, stream)
+            if rc != 0:
+                raise B.AttnError(rc, "attn_bwd")
+            for hb, db in zip(host_out, outs):
+                hb.copy_(db, non_blocking=True)
+            e1.record()
+            e1.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        e2e_avg = sum(e2e_ms) / len(e2e_ms)
+        if pg:
+            t = torch.tensor([e2e_avg], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_avg = t.item()
+
+    peak_tf, peak_hbm, peak_src = peaks()
+    value = world * fl / (ms_per_step * 1e-3) / 1e12
+    achieved = fl / (main_avg * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == torch.bfloat16 else str(wl.dtype),
+        "data": "synthetic", "config": config_of(wl),
+        "pct_of_peak": 100.0 * value / world / peak_tf,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None, "kernel": "bwd_tc_kernel",
+                     "peak_source": f"{peak_src} bf16 burst", "kernel_ms": main_avg,
+                     "step_stage_ms": [sum(s[i] for s in stage) / len(stage) for i in range(4)]},
+        "e2e": None if args.no_e2e else {"value": world * fl / (e2e_avg * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                                         "ms_per_step": e2e_avg},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "workspace_bytes": nbytes,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        groups = [(b, hk) for b in range(wl.batch) for hk in range(wl.hkv)]
+        f, s, desc = cpu_sample(wl, x, groups, args.cpu_budget)
+        out["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+                               "kind": "oracle", "sample": desc + f" ({s:.1f} s of fp64 CPU work, dense scores)"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gqa_causal_det", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch of a batch-mode workload")
+    ap.add_argument("--atomic", action="store_true", help="fp32 atomic dQ accumulation instead of split slices")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]()
+    if args.batch and not wl.group_mode:
+        wl.batch = args.batch
+        wl.name += f"_batch{args.batch}"
+    if args.atomic:
+        wl.deterministic = False
+        wl.name += "_atomic"
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()
