@@ -47,7 +47,7 @@ class AttnFwdParams(ctypes.Structure):
 
 
 EXPORTS = ["attn_bwd_workspace_size", "attn_bwd", "attn_bwd_timed", "attn_bwd_read_status",
-           "attn_fwd", "attn_status_string"]
+           "attn_fwd", "attn_status_string", "attn_bwd_static_ws"]
 
 _lib = None
 
@@ -113,6 +113,21 @@ def attn_fwd(p: AttnFwdParams, stream: int = 0) -> int:
 
 def attn_status_string(st: int) -> str:
     return load().attn_status_string(st).decode()
+
+
+STATIC_WS_BYTES = 64 << 20
+
+
+def attn_bwd_static_ws(p: AttnBwdParams, stream: int = 0) -> int:
+    """attn_bwd with the library's own fixed device workspace: for callers
+    that cannot allocate device memory.  Problems needing more than
+    STATIC_WS_BYTES of workspace are rejected (ATTN_ERR_WORKSPACE_TOO_SMALL);
+    calls overlapping on the GPU share that workspace and race."""
+    lib = load()
+    fn = lib.attn_bwd_static_ws
+    fn.argtypes = [ctypes.POINTER(AttnBwdParams), _vp]
+    fn.restype = ctypes.c_int
+    return fn(ctypes.byref(p), stream)
 
 
 # ------------------------------------------------------- tensor marshalling

@@ -171,6 +171,29 @@ int attn_fwd(const attn_fwd_params* p, cudaStream_t stream);
 /* Static description of a status code. */
 const char* attn_status_string(int status);
 
+/* Size of the device array attn_bwd_static_ws uses as its workspace. */
+#define ATTN_BWD_STATIC_WS_BYTES (64u << 20)
+
+/* attn_bwd for callers that cannot allocate device memory (for example code
+ * that runs where cudaMalloc is forbidden or whose allocator is not reachable
+ * from the call site).  The paper has no counterpart: it is an addition of
+ * this library.  The caller still passes every input and output through *p;
+ * the workspace is a fixed ATTN_BWD_STATIC_WS_BYTES device array inside the
+ * library (held on every GPU that loads the library until the process
+ * exits), so no memory is allocated by this call.
+ * - Problems whose attn_bwd_workspace_size exceeds ATTN_BWD_STATIC_WS_BYTES
+ *   are rejected with ATTN_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ * - The first call while a given device is current looks up the array's
+ *   device address (cudaGetSymbolAddress); make that first call before any
+ *   stream capture on that device.
+ * - All calls on a device share the one array: calls that overlap on the GPU
+ *   (other streams, other host threads) race and corrupt each other.  Calls
+ *   ordered on one stream are safe; each call initialises what it reads.
+ * - Problems found on the device (cu_seqlens breaking their bounds) are
+ *   recorded in the library's array, which this entry point does not expose;
+ *   use attn_bwd with a caller workspace when that status is needed. */
+int attn_bwd_static_ws(const attn_bwd_params* p, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
