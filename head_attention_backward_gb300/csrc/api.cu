@@ -101,6 +101,8 @@ static Problem make_problem(const attn_bwd_params& p, void* ws) {
   P.dvec = reinterpret_cast<float*>(w + L.off_dvec);
   P.items = reinterpret_cast<int4*>(w + L.off_items);
   P.max_items = L.max_items;
+  P.tile_off = reinterpret_cast<int*>(w + L.off_tiles);
+  P.ntiles = L.ntiles;
   P.dq_acc = reinterpret_cast<float*>(w + L.off_dqacc);
   P.n_lse = L.n_lse;
   return P;

@@ -76,6 +76,25 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P) {
       }
       P.hdr[HDR_NITEMS] = n;
     }
+  } else if (tid < 64 && P.group) {
+    // warp 1: first dq_acc query-tile index of every segment (exclusive scan
+    // of ceil(Lq_b / BM)); dq_acc holds P.ntiles tiles per (slice, head)
+    const int lane = tid - 32;
+    int base = 0;
+    for (int b0 = 0; b0 <= P.nseg; b0 += 32) {
+      const int b = b0 + lane;
+      int v = 0;
+      if (b < P.nseg) v = cdiv(P.cu_q[b + 1] - P.cu_q[b], BM);
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (b <= P.nseg) P.tile_off[b] = base + incl - v;
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0 && base > P.ntiles) P.hdr[HDR_STATUS] = ATTN_ERR_BAD_SEQLENS;
   }
 }
 
@@ -120,7 +139,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem P, long long nt
   }
   if (!P.det) {
     float4* acc4 = reinterpret_cast<float4*>(P.dq_acc);
-    const long long n4 = P.n_lse * P.dqk / 4;
+    const long long n4 = (long long)P.hq * P.ntiles * P.dqk * BM / 4;
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long nt = (long long)gridDim.x * blockDim.x;
     for (long long i = t; i < n4; i += nt) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -145,72 +164,112 @@ void launch_preprocess(const Problem& P, cudaStream_t st) {
 }
 
 // ----------------------------------------------------------- reduce/convert
-// One warp per (packed token, query head).  Deterministic mode sums, in
-// ascending KV-tile order, exactly the slices whose KV tile reaches this
-// row's query tile (the others were never written); atomic mode reads the
-// single slice.
+// One block per (query head, query tile).  The dQ^T tiles of the slices whose
+// KV tile reaches this query tile (the others were never written) are summed
+// in ascending slice order; atomic mode reads the single slice.  The sum is
+// transposed through shared memory, scaled and written as dQ rows.
+
+constexpr int RC_THREADS = 256;
 
 template <typename T>
-__global__ void __launch_bounds__(256) reduce_convert_kernel(Problem P, long long ntok) {
-  const int lane = threadIdx.x & 31;
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+__global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
+  extern __shared__ float tile[];   // [dqk][BM + 1]
+  const int dqk = P.dqk;
+  const int nv4 = dqk * BM / 4;      // float4 per dQ^T tile
+  const int ntq = cdiv(P.sq, BM);
   T* dQ = static_cast<T*>(P.dq);
-  const int nv = P.dqk / 4;
-  const long long slice = P.n_lse * P.dqk;
-  for (long long r = warp; r < ntok * P.hq; r += nwarps) {
-    const long long tok = r / P.hq;
-    const int h = (int)(r - tok * P.hq);
-    int b, q;
+  for (long long w = blockIdx.x; w < (long long)P.hq * P.ntiles; w += gridDim.x) {
+    const int h = (int)(w / P.ntiles), t = (int)(w - (long long)h * P.ntiles);
+    int b, qt;
     if (P.group) {
-      // segment of this packed token: binary search of cu_seqlens_q
-      int lo = 0, hi = P.nseg;
+      if (t >= __ldg(P.tile_off + P.nseg)) continue;   // beyond the last segment's tiles
+      int lo = 0, hi = P.nseg;                           // largest b with tile_off[b] <= t
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(P.cu_q + mid) <= tok) lo = mid; else hi = mid;
+        if (__ldg(P.tile_off + mid) <= t) lo = mid; else hi = mid;
       }
       b = lo;
-      q = (int)(tok - __ldg(P.cu_q + b));
+      qt = t - __ldg(P.tile_off + b);
     } else {
-      b = (int)(tok / P.sq);
-      q = (int)(tok - (long long)b * P.sq);
+      b = t / ntq;
+      qt = t - b * ntq;
     }
     const Seg s = segment(P, b);
-    const long long row = lse_row(P, b, h, s, q);
-    const float* base = P.dq_acc + row * P.dqk;
-    T* out = dQ + r * P.dqk;
-    for (int v = lane; v < nv; v += 32) {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (P.det) {
-        const MaskArgs m = mask_args(P.mask, P.left, P.right, s.lq, s.lk);
-        const int qt = q / BM;
-        int nkv = cdiv(s.lk, BN);
-        if (nkv > P.nsplits) nkv = P.nsplits;   // guards cu_seqlens that broke their bound
-        for (int kt = 0; kt < nkv; ++kt) {
-          int lo, hi;
-          qtile_range(m, s.lq, s.lk, kt, lo, hi);
-          if (qt < lo || qt >= hi) continue;
-          const float4 x = reinterpret_cast<const float4*>(base + (long long)kt * slice)[v];
-          a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+    const int nvalid = min(BM, s.lq - qt * BM);
+    if (nvalid <= 0) continue;
+    float4 acc[(192 * BM / 4 + RC_THREADS - 1) / RC_THREADS];
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(acc) / sizeof(acc[0])); ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add_tile = [&](const float* src) {
+      const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+      for (int i = 0; i < (int)(sizeof(acc) / sizeof(acc[0])); ++i) {
+        const int v = threadIdx.x + i * RC_THREADS;
+        if (v < nv4) {
+          const float4 x = __ldcs(s4 + v);
+          acc[i].x += x.x; acc[i].y += x.y; acc[i].z += x.z; acc[i].w += x.w;
         }
-      } else if (s.lk > 0) {
-        a = reinterpret_cast<const float4*>(base)[v];
       }
-      out[4 * v + 0] = TypeOps<T>::from_f(a.x * P.scale);
-      out[4 * v + 1] = TypeOps<T>::from_f(a.y * P.scale);
-      out[4 * v + 2] = TypeOps<T>::from_f(a.z * P.scale);
-      out[4 * v + 3] = TypeOps<T>::from_f(a.w * P.scale);
+    };
+    if (P.det) {
+      const MaskArgs m = mask_args(P.mask, P.left, P.right, s.lq, s.lk);
+      int nkv = cdiv(s.lk, BN);
+      if (nkv > P.nsplits) nkv = P.nsplits;   // guards cu_seqlens that broke their bound
+      for (int kt = 0; kt < nkv; ++kt) {
+        int lo, hi;
+        qtile_range(m, s.lq, s.lk, kt, lo, hi);
+        if (qt >= lo && qt < hi) add_tile(dq_tile(P, kt, h, t));
+      }
+    } else if (s.lk > 0) {
+      add_tile(dq_tile(P, 0, h, t));
     }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(acc) / sizeof(acc[0])); ++i) {
+      const int v = threadIdx.x + i * RC_THREADS;
+      if (v < nv4) {
+        const int e = (4 * v) / BM, c = (4 * v) % BM;
+        float* dst = tile + e * (BM + 1) + c;
+        dst[0] = acc[i].x; dst[1] = acc[i].y; dst[2] = acc[i].z; dst[3] = acc[i].w;
+      }
+    }
+    __syncthreads();
+    const int nch = dqk / 8;                 // 8-element chunks per dQ row
+    for (int u = threadIdx.x; u < nvalid * nch; u += RC_THREADS) {
+      const int c = u / nch, ch = u - c * nch;
+      T outv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) outv[k] = TypeOps<T>::from_f(tile[(ch * 8 + k) * (BM + 1) + c] * P.scale);
+      T* row = dQ + ((long long)(s.q0 + qt * BM + c) * P.hq + h) * dqk + ch * 8;
+      if (sizeof(T) == 2) {
+        *reinterpret_cast<uint4*>(row) = *reinterpret_cast<uint4*>(outv);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) row[k] = outv[k];
+      }
+    }
+    __syncthreads();
   }
 }
 
 void launch_reduce_convert(const Problem& P, cudaStream_t st) {
-  const long long ntok = P.group ? (long long)P.tq : (long long)P.nseg * P.sq;
-  const int grid = num_sms() * 8;
+  const long long work = (long long)P.hq * P.ntiles;
+  if (work <= 0) return;
+  const int grid = (int)(work < (long long)num_sms() * 16 ? work : (long long)num_sms() * 16);
+  const size_t smem = (size_t)P.dqk * (BM + 1) * sizeof(float);
   switch (P.dtype) {
-    case ATTN_BF16: reduce_convert_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(P, ntok); break;
-    case ATTN_FP16: reduce_convert_kernel<__half><<<grid, 256, 0, st>>>(P, ntok); break;
-    default: reduce_convert_kernel<float><<<grid, 256, 0, st>>>(P, ntok); break;
+    case ATTN_BF16:
+      cudaFuncSetAttribute(reduce_convert_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      reduce_convert_kernel<__nv_bfloat16><<<grid, RC_THREADS, smem, st>>>(P);
+      break;
+    case ATTN_FP16:
+      cudaFuncSetAttribute(reduce_convert_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      reduce_convert_kernel<__half><<<grid, RC_THREADS, smem, st>>>(P);
+      break;
+    default:
+      cudaFuncSetAttribute(reduce_convert_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      reduce_convert_kernel<float><<<grid, RC_THREADS, smem, st>>>(P);
+      break;
   }
 }
 

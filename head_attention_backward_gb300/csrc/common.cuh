@@ -61,13 +61,15 @@ struct Problem {
   float* dvec;       // D = rowsum(dO * O)
   int4* items;       // (segment, kv head, kv tile, unused)
   int max_items;
-  float* dq_acc;     // [nsplits][rows(lse layout)][dqk]
+  int* tile_off;     // group mode: first query-tile index of each segment [nseg+1]
+  int ntiles;        // query tiles per (slice, head): B*ceil(Sq/BM) or an upper bound
+  float* dq_acc;     // [nsplits][Hq][ntiles][dqk][BM]: one contiguous dQ^T tile each
   long long n_lse;   // rows of the LSE layout = B*Hq*Sq or Hq*Tq
 };
 
 struct WsLayout {
-  size_t off_hdr, off_lse2, off_dvec, off_items, off_dqacc, total;
-  int max_items, nsplits;
+  size_t off_hdr, off_lse2, off_dvec, off_items, off_tiles, off_dqacc, total;
+  int max_items, nsplits, ntiles;
   long long n_lse;
 };
 
@@ -91,12 +93,22 @@ inline WsLayout ws_layout(const attn_bwd_params& p) {
     nkv_tiles = (long long)p.batch * cdiv(p.seqlen_k > 0 ? p.seqlen_k : 1, BN);
   }
   L.max_items = (int)(nkv_tiles * p.nhead_kv);
+  if (group) {
+    // sum_b ceil(Lq_b / BM) <= floor(Tq / BM) + nseg
+    long long a = (long long)p.total_q / BM + p.batch;
+    long long b = (long long)p.batch * cdiv(p.seqlen_q > 0 ? p.seqlen_q : 1, BM);
+    L.ntiles = (int)(a < b ? a : b);
+  } else {
+    L.ntiles = p.batch * cdiv(p.seqlen_q, BM);
+  }
   size_t o = 0;
   L.off_hdr = o;   o = up(o + HDR_WORDS * sizeof(int));
   L.off_lse2 = o;  o = up(o + (size_t)L.n_lse * sizeof(float));
   L.off_dvec = o;  o = up(o + (size_t)L.n_lse * sizeof(float));
   L.off_items = o; o = up(o + (size_t)(L.max_items > 0 ? L.max_items : 1) * sizeof(int4));
-  L.off_dqacc = o; o = up(o + (size_t)L.nsplits * (size_t)L.n_lse * p.d_qk * sizeof(float));
+  L.off_tiles = o; o = up(o + (size_t)(p.batch + 1) * sizeof(int));
+  L.off_dqacc = o;
+  o = up(o + (size_t)L.nsplits * p.nhead_q * (size_t)L.ntiles * p.d_qk * BM * sizeof(float));
   L.total = o;
   return L;
 }
@@ -125,9 +137,19 @@ __device__ __forceinline__ Seg segment(const Problem& P, int b) {
 }
 
 // Row index of (segment b, head h, segment-local query q) in the LSE layout:
-// batch [B][Hq][Sq], group [Hq][Tq].  dq_acc slices use the same row order.
+// batch [B][Hq][Sq], group [Hq][Tq] (D and the log2 LSE share it).
 __device__ __forceinline__ long long lse_row(const Problem& P, int b, int h, const Seg& s, int q) {
   return P.group ? (long long)h * P.tq + s.q0 + q : ((long long)b * P.hq + h) * P.sq + q;
+}
+
+// Query-tile index of (segment b, tile qt) inside a dq_acc slice.
+__device__ __forceinline__ int qtile_index(const Problem& P, int b, int qt) {
+  return P.group ? __ldg(P.tile_off + b) + qt : b * cdiv(P.sq, BM) + qt;
+}
+
+// First float of the dQ^T tile (slice j, head h, query tile t): [dqk][BM] fp32.
+__device__ __forceinline__ float* dq_tile(const Problem& P, int j, int h, int t) {
+  return P.dq_acc + (((long long)j * P.hq + h) * P.ntiles + t) * (long long)P.dqk * BM;
 }
 
 // ---------------------------------------------------------------------- mask

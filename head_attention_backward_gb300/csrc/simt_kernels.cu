@@ -208,7 +208,6 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
   const MaskArgs m = mask_args(P.mask, P.left, P.right, sg.lq, sg.lk);
   int qlo, qhi;
   qtile_range(m, sg.lq, sg.lk, kt, qlo, qhi);
-  const long long slice = P.n_lse * dqk;
   for (int h = hk * P.g; h < (hk + 1) * P.g; ++h) {
     for (int qt = qlo; qt < qhi; ++qt) {
       const int qs = qt * BM;
@@ -246,9 +245,9 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
         if (qs + c >= sg.lq) continue;
         float a = 0.f;
         for (int rr = 0; rr < BN; ++rr) a += sdS[rr * (BM + 1) + c] * sK[rr * ks + e];
-        const long long row = lse_row(P, b, h, sg, qs + c);
-        if (P.det) P.dq_acc[(long long)kt * slice + row * dqk + e] = a;
-        else atomicAdd(P.dq_acc + row * dqk + e, a);
+        float* tile = dq_tile(P, P.det ? kt : 0, h, qtile_index(P, b, qt));
+        if (P.det) tile[e * BM + c] = a;
+        else atomicAdd(tile + e * BM + c, a);
       }
     }
   }

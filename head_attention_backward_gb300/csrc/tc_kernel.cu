@@ -7,25 +7,28 @@
 // scores from the stored LSE and runs the five dense products of the
 // softmax-attention gradient, all with the KV tile on the 128 TMEM lanes:
 //
-//   S^T  = K Q^T                 (M = keys,  N = queries, K = d_qk)
-//   dP^T = V dO^T                (M = keys,  N = queries, K = d_v)
+//   S^T  = K Q^T                 (M = keys,  N = queries, K = d_qk)   SMEM x SMEM
+//   dP^T = V dO^T                (M = keys,  N = queries, K = d_v)    SMEM x SMEM
 //   P^T  = exp(s S^T - LSE),  dS^T = P^T o (dP^T - D)      (CUDA cores)
-//   dQ^T = K^T dS^T              (M = d_qk,  N = queries, K = keys)
-//   dV  += P^T dO                (M = keys,  N = d_v,     K = queries)
-//   dK  += dS^T Q                (M = keys,  N = d_qk,    K = queries)
+//   dQ^T = K^T dS^T              (M = d_qk,  N = queries, K = keys)   SMEM x SMEM
+//   dV  += P^T dO                (M = keys,  N = d_v,     K = queries) TMEM x SMEM
+//   dK  += dS^T Q                (M = keys,  N = d_qk,    K = queries) TMEM x SMEM
 //
-// dK and dV accumulate in TMEM across the item and are written once, scaled;
-// each dQ^T partial is written to the item's slice of the fp32 dq_acc
-// workspace (deterministic mode) or added to the single slice with fp32
-// reductions.  This is the persistent, deterministic split-dQ design of
-// aiter PR #2216 (Motivation) re-derived for TMA + tcgen05 + TMEM.
+// dK and dV accumulate in TMEM across the item and are written once, scaled.
+// Each dQ^T partial (d_qk x 64 fp32) goes through a shared-memory staging
+// tile to one contiguous tile of the dq_acc workspace with a TMA bulk copy:
+// a plain store into the item's split slice (deterministic mode) or an fp32
+// bulk reduce-add into the single slice.  This is the persistent,
+// deterministic split-dQ design of aiter PR #2216 (Motivation) re-derived for
+// TMA + tcgen05 + TMEM.
 //
-// Warp roles (320 threads): warp 0 loads (TMA for Q/dO/K/V plus the LSE/D
+// Warp roles (448 threads): warp 0 loads (TMA for Q/dO/K/V plus the LSE/D
 // rows of each query tile) and fetches work items; warp 1 allocates TMEM and
-// one lane issues every MMA; warps 2-5 turn S/dP into P/dS (one key row per
-// thread); warps 6-9 drain dQ partials and the final dK/dV.  Every mbarrier
-// wait is bounded by %globaltimer: on expiry the CTA records ATTN_ERR_TIMEOUT
-// in the workspace header and all roles unwind to a clean TMEM release.
+// one lane issues every MMA; warps 2-9 turn S/dP into P/dS (one key row per
+// thread, warps 2-5 the first 32 query columns, warps 6-9 the last 32);
+// warps 10-13 drain dQ partials and the final dK/dV.  Every mbarrier wait is
+// bounded by %globaltimer: on expiry the CTA records ATTN_ERR_TIMEOUT in the
+// workspace header and all roles unwind to a clean TMEM release.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,13 +42,20 @@ namespace tc {
 
 using namespace ptx;
 
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_SOFTMAX_WARPS = 8;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int FIRST_SOFTMAX_WARP = 2;
+constexpr int FIRST_EPI_WARP = FIRST_SOFTMAX_WARP + NUM_SOFTMAX_WARPS;
+constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + NUM_EPI_WARPS);
+constexpr int EPI_BARRIER_ID = 1;
 constexpr int NI = 2;                       // work-item ring slots
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint32_t SLEEP_HINT_NS = 20000;   // longest single sleep inside a wait
 constexpr uint32_t TMEM_COLS = 512;
 
 struct TmaMaps {
   CUtensorMap q, k, v, dout;
+  CUtensorMap acc;   // dq_acc as 2-D fp32 [rows][BM], boxes of 32 x 64, 128-byte swizzle
 };
 
 template <int DQK, int DV>
@@ -63,23 +73,26 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NCK_PAD * KCH;
   static constexpr int OFF_Q = OFF_V + NCV * KCH;
   static constexpr int OFF_DO = OFF_Q + ST * NCK * QCH;
-  static constexpr int OFF_P = OFF_DO + ST * NCV * QCH;
-  static constexpr int OFF_DS = OFF_P + BN * BM * 2;
-  static constexpr int OFF_L = OFF_DS + BN * BM * 2;    // [ST][BM] log2 LSE
-  static constexpr int OFF_D = OFF_L + ST * BM * 4;     // [ST][BM] D
+  static constexpr int OFF_DS = OFF_DO + ST * NCV * QCH;   // dS^T, bf16 [128 keys][64 queries]
+  static constexpr int OFF_STAGE = OFF_DS + BN * BM * 2;   // dQ^T staging: 2 x [128 rows][32 fp32], swizzled
+  static constexpr int OFF_L = OFF_STAGE + 128 * BM * 4;   // [ST][BM] -log2 LSE
+  static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
   static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
   static constexpr int NBAR = 16 + 2 * ST + 2 * NI;
   static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MISC = OFF_RING + NI * 16;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
-  // TMEM column map
+  // TMEM column map; P^T and dS^T (bf16, two per column) are MMA A operands
   static constexpr int T_DK = 0;
   static constexpr int T_DV = DQK;
   static constexpr int T_S = DQK + DV;
   static constexpr int T_DP = T_S + BM;
-  static constexpr bool ALIAS = T_DP + BM + NMB * BM > (int)TMEM_COLS;
+  static constexpr bool ALIAS = T_DP + BM + NMB * BM + BM > (int)TMEM_COLS;
   static constexpr int T_DQ = ALIAS ? T_S : T_DP + BM;
-  static_assert(T_DQ + NMB * BM <= (int)TMEM_COLS, "TMEM overflow");
+  static constexpr int T_P = ALIAS ? T_DP + BM : T_DQ + NMB * BM;
+  static constexpr int T_DS = T_P + BM / 2;
+  static_assert(T_DS + BM / 2 <= (int)TMEM_COLS, "TMEM overflow");
+  static_assert(!ALIAS || T_S + NMB * BM <= T_P, "aliased dQ must fit in S and dP");
   static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
   static constexpr uint32_t KV_BYTES = (NCK + NCV) * KCH;
   static constexpr uint32_t QDO_BYTES = (NCK + NCV) * QCH;
@@ -101,17 +114,14 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity,
   const uint32_t a = smem_u32(c.bar + idx);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
-  uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((++n & 31u) == 0) {
-      if (*(volatile int*)c.abort_flag) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-        *(volatile int*)c.abort_flag = 1;
-        atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
-        atomicExch(c.hdr + HDR_DIAG, where);
-        return false;
-      }
+    if (mbar_try_wait_sleep(a, parity, SLEEP_HINT_NS)) return true;
+    if (*(volatile int*)c.abort_flag) return false;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      *(volatile int*)c.abort_flag = 1;
+      atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
+      atomicExch(c.hdr + HDR_DIAG, where);
+      return false;
     }
   }
 }
@@ -179,13 +189,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     mbar_init(bar + B_KV_FULL, 1);
     mbar_init(bar + B_KV_EMPTY, 1);
     mbar_init(bar + B_SDP_FULL, 1);
-    mbar_init(bar + B_SDP_EMPTY, 4);
-    mbar_init(bar + B_PDS_FULL, 4);
+    mbar_init(bar + B_SDP_EMPTY, NUM_SOFTMAX_WARPS);
+    mbar_init(bar + B_PDS_FULL, NUM_SOFTMAX_WARPS);
     mbar_init(bar + B_PDS_EMPTY, 1);
     mbar_init(bar + B_DQ_FULL, 1);
-    mbar_init(bar + B_DQ_EMPTY, 4);
+    mbar_init(bar + B_DQ_EMPTY, NUM_EPI_WARPS);
     mbar_init(bar + B_DKV_FULL, 1);
-    mbar_init(bar + B_DKV_EMPTY, 4);
+    mbar_init(bar + B_DKV_EMPTY, NUM_EPI_WARPS);
     mbar_init(bar + B_DRAIN, 1);
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(bar + B_Q_FULL + s, 32);
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     }
     for (int s = 0; s < NI; ++s) {
       mbar_init(bar + B_IT_FULL + s, 1);
-      mbar_init(bar + B_IT_EMPTY + s, 1 + 4 + 4);
+      mbar_init(bar + B_IT_EMPTY + s, 1 + NUM_SOFTMAX_WARPS + NUM_EPI_WARPS);
     }
     fence_mbar_init();
   }
@@ -247,13 +257,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
         for (int c = lane; c < BM; c += 32) {
           const int q = qt * BM + c;
-          float l = INFINITY, d = 0.f;
+          float nl = -INFINITY, d = 0.f;
           if (q < I.sg.lq) {
             const long long li = lse_row(P, I.b, h, I.sg, q);
-            l = P.lse2[li];
+            nl = -P.lse2[li];
             d = P.dvec[li];
           }
-          sL[st * BM + c] = l;
+          sL[st * BM + c] = nl;
           sD[st * BM + c] = d;
         }
         __syncwarp();
@@ -283,10 +293,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       constexpr uint32_t ID_DK = idesc_f16(128, DQK, false, true, F16);
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sP = smem_u32(smem + C::OFF_P), sdS = smem_u32(smem + C::OFF_DS);
+      const uint32_t sdS = smem_u32(smem + C::OFF_DS);
       uint32_t g = 0, it = 0, n_item = 0;
       bool ok = true;
-      // S^T and dP^T of global step gs (stage st) into TMEM.
+      // S^T and dP^T of global step gs into TMEM.
       auto issue_sdp = [&](uint32_t gs) -> bool {
         const uint32_t st = gs % C::ST;
         if (!wait_bar(ctx, B_Q_FULL + st, (gs / C::ST) & 1, 10)) return false;
@@ -341,13 +351,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
           }
           const uint32_t q = sQ + st * C::NCK * C::QCH, d = sdO + st * C::NCV * C::QCH;
 #pragma unroll
-          for (int ks = 0; ks < BM / 16; ++ks)   // dV += P^T dO
-            umma_ss(tmem + C::T_DV, sdesc_sw128(sP + ks * 32, 16, 1024), sdesc_sw128(d + ks * 2048, C::QCH, 1024),
-                    ID_DV, (s > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < BM / 16; ++ks)   // dV += P^T dO, P^T from TMEM
+            umma_ts(tmem + C::T_DV, tmem + C::T_P + ks * 8, sdesc_sw128(d + ks * 2048, C::QCH, 1024), ID_DV,
+                    (s > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < BM / 16; ++ks)   // dK += dS^T Q
-            umma_ss(tmem + C::T_DK, sdesc_sw128(sdS + ks * 32, 16, 1024), sdesc_sw128(q + ks * 2048, C::QCH, 1024),
-                    ID_DK, (s > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < BM / 16; ++ks)   // dK += dS^T Q, dS^T from TMEM
+            umma_ts(tmem + C::T_DK, tmem + C::T_DS + ks * 8, sdesc_sw128(q + ks * 2048, C::QCH, 1024), ID_DK,
+                    (s > 0 || ks > 0) ? 1u : 0u);
           umma_commit(bar + B_PDS_EMPTY);
           umma_commit(bar + B_Q_EMPTY + st);
           if (C::ALIAS && s + 1 < I.nsteps && !(ok = issue_sdp(gs + 1))) break;
@@ -362,13 +372,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       umma_commit(bar + B_DRAIN);
       wait_bar(ctx, B_DRAIN, 0, 18);
     }
-  } else if (warp < 6) {
+  } else if (warp < FIRST_EPI_WARP) {
     // ------------------------------------------------------- softmax / dS
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;                 // key row = TMEM lane
+    const int half = (warp - FIRST_SOFTMAX_WARP) >> 2;  // which 32 query columns
+    const int r = quarter * 32 + lane;                   // key row = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    uint8_t* pRow = smem + C::OFF_P + r * 128;
+    const int c0 = half * 32;
     uint8_t* dsRow = smem + C::OFF_DS + r * 128;
+    const float2 sl2 = make_float2(P.scale_log2, P.scale_log2);
     uint32_t g = 0, n_item = 0;
     while (true) {
       const int slot = n_item % NI;
@@ -388,54 +400,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         const int qt = I.qlo + s % I.nq;
         if (!(ok = wait_bar(ctx, B_SDP_FULL, gs & 1, 21))) break;
         tc_fence_after();
-        uint32_t sv[BM], dpv[BM];
-        tmem_ld32(lane_addr + C::T_S, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(lane_addr + C::T_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld32(lane_addr + C::T_DP, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
-        tmem_ld32(lane_addr + C::T_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(lane_addr + C::T_S + c0, sv);
+        tmem_ld32(lane_addr + C::T_DP + c0, dpv);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar + B_SDP_EMPTY);
         if (!(ok = wait_bar(ctx, B_Q_FULL + st, (gs / C::ST) & 1, 22))) break;
-        const float* lrow = sL + st * BM;
-        const float* drow = sD + st * BM;
+        const float4* nl4 = reinterpret_cast<const float4*>(sL + st * BM + c0);
+        const float4* d4 = reinterpret_cast<const float4*>(sD + st * BM + c0);
         // whole tile visible and in range: skip the per-element predicate
         const int q_first = qt * BM, q_last = qt * BM + BM - 1;
         const int k_first = I.kt * BN, k_last = I.kt * BN + BN - 1;
         const bool full = I.klen == BN && q_last < I.sg.lq &&
                           (I.m.right < 0 || k_last <= q_first + I.m.off + I.m.right) &&
                           (I.m.left < 0 || k_first >= q_last + I.m.off - I.m.left);
-        float pv[BM], dsv[BM];
+        uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int c = 0; c < BM; ++c) {
-          const float l = lrow[c];
-          float p = fast_exp2(fmaf(__uint_as_float(sv[c]), P.scale_log2, -l));
-          if (!full) {
-            const int q = q_first + c;
-            const bool vis = key_ok && q < I.sg.lq && visible(I.m, q, kk);
-            p = vis ? p : 0.f;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 nl = nl4[c4], dd = d4[c4];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c = 4 * c4 + 2 * hh;
+            const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2,
+                                  hh ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y));
+            float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+            if (!full) {
+              const int q = q_first + c0 + c;
+              p0 = (key_ok && q < I.sg.lq && visible(I.m, q, kk)) ? p0 : 0.f;
+              p1 = (key_ok && q + 1 < I.sg.lq && visible(I.m, q + 1, kk)) ? p1 : 0.f;
+            }
+            const float2 p = make_float2(p0, p1);
+            const float2 ds = mul2(p, sub2(make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                           hh ? make_float2(dd.z, dd.w) : make_float2(dd.x, dd.y)));
+            pk[c >> 1] = pack2(p.x, p.y, (T*)nullptr);
+            dk[c >> 1] = pack2(ds.x, ds.y, (T*)nullptr);
           }
-          pv[c] = p;
-          dsv[c] = p * (__uint_as_float(dpv[c]) - drow[c]);
         }
         if (!(ok = wait_bar(ctx, B_PDS_EMPTY, (gs & 1) ^ 1, 23))) break;
+        tc_fence_after();
+        tmem_st16(lane_addr + C::T_P + c0 / 2, pk);
+        tmem_st16(lane_addr + C::T_DS + c0 / 2, dk);
 #pragma unroll
-        for (int ch = 0; ch < BM / 8; ++ch) {
-          const int sw = ((ch ^ (r & 7)) << 4);
-          uint4 a, b;
-          a.x = pack2(pv[8 * ch + 0], pv[8 * ch + 1], (T*)nullptr);
-          a.y = pack2(pv[8 * ch + 2], pv[8 * ch + 3], (T*)nullptr);
-          a.z = pack2(pv[8 * ch + 4], pv[8 * ch + 5], (T*)nullptr);
-          a.w = pack2(pv[8 * ch + 6], pv[8 * ch + 7], (T*)nullptr);
-          b.x = pack2(dsv[8 * ch + 0], dsv[8 * ch + 1], (T*)nullptr);
-          b.y = pack2(dsv[8 * ch + 2], dsv[8 * ch + 3], (T*)nullptr);
-          b.z = pack2(dsv[8 * ch + 4], dsv[8 * ch + 5], (T*)nullptr);
-          b.w = pack2(dsv[8 * ch + 6], dsv[8 * ch + 7], (T*)nullptr);
-          *reinterpret_cast<uint4*>(pRow + sw) = a;
-          *reinterpret_cast<uint4*>(dsRow + sw) = b;
+        for (int j = 0; j < 4; ++j) {
+          const int ch = half * 4 + j;
+          *reinterpret_cast<uint4*>(dsRow + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
         }
+        tmem_wait_st();
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar + B_PDS_FULL);
       }
@@ -446,10 +461,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     // ------------------------------------------------------ dQ / dK / dV out
     const int quarter = warp & 3;
     const int L = quarter * 32 + lane;                 // TMEM lane
+    const bool leader = warp == FIRST_EPI_WARP && lane == 0;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_STAGE);
     T* dKg = static_cast<T*>(P.dk);
     T* dVg = static_cast<T*>(P.dv_out);
-    const long long slice = P.n_lse * DQK;
     uint32_t g = 0, it = 0, n_item = 0;
     while (true) {
       const int slot = n_item % NI;
@@ -468,36 +484,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         }
         continue;
       }
-      float* acc = P.dq_acc + (P.det ? (long long)I.kt * slice : 0);
       bool ok = true;
       for (int s = 0; s < I.nsteps; ++s) {
         const uint32_t gs = g + s;
         const int h = I.hk * P.g + s / I.nq, qt = I.qlo + s % I.nq;
         if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
         tc_fence_after();
-        uint32_t v[C::NMB][BM];
-#pragma unroll
+        float* dst_tile = dq_tile(P, P.det ? I.kt : 0, h, qtile_index(P, I.b, qt));
+#pragma unroll 1
         for (int mb = 0; mb < C::NMB; ++mb) {
-          tmem_ld32(lane_addr + C::T_DQ + mb * BM, *reinterpret_cast<uint32_t(*)[32]>(&v[mb][0]));
-          tmem_ld32(lane_addr + C::T_DQ + mb * BM + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[mb][32]));
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
-        const int nvalid = min(BM, I.sg.lq - qt * BM);
-        const long long row0 = lse_row(P, I.b, h, I.sg, qt * BM);
+          uint32_t v[BM];
+          tmem_ld32(lane_addr + C::T_DQ + mb * BM, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(lane_addr + C::T_DQ + mb * BM + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (mb == C::NMB - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
+          }
+          const int rows = min(128, DQK - mb * 128);
+          // staging buffer free once the previous tensor copies have read it
+          if (leader) bulk_wait_read_all();
+          named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
+          // row L of the dQ^T block -> two 128-byte rows (query columns 0-31
+          // and 32-63), 16-byte chunks XOR-swizzled by L & 7 as TMA expects
 #pragma unroll
-        for (int mb = 0; mb < C::NMB; ++mb) {
-          const int e = mb * 128 + L;
-          if (e >= DQK) continue;
-          float* dst = acc + row0 * DQK + e;
+          for (int c = 0; c < BM / 4; ++c) {
+            uint8_t* half_buf = smem + C::OFF_STAGE + (c >> 3) * (128 * 128);
+            *reinterpret_cast<uint4*>(half_buf + L * 128 + (((c & 7) ^ (L & 7)) << 4)) =
+                make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
+          if (leader) {
+            const int row0 = (int)((dst_tile - P.dq_acc) / BM) + mb * 128;
+            for (int rg = 0; rg < rows; rg += 64) {
 #pragma unroll
-          for (int c = 0; c < BM; ++c) {
-            if (c < nvalid) {
-              if (P.det) dst[(long long)c * DQK] = __uint_as_float(v[mb][c]);
-              else atomicAdd(dst + (long long)c * DQK, __uint_as_float(v[mb][c]));
+              for (int hx = 0; hx < 2; ++hx) {
+                const uint8_t* box = smem + C::OFF_STAGE + hx * (128 * 128) + rg * 128;
+                if (P.det) tma_store_2d(&maps.acc, box, hx * 32, row0 + rg);
+                else tma_reduce_add_2d(&maps.acc, box, hx * 32, row0 + rg);
+              }
             }
+            bulk_commit();
           }
         }
       }
@@ -547,6 +576,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(bar + B_DKV_EMPTY);
       ++it;
     }
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -589,6 +619,22 @@ static bool make_map(CUtensorMap* m, const void* base, bool fp16, int dim, int h
   return r == CUDA_SUCCESS;
 }
 
+// dq_acc viewed as 2-D fp32 [nsplits * Hq * ntiles * d_qk rows][BM columns];
+// boxes of 32 columns x 64 rows with 128-byte swizzle (the staging layout).
+static bool make_acc_map(CUtensorMap* m, const Problem& P) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const unsigned long long rows = (unsigned long long)P.nsplits * P.hq * P.ntiles * P.dqk;
+  cuuint64_t dims[2] = {(cuuint64_t)BM, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)BM * 4};
+  cuuint32_t box[2] = {32, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P.dq_acc, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int DQK, int DV, typename T>
 static int launch_typed(const Problem& P, cudaStream_t st) {
   using C = Cfg<DQK, DV>;
@@ -597,7 +643,8 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
   const long long rq = P.group ? P.tq : (long long)P.nseg * P.sq;
   const long long rk = P.group ? P.tk : (long long)P.nseg * P.sk;
   if (!make_map(&maps.q, P.q, fp16, DQK, P.hq, rq, BM) || !make_map(&maps.dout, P.dout, fp16, DV, P.hq, rq, BM) ||
-      !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, BN) || !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, BN))
+      !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, BN) || !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, BN) ||
+      !make_acc_map(&maps.acc, P))
     return ATTN_ERR_CUDA;
   auto kern = bwd_tc_kernel<DQK, DV, T>;
   // at least 120 KB so that two CTAs never share an SM (each holds all 512 TMEM columns)
