@@ -97,7 +97,7 @@ static Problem make_problem(const attn_bwd_params& p, void* ws) {
   P.dq = p.dq; P.dk = p.dk; P.dv_out = p.dv;
   char* w = static_cast<char*>(ws);
   P.hdr = reinterpret_cast<int*>(w + L.off_hdr);
-  P.lse2 = reinterpret_cast<float*>(w + L.off_lse2);
+  P.nlse2 = reinterpret_cast<float*>(w + L.off_lse2);
   P.dvec = reinterpret_cast<float*>(w + L.off_dvec);
   P.items = reinterpret_cast<int4*>(w + L.off_items);
   P.max_items = L.max_items;

@@ -5,7 +5,7 @@
 //   expensive causal tiles (lowest KV-tile index) are dealt first.  It replaces
 //   the host-side seqstart copy CK's group-mode launcher needed (aiter PR
 //   #2216 follow-up commit on the unified workspace: ".to(at::kCPU)").
-// * preprocess: D = rowsum(dO * O) in fp32 and the log2-scaled LSE, plus the
+// * preprocess: D = rowsum(dO * O) in fp32 and the negated log2-scaled LSE, plus the
 //   zero-fill of the single atomic dq_acc slice (the "zero_init" the atomic
 //   path requires, aiter PR #2216 follow-up: workspace_alloc(bytes, zero_init)).
 // * reduce_convert: dQ = scale * sum over KV tiles of the dq_acc slices, in
@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P) {
     P.hdr[HDR_NEXT] = 0;
     P.hdr[HDR_DIAG] = 0;
   }
+  if (tid >= 16 && tid < HDR_WORDS) P.hdr[tid] = 0;   // optional per-site wait counters
   __syncthreads();
   if (P.group) {
     for (int b = tid; b < P.nseg; b += blockDim.x) {
@@ -103,46 +104,91 @@ void launch_schedule(const Problem& P, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------- preprocess
-// One warp per (packed token, query head): reads one O row and one dO row
-// (d_v elements, contiguous) and writes D and the log2-scaled LSE.
+// D and -LSE*log2(e) of every (packed token, query head) row.  16-bit
+// inputs: half a warp per row, 16-byte loads of O and dO.  fp32 inputs: one
+// warp per row.  In atomic mode the single dq_acc slice is zeroed as well.
+
+__device__ __forceinline__ void write_row_stats(const Problem& P, long long r, float acc) {
+  const float LOG2E = 1.4426950408889634f;
+  const long long tok = r / P.hq;
+  const int h = (int)(r - tok * P.hq);
+  long long li;
+  if (P.group) {
+    li = (long long)h * P.tq + tok;
+  } else {
+    const long long b = tok / P.sq, q = tok - b * P.sq;
+    li = (b * P.hq + h) * P.sq + q;
+  }
+  const float l = P.lse[li];
+  P.dvec[li] = acc;
+  P.nlse2[li] = (l == -INFINITY) ? -INFINITY : -l * LOG2E;
+}
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, __nv_bfloat16*) {
+  const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 u = __bfloat1622float2(x[i]), v = __bfloat1622float2(y[i]);
+    s = fmaf(u.x, v.x, s);
+    s = fmaf(u.y, v.y, s);
+  }
+  return s;
+}
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, __half*) {
+  const __half2* x = reinterpret_cast<const __half2*>(&a);
+  const __half2* y = reinterpret_cast<const __half2*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 u = __half22float2(x[i]), v = __half22float2(y[i]);
+    s = fmaf(u.x, v.x, s);
+    s = fmaf(u.y, v.y, s);
+  }
+  return s;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256) preprocess_kernel(Problem P, long long ntok) {
   const int lane = threadIdx.x & 31;
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const T* O = static_cast<const T*>(P.o);
-  const T* dO = static_cast<const T*>(P.dout);
-  const float LOG2E = 1.4426950408889634f;
-  for (long long r = warp; r < ntok * P.hq; r += nwarps) {
-    const long long tok = r / P.hq;
-    const int h = (int)(r - tok * P.hq);
-    const T* orow = O + r * P.dv;
-    const T* drow = dO + r * P.dv;
-    float acc = 0.f;
-    for (int c = lane; c < P.dv; c += 32)
-      acc += TypeOps<T>::to_f(orow[c]) * TypeOps<T>::to_f(drow[c]);
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const long long nrows = ntok * P.hq;
+  if constexpr (sizeof(T) == 2) {
+    // half warp per row; d_v is a multiple of 8 for the 16-bit kernels
+    const int sub = lane & 15;
+    const long long hw = tid >> 4, nhw = nthreads >> 4;
+    const uint4* O = static_cast<const uint4*>(P.o);
+    const uint4* dO = static_cast<const uint4*>(P.dout);
+    const int nv = P.dv / 8;
+    for (long long r0 = hw - (hw & 1); r0 < nrows; r0 += nhw) {
+      const long long r = r0 + (hw & 1);
+      float acc = 0.f;
+      if (r < nrows)
+        for (int v = sub; v < nv; v += 16) acc += dot8(O[r * nv + v], dO[r * nv + v], (T*)nullptr);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      long long li;
-      if (P.group) {
-        li = (long long)h * P.tq + tok;
-      } else {
-        const long long b = tok / P.sq, q = tok - b * P.sq;
-        li = (b * P.hq + h) * P.sq + q;
-      }
-      const float l = P.lse[li];
-      P.dvec[li] = acc;
-      P.lse2[li] = (l == -INFINITY) ? INFINITY : l * LOG2E;
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (sub == 0 && r < nrows) write_row_stats(P, r, acc);
+    }
+  } else {
+    const long long warp = tid >> 5, nwarps = nthreads >> 5;
+    const T* O = static_cast<const T*>(P.o);
+    const T* dO = static_cast<const T*>(P.dout);
+    for (long long r = warp; r < nrows; r += nwarps) {
+      float acc = 0.f;
+      for (int c = lane; c < P.dv; c += 32)
+        acc += TypeOps<T>::to_f(O[r * P.dv + c]) * TypeOps<T>::to_f(dO[r * P.dv + c]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) write_row_stats(P, r, acc);
     }
   }
   if (!P.det) {
     float4* acc4 = reinterpret_cast<float4*>(P.dq_acc);
     const long long n4 = (long long)P.hq * P.ntiles * P.dqk * BM / 4;
-    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long nt = (long long)gridDim.x * blockDim.x;
-    for (long long i = t; i < n4; i += nt) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long i = tid; i < n4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 

@@ -57,7 +57,7 @@ struct Problem {
   void* dv_out;
   // workspace
   int* hdr;
-  float* lse2;       // LSE * log2(e), +inf for rows without a visible key
+  float* nlse2;      // -LSE * log2(e), -inf for rows without a visible key
   float* dvec;       // D = rowsum(dO * O)
   int4* items;       // (segment, kv head, kv tile, unused)
   int max_items;

@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
   float* sQ = sdV + BN * vs;            // [BM][dqk]
   float* sdO = sQ + BM * dqk;           // [BM][dv]
   float* sdS = sdO + BM * dv;           // [BN][BM+1]
-  float* sL = sdS + BN * (BM + 1);      // [BM] log2-scaled LSE
+  float* sL = sdS + BN * (BM + 1);      // [BM] -LSE * log2(e)
   float* sD = sL + BM;                  // [BM]
 
   const T* Qg = static_cast<const T*>(P.q);
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
       if (r < BM) {
         const bool ok = qs + r < sg.lq;
         const long long li = ok ? lse_row(P, b, h, sg, qs + r) : 0;
-        sL[r] = ok ? P.lse2[li] : INFINITY;
+        sL[r] = ok ? P.nlse2[li] : -INFINITY;
         sD[r] = ok ? P.dvec[li] : 0.f;
       }
       __syncthreads();
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
         for (int e = 0; e < dqk; ++e) s += sK[r * ks + e] * sQ[c * dqk + e];
         for (int e = 0; e < dv; ++e) dp += sV[r * vs + e] * sdO[c * dv + e];
         const bool ok = r < klen && qi < sg.lq && visible(m, qi, kk);
-        const float pr = ok ? fast_exp2(s * P.scale_log2 - sL[c]) : 0.f;
+        const float pr = ok ? fast_exp2(fmaf(s, P.scale_log2, sL[c])) : 0.f;
         const float ds = pr * (dp - sD[c]);
         sdS[r * (BM + 1) + c] = ds;
         for (int e = 0; e < dv; ++e) sdV[r * vs + e] += pr * sdO[c * dv + e];

@@ -75,7 +75,7 @@ struct Cfg {
   static constexpr int OFF_DO = OFF_Q + ST * NCK * QCH;
   static constexpr int OFF_DS = OFF_DO + ST * NCV * QCH;   // dS^T, bf16 [128 keys][64 queries]
   static constexpr int OFF_STAGE = OFF_DS + BN * BM * 2;   // dQ^T staging: 2 x [128 rows][32 fp32], swizzled
-  static constexpr int OFF_L = OFF_STAGE + 128 * BM * 4;   // [ST][BM] -log2 LSE
+  static constexpr int OFF_L = OFF_STAGE + 128 * BM * 4;   // [ST][BM] -LSE*log2(e)
   static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
   static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
   static constexpr int NBAR = 16 + 2 * ST + 2 * NI;
@@ -110,10 +110,31 @@ struct Ctx {
   int* hdr;
 };
 
+#ifdef ATTN_WAIT_STATS
+__shared__ unsigned long long g_wait_stats[24];
+#endif
+
+#ifdef ATTN_WAIT_STATS
+// Optional instrumentation (off in normal builds): cycles each warp's lane 0
+// spent blocked at every wait site, summed per CTA in shared memory and added
+// to workspace header words [16 + 2*site] as 64-bit counters at exit.
+constexpr int N_WAIT_SITES = 24;
+__device__ __forceinline__ void stat_add(unsigned long long* s, int where, unsigned long long v) {
+  if ((threadIdx.x & 31) == 0) atomicAdd(s + (where % N_WAIT_SITES), v);
+}
+#endif
+
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity, int where) {
   const uint32_t a = smem_u32(c.bar + idx);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_test_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
+#ifdef ATTN_WAIT_STATS
+  const long long c0 = clock64();
+  struct Guard {
+    long long c0; int where;
+    __device__ ~Guard() { stat_add(g_wait_stats, where, (unsigned long long)(clock64() - c0)); }
+  } guard{c0, where};
+#endif
   while (true) {
     if (mbar_try_wait_sleep(a, parity, SLEEP_HINT_NS)) return true;
     if (*(volatile int*)c.abort_flag) return false;
@@ -184,6 +205,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       z[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
+#ifdef ATTN_WAIT_STATS
+  if (threadIdx.x < N_WAIT_SITES) g_wait_stats[threadIdx.x] = 0;
+#endif
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar + B_KV_FULL, 1);
@@ -198,7 +222,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     mbar_init(bar + B_DKV_EMPTY, NUM_EPI_WARPS);
     mbar_init(bar + B_DRAIN, 1);
     for (int s = 0; s < C::ST; ++s) {
-      mbar_init(bar + B_Q_FULL + s, 32);
+      mbar_init(bar + B_Q_FULL + s, 32 + 1);   // 32 cp.async arrivals + the TMA expect_tx arrival
       mbar_init(bar + B_Q_EMPTY + s, 1);
     }
     for (int s = 0; s < NI; ++s) {
@@ -255,18 +279,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         const uint32_t gs = g + s, st = gs % C::ST;
         const int h = I.hk * P.g + s / I.nq, qt = I.qlo + s % I.nq;
         if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
+        // -LSE*log2(e) and D of the tile's 64 query rows, copied asynchronously;
+        // rows past the segment end read as zeros (their columns are masked)
         for (int c = lane; c < BM; c += 32) {
           const int q = qt * BM + c;
-          float nl = -INFINITY, d = 0.f;
-          if (q < I.sg.lq) {
-            const long long li = lse_row(P, I.b, h, I.sg, q);
-            nl = -P.lse2[li];
-            d = P.dvec[li];
-          }
-          sL[st * BM + c] = nl;
-          sD[st * BM + c] = d;
+          const bool valid = q < I.sg.lq;
+          const long long li = valid ? lse_row(P, I.b, h, I.sg, q) : 0;
+          cp_async_4(sL + st * BM + c, P.nlse2 + li, valid ? 4u : 0u);
+          cp_async_4(sD + st * BM + c, P.dvec + li, valid ? 4u : 0u);
         }
-        __syncwarp();
+        cp_async_arrive_noinc(bar + B_Q_FULL + st);
         if (lane == 0) {
           mbar_arrive_expect_tx(bar + B_Q_FULL + st, C::QDO_BYTES);
           const int qrow = I.sg.q0 + qt * BM;
@@ -275,8 +297,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
           for (int c = 0; c < C::NCV; ++c)
             tma_load_3d(smem + C::OFF_DO + (st * C::NCV + c) * C::QCH, &maps.dout, bar + B_Q_FULL + st, c * 64, h,
                         qrow);
-        } else {
-          mbar_arrive(bar + B_Q_FULL + st);
         }
       }
       if (!ok) break;
@@ -291,9 +311,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       constexpr uint32_t ID_DQ = idesc_f16(128, BM, true, true, F16);
       constexpr uint32_t ID_DV = idesc_f16(128, DV, false, true, F16);
       constexpr uint32_t ID_DK = idesc_f16(128, DQK, false, true, F16);
-      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sdS = smem_u32(smem + C::OFF_DS);
+      // Descriptors of each operand's first 16-element K step; later steps add
+      // (byte offset >> 4) to the start-address field (no carry: smem < 256 KB).
+      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);          // K-major
+      const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::KCH, 1024);     // MN-major
+      const uint64_t ddS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::KCH, 1024);
+      const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      const uint64_t ddO_k = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+      const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::QCH, 1024);
+      const uint64_t ddO_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::QCH, 1024);
       uint32_t g = 0, it = 0, n_item = 0;
       bool ok = true;
       // S^T and dP^T of global step gs into TMEM.
@@ -303,17 +330,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         if (!wait_bar(ctx, B_SDP_EMPTY, (gs & 1) ^ 1, 11)) return false;
         if (C::ALIAS && !wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 12)) return false;
         tc_fence_after();
-        const uint32_t q = sQ + st * C::NCK * C::QCH, d = sdO + st * C::NCV * C::QCH;
+        const uint64_t q = dQ_k + ((st * C::NCK * C::QCH) >> 4), d = ddO_k + ((st * C::NCV * C::QCH) >> 4);
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks) {
           const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
-          umma_ss(tmem + C::T_S, sdesc_sw128(sK + off_a, 16, 1024), sdesc_sw128(q + off_b, 16, 1024), ID_SDP, ks > 0);
+          umma_ss(tmem + C::T_S, dK_k + (off_a >> 4), q + (off_b >> 4), ID_SDP, ks > 0);
         }
 #pragma unroll
         for (int ks = 0; ks < DV / 16; ++ks) {
           const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
-          umma_ss(tmem + C::T_DP, sdesc_sw128(sV + off_a, 16, 1024), sdesc_sw128(d + off_b, 16, 1024), ID_SDP,
-                  ks > 0);
+          umma_ss(tmem + C::T_DP, dV_k + (off_a >> 4), d + (off_b >> 4), ID_SDP, ks > 0);
         }
         umma_commit(bar + B_SDP_FULL);
         return true;
@@ -340,8 +366,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
           for (int mb = 0; mb < C::NMB; ++mb) {
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
-              umma_ss(tmem + C::T_DQ + mb * BM, sdesc_sw128(sK + mb * 2 * C::KCH + ks * 2048, C::KCH, 1024),
-                      sdesc_sw128(sdS + ks * 2048, C::KCH, 1024), ID_DQ, ks > 0);
+              umma_ss(tmem + C::T_DQ + mb * BM, dK_mn + ((mb * 2 * C::KCH + ks * 2048) >> 4),
+                      ddS_mn + ((ks * 2048) >> 4), ID_DQ, ks > 0);
             }
           }
           umma_commit(bar + B_DQ_FULL);
@@ -349,14 +375,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
             if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17))) break;
             tc_fence_after();
           }
-          const uint32_t q = sQ + st * C::NCK * C::QCH, d = sdO + st * C::NCV * C::QCH;
+          const uint64_t q = dQ_mn + ((st * C::NCK * C::QCH) >> 4), d = ddO_mn + ((st * C::NCV * C::QCH) >> 4);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks)   // dV += P^T dO, P^T from TMEM
-            umma_ts(tmem + C::T_DV, tmem + C::T_P + ks * 8, sdesc_sw128(d + ks * 2048, C::QCH, 1024), ID_DV,
+            umma_ts(tmem + C::T_DV, tmem + C::T_P + ks * 8, d + ((ks * 2048) >> 4), ID_DV,
                     (s > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks)   // dK += dS^T Q, dS^T from TMEM
-            umma_ts(tmem + C::T_DK, tmem + C::T_DS + ks * 8, sdesc_sw128(q + ks * 2048, C::QCH, 1024), ID_DK,
+            umma_ts(tmem + C::T_DK, tmem + C::T_DS + ks * 8, q + ((ks * 2048) >> 4), ID_DK,
                     (s > 0 || ks > 0) ? 1u : 0u);
           umma_commit(bar + B_PDS_EMPTY);
           umma_commit(bar + B_Q_EMPTY + st);
@@ -581,6 +607,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
 
   tc_fence_before();
   __syncthreads();
+#ifdef ATTN_WAIT_STATS
+  if (threadIdx.x < N_WAIT_SITES)
+    atomicAdd(reinterpret_cast<unsigned long long*>(P.hdr + 16) + threadIdx.x, g_wait_stats[threadIdx.x]);
+#endif
   if (warp == 1) {
     tc_fence_after();
     __syncwarp();
