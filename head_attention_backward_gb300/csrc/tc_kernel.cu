@@ -323,13 +323,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       const uint64_t ddO_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::QCH, 1024);
       uint32_t g = 0, it = 0, n_item = 0;
       bool ok = true;
-      // S^T and dP^T of global step gs into TMEM.
-      auto issue_sdp = [&](uint32_t gs) -> bool {
+      // The MMA groups below are issued from straight-line code that no
+      // conditional encloses: tcgen05.mma issued inside an if/else block
+      // measured about twice as slow per instruction on GB300, so every wait
+      // (and early exit) comes before a group, never around it.
+      //
+      // Inputs of S^T / dP^T for global step gs are ready and their TMEM free.
+      auto wait_sdp = [&](uint32_t gs) -> bool {
+        return wait_bar(ctx, B_Q_FULL + gs % C::ST, (gs / C::ST) & 1, 10) &&
+               wait_bar(ctx, B_SDP_EMPTY, (gs & 1) ^ 1, 11) &&
+               (!C::ALIAS || wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 12));
+      };
+      // S^T = K Q^T and dP^T = V dO^T of step gs.
+      auto mma_sdp = [&](uint32_t gs) {
         const uint32_t st = gs % C::ST;
-        if (!wait_bar(ctx, B_Q_FULL + st, (gs / C::ST) & 1, 10)) return false;
-        if (!wait_bar(ctx, B_SDP_EMPTY, (gs & 1) ^ 1, 11)) return false;
-        if (C::ALIAS && !wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 12)) return false;
-        tc_fence_after();
         const uint64_t q = dQ_k + ((st * C::NCK * C::QCH) >> 4), d = ddO_k + ((st * C::NCV * C::QCH) >> 4);
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks) {
@@ -342,7 +349,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
           umma_ss(tmem + C::T_DP, dV_k + (off_a >> 4), d + (off_b >> 4), ID_SDP, ks > 0);
         }
         umma_commit(bar + B_SDP_FULL);
-        return true;
+      };
+      // P^T / dS^T of step gs are in TMEM and smem (and the dQ TMEM is free).
+      auto wait_bwd = [&](uint32_t gs) -> bool {
+        return wait_bar(ctx, B_PDS_FULL, gs & 1, 15) &&
+               (C::ALIAS || wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16));
+      };
+      // dQ^T = K^T dS^T, dV += P^T dO, dK += dS^T Q of step gs.
+      auto mma_bwd = [&](uint32_t gs, uint32_t acc_first) {
+        const uint32_t st = gs % C::ST;
+#pragma unroll
+        for (int mb = 0; mb < C::NMB; ++mb) {
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            umma_ss(tmem + C::T_DQ + mb * BM, dK_mn + ((mb * 2 * C::KCH + ks * 2048) >> 4),
+                    ddS_mn + ((ks * 2048) >> 4), ID_DQ, ks > 0);
+          }
+        }
+        umma_commit(bar + B_DQ_FULL);
+        const uint64_t q = dQ_mn + ((st * C::NCK * C::QCH) >> 4), d = ddO_mn + ((st * C::NCV * C::QCH) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)   // dV += P^T dO, P^T from TMEM
+          umma_ts(tmem + C::T_DV, tmem + C::T_P + ks * 8, d + ((ks * 2048) >> 4), ID_DV, ks > 0 ? 1u : acc_first);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)   // dK += dS^T Q, dS^T from TMEM
+          umma_ts(tmem + C::T_DK, tmem + C::T_DS + ks * 8, q + ((ks * 2048) >> 4), ID_DK, ks > 0 ? 1u : acc_first);
+        umma_commit(bar + B_PDS_EMPTY);
+        umma_commit(bar + B_Q_EMPTY + st);
       };
       while (ok) {
         const int slot = n_item % NI;
@@ -353,40 +386,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         if (item.x < 0) break;
         const ItemInfo I = item_info(P, item);
         if (I.nsteps == 0) continue;
-        if (!wait_bar(ctx, B_KV_FULL, it & 1, 14)) break;
-        if (!(ok = issue_sdp(g))) break;
-        for (int s = 0; s < I.nsteps; ++s) {
-          const uint32_t gs = g + s, st = gs % C::ST;
-          if (!C::ALIAS && s + 1 < I.nsteps && !(ok = issue_sdp(gs + 1))) break;
-          if (!(ok = wait_bar(ctx, B_PDS_FULL, gs & 1, 15))) break;
-          if (!C::ALIAS && !(ok = wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16))) break;
-          tc_fence_after();
-          // dQ^T = K^T dS^T: A = K tile read MN-major, B = dS^T read MN-major
-#pragma unroll
-          for (int mb = 0; mb < C::NMB; ++mb) {
-#pragma unroll
-            for (int ks = 0; ks < BN / 16; ++ks) {
-              umma_ss(tmem + C::T_DQ + mb * BM, dK_mn + ((mb * 2 * C::KCH + ks * 2048) >> 4),
-                      ddS_mn + ((ks * 2048) >> 4), ID_DQ, ks > 0);
-            }
-          }
-          umma_commit(bar + B_DQ_FULL);
-          if (s == 0) {
-            if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17))) break;
+        ok = wait_bar(ctx, B_KV_FULL, it & 1, 14) && wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17);
+        if (!ok) break;
+        const uint32_t last = g + I.nsteps - 1;
+        if (C::ALIAS) {
+          // S/dP of a step reuse the dQ columns: issue them one step at a time
+          for (uint32_t gs = g; gs <= last; ++gs) {
+            if (!(ok = wait_sdp(gs))) break;
             tc_fence_after();
+            mma_sdp(gs);
+            if (!(ok = wait_bwd(gs))) break;
+            tc_fence_after();
+            mma_bwd(gs, gs != g);
           }
-          const uint64_t q = dQ_mn + ((st * C::NCK * C::QCH) >> 4), d = ddO_mn + ((st * C::NCV * C::QCH) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < BM / 16; ++ks)   // dV += P^T dO, P^T from TMEM
-            umma_ts(tmem + C::T_DV, tmem + C::T_P + ks * 8, d + ((ks * 2048) >> 4), ID_DV,
-                    (s > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-          for (int ks = 0; ks < BM / 16; ++ks)   // dK += dS^T Q, dS^T from TMEM
-            umma_ts(tmem + C::T_DK, tmem + C::T_DS + ks * 8, q + ((ks * 2048) >> 4), ID_DK,
-                    (s > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(bar + B_PDS_EMPTY);
-          umma_commit(bar + B_Q_EMPTY + st);
-          if (C::ALIAS && s + 1 < I.nsteps && !(ok = issue_sdp(gs + 1))) break;
+        } else {
+          // S/dP of step gs+1 run on the tensor pipe while P/dS of step gs
+          // are formed; the last step is peeled so no group is conditional
+          if (!(ok = wait_sdp(g))) break;
+          tc_fence_after();
+          mma_sdp(g);
+          for (uint32_t gs = g; gs < last; ++gs) {
+            if (!(ok = wait_sdp(gs + 1))) break;
+            tc_fence_after();
+            mma_sdp(gs + 1);
+            if (!(ok = wait_bwd(gs))) break;
+            tc_fence_after();
+            mma_bwd(gs, gs != g);
+          }
+          if (!ok) break;
+          if (!(ok = wait_bwd(last))) break;
+          tc_fence_after();
+          mma_bwd(last, last != g);
         }
         if (!ok) break;
         g += I.nsteps;
