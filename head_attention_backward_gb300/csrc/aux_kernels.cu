@@ -274,9 +274,15 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
     for (int i = 0; i < (int)(sizeof(acc) / sizeof(acc[0])); ++i) {
       const int v = threadIdx.x + i * RC_THREADS;
       if (v < nv4) {
-        const int e = (4 * v) / BM, c = (4 * v) % BM;
-        float* dst = tile + e * (BM + 1) + c;
-        dst[0] = acc[i].x; dst[1] = acc[i].y; dst[2] = acc[i].z; dst[3] = acc[i].w;
+        if (P.det) {                 // query-major tiles: 4 consecutive d of one query
+          const int c = (4 * v) / dqk, e = (4 * v) % dqk;
+          float* dst = tile + e * (BM + 1) + c;
+          dst[0] = acc[i].x; dst[BM + 1] = acc[i].y; dst[2 * (BM + 1)] = acc[i].z; dst[3 * (BM + 1)] = acc[i].w;
+        } else {                     // d-major tile: 4 consecutive queries of one d
+          const int e = (4 * v) / BM, c = (4 * v) % BM;
+          float* dst = tile + e * (BM + 1) + c;
+          dst[0] = acc[i].x; dst[1] = acc[i].y; dst[2] = acc[i].z; dst[3] = acc[i].w;
+        }
       }
     }
     __syncthreads();

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
         float a = 0.f;
         for (int rr = 0; rr < BN; ++rr) a += sdS[rr * (BM + 1) + c] * sK[rr * ks + e];
         float* tile = dq_tile(P, P.det ? kt : 0, h, qtile_index(P, b, qt));
-        if (P.det) tile[e * BM + c] = a;
+        if (P.det) tile[c * dqk + e] = a;
         else atomicAdd(tile + e * BM + c, a);
       }
     }

@@ -559,6 +559,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
             if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
           }
           const int rows = min(128, DQK - mb * 128);
+          if (P.det) {
+            // deterministic slice, tile stored query-major ([BM][d_qk]):
+            // for each query the warp's 32 consecutive d values fill one
+            // 128-byte line, written straight from registers (a shared-memory
+            // staging round trip plus TMA store measured ~20% slower on the
+            // whole kernel, 16-byte row-segment stores slower still)
+            if (L < rows) {
+              float* dst = dst_tile + mb * 128 + L;
+#pragma unroll
+              for (int c = 0; c < BM; ++c) __stcg(dst + c * DQK, __uint_as_float(v[c]));
+            }
+            continue;
+          }
+          // atomic mode: fp32 bulk reduce-add of the staged tile
           // staging buffer free once the previous tensor copies have read it
           if (leader) bulk_wait_read_all();
           named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
@@ -578,8 +592,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
 #pragma unroll
               for (int hx = 0; hx < 2; ++hx) {
                 const uint8_t* box = smem + C::OFF_STAGE + hx * (128 * 128) + rg * 128;
-                if (P.det) tma_store_2d(&maps.acc, box, hx * 32, row0 + rg);
-                else tma_reduce_add_2d(&maps.acc, box, hx * 32, row0 + rg);
+                tma_reduce_add_2d(&maps.acc, box, hx * 32, row0 + rg);
               }
             }
             bulk_commit();
