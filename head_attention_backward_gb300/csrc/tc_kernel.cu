@@ -42,7 +42,8 @@ namespace tc {
 
 using namespace ptx;
 
-constexpr int NUM_SOFTMAX_WARPS = 8;
+constexpr int NUM_SOFTMAX_WARPS = 16;                  // four per scheduler
+constexpr int SOFTMAX_COLS = BM * 4 / NUM_SOFTMAX_WARPS;  // query columns per softmax thread
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int FIRST_SOFTMAX_WARP = 2;
 constexpr int FIRST_EPI_WARP = FIRST_SOFTMAX_WARP + NUM_SOFTMAX_WARPS;
@@ -431,10 +432,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
   } else if (warp < FIRST_EPI_WARP) {
     // ------------------------------------------------------- softmax / dS
     const int quarter = warp & 3;
-    const int half = (warp - FIRST_SOFTMAX_WARP) >> 2;  // which 32 query columns
+    const int grp = (warp - FIRST_SOFTMAX_WARP) >> 2;   // which SOFTMAX_COLS query columns
     const int r = quarter * 32 + lane;                   // key row = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int c0 = half * 32;
+    constexpr int CW = SOFTMAX_COLS;
+    const int c0 = grp * CW;
     uint8_t* dsRow = smem + C::OFF_DS + r * 128;
     const float2 sl2 = make_float2(P.scale_log2, P.scale_log2);
     uint32_t g = 0, n_item = 0;
@@ -456,9 +458,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         const int qt = I.qlo + s % I.nq;
         if (!(ok = wait_bar(ctx, B_SDP_FULL, gs & 1, 21))) break;
         tc_fence_after();
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(lane_addr + C::T_S + c0, sv);
-        tmem_ld32(lane_addr + C::T_DP + c0, dpv);
+        uint32_t sv[CW], dpv[CW];
+        tmem_ld16(lane_addr + C::T_S + c0, sv);
+        tmem_ld16(lane_addr + C::T_DP + c0, dpv);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -472,9 +474,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         const bool full = I.klen == BN && q_last < I.sg.lq &&
                           (I.m.right < 0 || k_last <= q_first + I.m.off + I.m.right) &&
                           (I.m.left < 0 || k_first >= q_last + I.m.off - I.m.left);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[CW / 2], dk[CW / 2];
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
+        for (int c4 = 0; c4 < CW / 4; ++c4) {
           const float4 nl = nl4[c4], dd = d4[c4];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -496,11 +498,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         }
         if (!(ok = wait_bar(ctx, B_PDS_EMPTY, (gs & 1) ^ 1, 23))) break;
         tc_fence_after();
-        tmem_st16(lane_addr + C::T_P + c0 / 2, pk);
-        tmem_st16(lane_addr + C::T_DS + c0 / 2, dk);
+        tmem_st8(lane_addr + C::T_P + c0 / 2, pk);
+        tmem_st8(lane_addr + C::T_DS + c0 / 2, dk);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ch = half * 4 + j;
+        for (int j = 0; j < CW / 8; ++j) {
+          const int ch = grp * (CW / 8) + j;
           *reinterpret_cast<uint4*>(dsRow + ((ch ^ (r & 7)) << 4)) =
               make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
         }
@@ -549,53 +551,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         float* dst_tile = dq_tile(P, P.det ? I.kt : 0, h, qtile_index(P, I.b, qt));
 #pragma unroll 1
         for (int mb = 0; mb < C::NMB; ++mb) {
-          uint32_t v[BM];
-          tmem_ld32(lane_addr + C::T_DQ + mb * BM, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(lane_addr + C::T_DQ + mb * BM + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
-          if (mb == C::NMB - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
-          }
           const int rows = min(128, DQK - mb * 128);
-          if (P.det) {
-            // deterministic slice, tile stored query-major ([BM][d_qk]):
-            // for each query the warp's 32 consecutive d values fill one
-            // 128-byte line, written straight from registers (a shared-memory
-            // staging round trip plus TMA store measured ~20% slower on the
-            // whole kernel, 16-byte row-segment stores slower still)
-            if (L < rows) {
-              float* dst = dst_tile + mb * 128 + L;
-#pragma unroll
-              for (int c = 0; c < BM; ++c) __stcg(dst + c * DQK, __uint_as_float(v[c]));
+          if (!P.det) {
+            // atomic mode stages the tile for a bulk reduce-add: the staging
+            // buffer is free once the previous tensor copies have read it
+            if (leader) bulk_wait_read_all();
+            named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
+          }
+#pragma unroll 1
+          for (int hx = 0; hx < 2; ++hx) {     // query columns 0-31, then 32-63
+            uint32_t v[32];
+            tmem_ld32(lane_addr + C::T_DQ + mb * BM + hx * 32, v);
+            tmem_wait_ld();
+            if (mb == C::NMB - 1 && hx == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
             }
-            continue;
-          }
-          // atomic mode: fp32 bulk reduce-add of the staged tile
-          // staging buffer free once the previous tensor copies have read it
-          if (leader) bulk_wait_read_all();
-          named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
-          // row L of the dQ^T block -> two 128-byte rows (query columns 0-31
-          // and 32-63), 16-byte chunks XOR-swizzled by L & 7 as TMA expects
+            if (P.det) {
+              // deterministic slice, tile stored query-major ([BM][d_qk]): for
+              // each query the warp's 32 consecutive d values fill one 128-byte
+              // line, written straight from registers (a shared-memory staging
+              // round trip plus TMA store measured ~20% slower on the whole
+              // kernel, 16-byte row-segment stores slower still)
+              if (L < rows) {
+                float* dst = dst_tile + mb * 128 + L + hx * 32 * DQK;
 #pragma unroll
-          for (int c = 0; c < BM / 4; ++c) {
-            uint8_t* half_buf = smem + C::OFF_STAGE + (c >> 3) * (128 * 128);
-            *reinterpret_cast<uint4*>(half_buf + L * 128 + (((c & 7) ^ (L & 7)) << 4)) =
-                make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
-          if (leader) {
-            const int row0 = (int)((dst_tile - P.dq_acc) / BM) + mb * 128;
-            for (int rg = 0; rg < rows; rg += 64) {
-#pragma unroll
-              for (int hx = 0; hx < 2; ++hx) {
-                const uint8_t* box = smem + C::OFF_STAGE + hx * (128 * 128) + rg * 128;
-                tma_reduce_add_2d(&maps.acc, box, hx * 32, row0 + rg);
+                for (int c = 0; c < 32; ++c) __stcg(dst + c * DQK, __uint_as_float(v[c]));
               }
+            } else {
+              // row L of the dQ^T block -> 128-byte row of staging half hx,
+              // 16-byte chunks XOR-swizzled by L & 7 as TMA expects
+              uint8_t* half_buf = smem + C::OFF_STAGE + hx * (128 * 128);
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(half_buf + L * 128 + ((c ^ (L & 7)) << 4)) =
+                    make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
             }
-            bulk_commit();
+          }
+          if (!P.det) {
+            fence_proxy_async_smem();
+            named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
+            if (leader) {
+              const int row0 = (int)((dst_tile - P.dq_acc) / BM) + mb * 128;
+              for (int rg = 0; rg < rows; rg += 64) {
+#pragma unroll
+                for (int hx = 0; hx < 2; ++hx)
+                  tma_reduce_add_2d(&maps.acc, smem + C::OFF_STAGE + hx * (128 * 128) + rg * 128, hx * 32, row0 + rg);
+              }
+              bulk_commit();
+            }
           }
         }
       }
