@@ -22,11 +22,12 @@
 // deterministic split-dQ design of aiter PR #2216 (Motivation) re-derived for
 // TMA + tcgen05 + TMEM.
 //
-// Warp roles (448 threads): warp 0 loads (TMA for Q/dO/K/V plus the LSE/D
+// Warp roles (736 threads): warp 0 loads (TMA for Q/dO/K/V plus the LSE/D
 // rows of each query tile) and fetches work items; warp 1 allocates TMEM and
-// one lane issues every MMA; warps 2-9 turn S/dP into P/dS (one key row per
-// thread, warps 2-5 the first 32 query columns, warps 6-9 the last 32);
-// warps 10-13 drain dQ partials and the final dK/dV.  Every mbarrier wait is
+// one lane issues the dQ^T/dV/dK MMAs; warp 22's lane issues the S^T/dP^T
+// MMAs; warps 2-17 turn S/dP into P/dS (one key row per thread, 16 query
+// columns per warp); warps 18-21 drain dQ partials and the final dK/dV.
+// Every mbarrier wait is
 // bounded by %globaltimer: on expiry the CTA records ATTN_ERR_TIMEOUT in the
 // workspace header and all roles unwind to a clean TMEM release.
 #include <cuda.h>
@@ -47,7 +48,8 @@ constexpr int SOFTMAX_COLS = BM * 4 / NUM_SOFTMAX_WARPS;  // query columns per s
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int FIRST_SOFTMAX_WARP = 2;
 constexpr int FIRST_EPI_WARP = FIRST_SOFTMAX_WARP + NUM_SOFTMAX_WARPS;
-constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + NUM_EPI_WARPS);
+constexpr int SDP_ISSUER_WARP = FIRST_EPI_WARP + NUM_EPI_WARPS;   // issues the S / dP MMAs
+constexpr int NUM_THREADS = 32 * (SDP_ISSUER_WARP + 1);
 constexpr int EPI_BARRIER_ID = 1;
 constexpr int NI = 2;                       // work-item ring slots
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
@@ -102,7 +104,7 @@ struct Cfg {
 // barrier indices
 enum {
   B_KV_FULL = 0, B_KV_EMPTY, B_SDP_FULL, B_SDP_EMPTY, B_PDS_FULL, B_PDS_EMPTY,
-  B_DQ_FULL, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_FIXED_END = 16
+  B_DQ_FULL, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_DRAIN2, B_FIXED_END = 16
 };
 
 struct Ctx {
@@ -208,6 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
   }
 #ifdef ATTN_WAIT_STATS
   if (threadIdx.x < N_WAIT_SITES) g_wait_stats[threadIdx.x] = 0;
+  const long long kernel_c0 = clock64();
 #endif
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -222,13 +225,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     mbar_init(bar + B_DKV_FULL, 1);
     mbar_init(bar + B_DKV_EMPTY, NUM_EPI_WARPS);
     mbar_init(bar + B_DRAIN, 1);
+    mbar_init(bar + B_DRAIN2, 1);
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(bar + B_Q_FULL + s, 32 + 1);   // 32 cp.async arrivals + the TMA expect_tx arrival
       mbar_init(bar + B_Q_EMPTY + s, 1);
     }
     for (int s = 0; s < NI; ++s) {
       mbar_init(bar + B_IT_FULL + s, 1);
-      mbar_init(bar + B_IT_EMPTY + s, 1 + NUM_SOFTMAX_WARPS + NUM_EPI_WARPS);
+      mbar_init(bar + B_IT_EMPTY + s, 2 + NUM_SOFTMAX_WARPS + NUM_EPI_WARPS);
     }
     fence_mbar_init();
   }
@@ -304,9 +308,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       g += I.nsteps;
       ++it;
     }
-  } else if (warp == 1) {
-    // ----------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == SDP_ISSUER_WARP) {
+    // ---------------------------------------------------------- MMA issuers
+    // Two single-thread issuers on different schedulers: warp SDP_ISSUER_WARP
+    // issues S^T / dP^T, warp 1 (which owns the TMEM allocation) issues
+    // dQ^T / dV / dK and the per-item K/V and dK/dV releases.  One thread
+    // issuing every MMA, wait and commit of a step was measured as the
+    // kernel's serial bottleneck.
     if (lane == 0) {
+      const bool is_sdp = warp == SDP_ISSUER_WARP;
       constexpr bool F16 = IsHalf<T>::value;
       constexpr uint32_t ID_SDP = idesc_f16(128, BM, false, false, F16);
       constexpr uint32_t ID_DQ = idesc_f16(128, BM, true, true, F16);
@@ -324,10 +334,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       const uint64_t ddO_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::QCH, 1024);
       uint32_t g = 0, it = 0, n_item = 0;
       bool ok = true;
-      // The MMA groups below are issued from straight-line code that no
-      // conditional encloses: tcgen05.mma issued inside an if/else block
-      // measured about twice as slow per instruction on GB300, so every wait
-      // (and early exit) comes before a group, never around it.
+      // The MMA groups are issued from straight-line code: a tcgen05.mma
+      // sequence chosen per iteration by an if/else measured about twice as
+      // slow per instruction on GB300, so every wait (and early exit) comes
+      // before a group, never around it.
       //
       // Inputs of S^T / dP^T for global step gs are ready and their TMEM free.
       auto wait_sdp = [&](uint32_t gs) -> bool {
@@ -337,6 +347,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       };
       // S^T = K Q^T and dP^T = V dO^T of step gs.
       auto mma_sdp = [&](uint32_t gs) {
+#ifdef ATTN_WAIT_STATS
+        const long long t0 = clock64();
+#endif
         const uint32_t st = gs % C::ST;
         const uint64_t q = dQ_k + ((st * C::NCK * C::QCH) >> 4), d = ddO_k + ((st * C::NCV * C::QCH) >> 4);
 #pragma unroll
@@ -350,6 +363,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
           umma_ss(tmem + C::T_DP, dV_k + (off_a >> 4), d + (off_b >> 4), ID_SDP, ks > 0);
         }
         umma_commit(bar + B_SDP_FULL);
+#ifdef ATTN_WAIT_STATS
+        stat_add(g_wait_stats, 4, (unsigned long long)(clock64() - t0));   // S/dP group issue
+        stat_add(g_wait_stats, 9, 1ull);                                   // steps
+#endif
       };
       // P^T / dS^T of step gs are in TMEM and smem (and the dQ TMEM is free).
       auto wait_bwd = [&](uint32_t gs) -> bool {
@@ -358,6 +375,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       };
       // dQ^T = K^T dS^T, dV += P^T dO, dK += dS^T Q of step gs.
       auto mma_bwd = [&](uint32_t gs, uint32_t acc_first) {
+#ifdef ATTN_WAIT_STATS
+        const long long t0 = clock64();
+#endif
         const uint32_t st = gs % C::ST;
 #pragma unroll
         for (int mb = 0; mb < C::NMB; ++mb) {
@@ -377,6 +397,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
           umma_ts(tmem + C::T_DK, tmem + C::T_DS + ks * 8, q + ((ks * 2048) >> 4), ID_DK, ks > 0 ? 1u : acc_first);
         umma_commit(bar + B_PDS_EMPTY);
         umma_commit(bar + B_Q_EMPTY + st);
+#ifdef ATTN_WAIT_STATS
+        stat_add(g_wait_stats, 5, (unsigned long long)(clock64() - t0));   // dQ/dV/dK group issue
+#endif
       };
       while (ok) {
         const int slot = n_item % NI;
@@ -387,47 +410,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         if (item.x < 0) break;
         const ItemInfo I = item_info(P, item);
         if (I.nsteps == 0) continue;
-        ok = wait_bar(ctx, B_KV_FULL, it & 1, 14) && wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17);
-        if (!ok) break;
         const uint32_t last = g + I.nsteps - 1;
-        if (C::ALIAS) {
-          // S/dP of a step reuse the dQ columns: issue them one step at a time
+        if (is_sdp) {
+          if (!(ok = wait_bar(ctx, B_KV_FULL, it & 1, 14))) break;
           for (uint32_t gs = g; gs <= last; ++gs) {
             if (!(ok = wait_sdp(gs))) break;
             tc_fence_after();
             mma_sdp(gs);
-            if (!(ok = wait_bwd(gs))) break;
-            tc_fence_after();
-            mma_bwd(gs, gs != g);
           }
         } else {
-          // S/dP of step gs+1 run on the tensor pipe while P/dS of step gs
-          // are formed; the last step is peeled so no group is conditional
-          if (!(ok = wait_sdp(g))) break;
-          tc_fence_after();
-          mma_sdp(g);
-          for (uint32_t gs = g; gs < last; ++gs) {
-            if (!(ok = wait_sdp(gs + 1))) break;
-            tc_fence_after();
-            mma_sdp(gs + 1);
+          if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17))) break;
+          for (uint32_t gs = g; gs <= last; ++gs) {
             if (!(ok = wait_bwd(gs))) break;
             tc_fence_after();
             mma_bwd(gs, gs != g);
           }
           if (!ok) break;
-          if (!(ok = wait_bwd(last))) break;
-          tc_fence_after();
-          mma_bwd(last, last != g);
+          // the item's last dQ/dV/dK followed its last P/dS, which followed
+          // every S/dP of the item: K/V and the dK/dV accumulators are done
+          umma_commit(bar + B_KV_EMPTY);
+          umma_commit(bar + B_DKV_FULL);
         }
         if (!ok) break;
         g += I.nsteps;
-        umma_commit(bar + B_KV_EMPTY);
-        umma_commit(bar + B_DKV_FULL);
         ++it;
       }
-      // make sure no MMA is in flight before TMEM is released
-      umma_commit(bar + B_DRAIN);
-      wait_bar(ctx, B_DRAIN, 0, 18);
+      // make sure no MMA of this issuer is in flight before TMEM is released
+      umma_commit(bar + (is_sdp ? B_DRAIN2 : B_DRAIN));
+      wait_bar(ctx, is_sdp ? B_DRAIN2 : B_DRAIN, 0, 18);
     }
   } else if (warp < FIRST_EPI_WARP) {
     // ------------------------------------------------------- softmax / dS
@@ -656,8 +666,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
 #ifdef ATTN_WAIT_STATS
-  if (threadIdx.x < N_WAIT_SITES)
-    atomicAdd(reinterpret_cast<unsigned long long*>(P.hdr + 16) + threadIdx.x, g_wait_stats[threadIdx.x]);
+  // site 0: CTA cycles (sum over CTAs), site 19: the longest CTA
+  unsigned long long* gstat = reinterpret_cast<unsigned long long*>(P.hdr + 16);
+  if (threadIdx.x == 0) {
+    const unsigned long long cyc = (unsigned long long)(clock64() - kernel_c0);
+    g_wait_stats[0] = cyc;
+    atomicMax(gstat + 19, cyc);
+  }
+  __syncthreads();
+  if (threadIdx.x < N_WAIT_SITES && threadIdx.x != 19) atomicAdd(gstat + threadIdx.x, g_wait_stats[threadIdx.x]);
 #endif
   if (warp == 1) {
     tc_fence_after();
