@@ -67,6 +67,34 @@ def peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+# DRAM bytes (read + write) per launch of the main kernel, from a one-pass ncu capture
+# of the named workload.  Reported only while the kernel sources hash to ``src``: any
+# change to the kernel makes the figure stale, and then ``traffic`` is null.
+KERNEL_SOURCES = ("tc_kernel.cu", "common.cuh", "sm100_ptx.cuh")
+KERNEL_TRAFFIC = {
+    "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det": {
+        "bytes": 551.55e6 + 2.19e9,
+        "src": "523903848972bbd9",
+        "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
+}
+
+
+def kernel_src_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "head_attention_backward_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_name):
+    t = KERNEL_TRAFFIC.get(workload_name)
+    if t is None or t["src"] != kernel_src_hash():
+        return None, None
+    return t["bytes"], t["profile"]
+
+
 def config_of(wl):
     c = {"workload": wl.name, "batch": wl.batch, "nhead_q": wl.hq, "nhead_kv": wl.hkv,
          "seqlen": wl.sq, "d_qk": wl.d_qk, "d_v": wl.d_v, "mask": wl.mask,
@@ -96,7 +124,7 @@ class ClockSampler:
             pass
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", target], stdout=self.tmp, stderr=subprocess.DEVNULL)
+                                          "-lms", "50", "-i", target], stdout=self.tmp, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -153,25 +181,40 @@ def cpu_sample(wl, x, groups, budget_s):
 
 
 def run_reference(args, wl):
+    """The fp64 oracle timed on the host cores.  One step = the backward of one
+    query head (with its kv head) of the workload at full sequence length; the
+    forward that feeds it is computed once per head, outside the timed region."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    from oracle import attn_ref as R
     x = wl.inputs()
-    steps = []
+    g = wl.hq // wl.hkv
+    kw = dict(mask=wl.mask, left=wl.left, right=wl.right)
+    per_head = 2.0 * (3 * wl.d_qk + 2 * wl.d_v) * FL.visible_pairs(wl.sq, wl.sk, wl.mask, wl.left, wl.right)
+    fwd = {}
+    secs = []
     for i in range(args.warmup + args.steps):
-        f, s, desc = cpu_sample(wl, x, [(0, i % wl.hkv)], 0.0)
+        h = i % wl.hq
+        q, k, v, do = (x["q"][0:1, :, h:h + 1], x["k"][0:1, :, h // g:h // g + 1],
+                       x["v"][0:1, :, h // g:h // g + 1], x["do"][0:1, :, h:h + 1])
+        if h not in fwd:
+            fwd[h] = R.attn_forward(q, k, v, wl.scale, **kw)
+        o, lse = fwd[h]
+        t0 = time.perf_counter()
+        R.attn_backward(q, k, v, o, do, lse, wl.scale, **kw)
         if i >= args.warmup:
-            steps.append((f, s))
-    tot_f = sum(f for f, _ in steps)
-    tot_s = sum(s for _, s in steps)
-    value = tot_f / tot_s / 1e12
+            secs.append(time.perf_counter() - t0)
+    tot_s = sum(secs)
+    value = per_head * len(secs) / tot_s / 1e12
     cores = torch.get_num_threads()
+    desc = f"per step: the backward of one query head of {wl.name} (batch 0, full S={wl.sq}, dense fp64 scores)"
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / len(steps),
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / len(secs),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "config": config_of(wl),
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                            "sample": "per step: " + desc},
+                            "sample": desc},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -266,6 +309,7 @@ def run_ours(args, wl):
         e2e_avg = max_over_ranks([sum(e2e_ms) / len(e2e_ms)], pg, dev)[0]
 
     peak_tf, peak_hbm, peak_src = peaks()
+    traffic, traffic_src = measured_traffic(wl.name)
     value = job_throughput(world, fl, ms_per_step)
     achieved = fl / (main_avg * 1e-3) / 1e12
     out = {
@@ -275,7 +319,8 @@ def run_ours(args, wl):
         "data": "synthetic", "config": config_of(wl),
         "pct_of_peak": 100.0 * value / world / peak_tf,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": None, "kernel": "bwd_tc_kernel",
+                     "frac": achieved / peak_tf, "traffic": traffic, "traffic_source": traffic_src,
+                     "kernel": "bwd_tc_kernel",
                      "peak_source": f"{peak_src} bf16 burst", "kernel_ms": main_avg,
                      "step_stage_ms": [sum(s[i] for s in stage) / len(stage) for i in range(4)]},
         "e2e": None if args.no_e2e else {"value": job_throughput(world, fl, e2e_avg), "unit": "TFLOP/s",
@@ -300,7 +345,7 @@ def run_ours(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_causal_det", choices=sorted(WORKLOADS))

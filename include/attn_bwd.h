@@ -73,8 +73,9 @@ typedef enum {
 
 /* Element type of q, k, v, o, dout, dq, dk, dv (lse is always fp32).
  * Supported head dims: BF16/FP16 (d_qk, d_v) in {(64,64), (128,128),
- * (192,128)} on the tensor-core kernel; FP32 any d_qk, d_v in [1, 128]
- * on the fp32 SIMT kernel. */
+ * (192,128)} on the tensor-core kernel; FP32 d_qk in [4, 64] with
+ * d_qk % 4 == 0 and d_v in [1, 64] on the fp32 SIMT kernel.  Any other pair
+ * returns ATTN_ERR_UNSUPPORTED_HEADDIM before a launch. */
 typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1, ATTN_FP32 = 2 } attn_dtype_t;
 
 typedef struct {
