@@ -210,118 +210,122 @@ void launch_preprocess(const Problem& P, cudaStream_t st) {
 }
 
 // ----------------------------------------------------------- reduce/convert
-// One block per (query head, query tile).  The dQ^T tiles of the slices whose
-// KV tile reaches this query tile (the others were never written) are summed
-// in ascending slice order; atomic mode reads the single slice.  The sum is
-// transposed through shared memory, scaled and written as dQ rows.
+// One block per (query head, query tile).  The query-major dQ tiles of the slices whose KV tile reaches this query tile
+// (the others were never written) are summed in ascending slice order; atomic
+// mode reads the single slice.  Each thread owns four consecutive d of one
+// query row, so the scaled sum goes straight to dQ without a transpose.
 
 constexpr int RC_THREADS = 256;
 
-template <typename T>
+// NACC = float4 accumulators per thread = ceil(d_qk * BM / 4 / RC_THREADS).
+template <typename T, int NACC>
 __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
-  extern __shared__ float tile[];   // [dqk][BM + 1]
   const int dqk = P.dqk;
-  const int nv4 = dqk * BM / 4;      // float4 per dQ^T tile
+  const int nv4 = dqk * BM / 4;      // float4 per dQ tile
   const int ntq = cdiv(P.sq, BM);
   T* dQ = static_cast<T*>(P.dq);
-  for (long long w = blockIdx.x; w < (long long)P.hq * P.ntiles; w += gridDim.x) {
-    const int h = (int)(w / P.ntiles), t = (int)(w - (long long)h * P.ntiles);
-    int b, qt;
-    if (P.group) {
-      if (t >= __ldg(P.tile_off + P.nseg)) continue;   // beyond the last segment's tiles
-      int lo = 0, hi = P.nseg;                           // largest b with tile_off[b] <= t
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(P.tile_off + mid) <= t) lo = mid; else hi = mid;
-      }
-      b = lo;
-      qt = t - __ldg(P.tile_off + b);
-    } else {
-      b = t / ntq;
-      qt = t - b * ntq;
+  // block -> (head, tile), head-major (measured a few percent faster than
+  // interleaving heads or putting the most-loaded causal tiles first)
+  const long long w = blockIdx.x;
+  const int h = (int)(w / P.ntiles);
+  const int r = (int)(w % P.ntiles);
+  int b, qt, t;
+  if (P.group) {
+    t = r;
+    if (t >= __ldg(P.tile_off + P.nseg)) return;   // beyond the last segment's tiles
+    int lo = 0, hi = P.nseg;                        // largest b with tile_off[b] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(P.tile_off + mid) <= t) lo = mid; else hi = mid;
     }
-    const Seg s = segment(P, b);
-    const int nvalid = min(BM, s.lq - qt * BM);
-    if (nvalid <= 0) continue;
-    float4 acc[(192 * BM / 4 + RC_THREADS - 1) / RC_THREADS];
+    b = lo;
+    qt = t - __ldg(P.tile_off + b);
+  } else {
+    qt = r % ntq;
+    b = r / ntq;
+    t = r;
+  }
+  const Seg s = segment(P, b);
+  const int nvalid = min(BM, s.lq - qt * BM);
+  if (nvalid <= 0) return;
+  float4 acc[NACC];
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(acc) / sizeof(acc[0])); ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add_tile = [&](const float* src) {
-      const float4* s4 = reinterpret_cast<const float4*>(src);
+  for (int i = 0; i < NACC; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // acc += tile a, then acc += tile b (b may be null); both tiles' loads are
+  // issued before the first add, the order of the additions stays a then b
+  auto add_tiles = [&](const float* a, const float* bt) {
+    float4 xa[NACC], xb[NACC];
 #pragma unroll
-      for (int i = 0; i < (int)(sizeof(acc) / sizeof(acc[0])); ++i) {
-        const int v = threadIdx.x + i * RC_THREADS;
-        if (v < nv4) {
-          const float4 x = __ldcs(s4 + v);
-          acc[i].x += x.x; acc[i].y += x.y; acc[i].z += x.z; acc[i].w += x.w;
-        }
+    for (int i = 0; i < NACC; ++i) {
+      const int v = threadIdx.x + i * RC_THREADS;
+      xa[i] = v < nv4 ? __ldcs(reinterpret_cast<const float4*>(a) + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+      xb[i] = (bt && v < nv4) ? __ldcs(reinterpret_cast<const float4*>(bt) + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < NACC; ++i) {
+      acc[i].x += xa[i].x; acc[i].y += xa[i].y; acc[i].z += xa[i].z; acc[i].w += xa[i].w;
+    }
+    if (bt) {
+#pragma unroll
+      for (int i = 0; i < NACC; ++i) {
+        acc[i].x += xb[i].x; acc[i].y += xb[i].y; acc[i].z += xb[i].z; acc[i].w += xb[i].w;
       }
-    };
-    if (P.det) {
-      const MaskArgs m = mask_args(P.mask, P.left, P.right, s.lq, s.lk);
-      int nkv = cdiv(s.lk, BN);
-      if (nkv > P.nsplits) nkv = P.nsplits;   // guards cu_seqlens that broke their bound
-      for (int kt = 0; kt < nkv; ++kt) {
+    }
+  };
+  if (P.det) {
+    const MaskArgs m = mask_args(P.mask, P.left, P.right, s.lq, s.lk);
+    int nkv = cdiv(s.lk, BN);
+    if (nkv > P.nsplits) nkv = P.nsplits;   // guards cu_seqlens that broke their bound
+    // the slices whose KV tile reaches query tile qt, two at a time, ascending
+    auto next = [&](int kt) {
+      for (; kt < nkv; ++kt) {
         int lo, hi;
         qtile_range(m, s.lq, s.lk, kt, lo, hi);
-        if (qt >= lo && qt < hi) add_tile(dq_tile(P, kt, h, t));
+        if (qt >= lo && qt < hi) break;
       }
-    } else if (s.lk > 0) {
-      add_tile(dq_tile(P, 0, h, t));
+      return kt;
+    };
+    for (int k0 = next(0); k0 < nkv;) {
+      const int k1 = next(k0 + 1);
+      add_tiles(dq_tile(P, k0, h, t), k1 < nkv ? dq_tile(P, k1, h, t) : nullptr);
+      k0 = k1 < nkv ? next(k1 + 1) : nkv;
     }
-    __syncthreads();
+  } else if (s.lk > 0) {
+    add_tiles(dq_tile(P, 0, h, t), nullptr);
+  }
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(acc) / sizeof(acc[0])); ++i) {
-      const int v = threadIdx.x + i * RC_THREADS;
-      if (v < nv4) {
-        if (P.det) {                 // query-major tiles: 4 consecutive d of one query
-          const int c = (4 * v) / dqk, e = (4 * v) % dqk;
-          float* dst = tile + e * (BM + 1) + c;
-          dst[0] = acc[i].x; dst[BM + 1] = acc[i].y; dst[2 * (BM + 1)] = acc[i].z; dst[3 * (BM + 1)] = acc[i].w;
-        } else {                     // d-major tile: 4 consecutive queries of one d
-          const int e = (4 * v) / BM, c = (4 * v) % BM;
-          float* dst = tile + e * (BM + 1) + c;
-          dst[0] = acc[i].x; dst[1] = acc[i].y; dst[2] = acc[i].z; dst[3] = acc[i].w;
-        }
-      }
-    }
-    __syncthreads();
-    const int nch = dqk / 8;                 // 8-element chunks per dQ row
-    for (int u = threadIdx.x; u < nvalid * nch; u += RC_THREADS) {
-      const int c = u / nch, ch = u - c * nch;
-      T outv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) outv[k] = TypeOps<T>::from_f(tile[(ch * 8 + k) * (BM + 1) + c] * P.scale);
-      T* row = dQ + ((long long)(s.q0 + qt * BM + c) * P.hq + h) * dqk + ch * 8;
+  for (int i = 0; i < NACC; ++i) {
+    const int v = threadIdx.x + i * RC_THREADS;
+    const int c = (4 * v) / dqk, e = (4 * v) - c * dqk;   // query row, first d
+    if (v < nv4 && c < nvalid) {
+      T* row = dQ + ((long long)(s.q0 + qt * BM + c) * P.hq + h) * dqk + e;
+      T o4[4] = {TypeOps<T>::from_f(acc[i].x * P.scale), TypeOps<T>::from_f(acc[i].y * P.scale),
+                 TypeOps<T>::from_f(acc[i].z * P.scale), TypeOps<T>::from_f(acc[i].w * P.scale)};
       if (sizeof(T) == 2) {
-        *reinterpret_cast<uint4*>(row) = *reinterpret_cast<uint4*>(outv);
+        *reinterpret_cast<uint2*>(row) = *reinterpret_cast<uint2*>(o4);
       } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) row[k] = outv[k];
+        for (int k = 0; k < 4; ++k) row[k] = o4[k];
       }
     }
-    __syncthreads();
   }
 }
 
+template <typename T>
+static void launch_rc(const Problem& P, unsigned grid, cudaStream_t st) {
+  const int nacc = cdiv(P.dqk * BM / 4, RC_THREADS);
+  if (nacc <= 4) reduce_convert_kernel<T, 4><<<grid, RC_THREADS, 0, st>>>(P);
+  else if (nacc <= 8) reduce_convert_kernel<T, 8><<<grid, RC_THREADS, 0, st>>>(P);
+  else reduce_convert_kernel<T, 12><<<grid, RC_THREADS, 0, st>>>(P);
+}
+
 void launch_reduce_convert(const Problem& P, cudaStream_t st) {
-  const long long work = (long long)P.hq * P.ntiles;
+  const long long work = (long long)P.hq * P.ntiles;   // one block per (head, query tile)
   if (work <= 0) return;
-  const int grid = (int)(work < (long long)num_sms() * 16 ? work : (long long)num_sms() * 16);
-  const size_t smem = (size_t)P.dqk * (BM + 1) * sizeof(float);
   switch (P.dtype) {
-    case ATTN_BF16:
-      cudaFuncSetAttribute(reduce_convert_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      reduce_convert_kernel<__nv_bfloat16><<<grid, RC_THREADS, smem, st>>>(P);
-      break;
-    case ATTN_FP16:
-      cudaFuncSetAttribute(reduce_convert_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      reduce_convert_kernel<__half><<<grid, RC_THREADS, smem, st>>>(P);
-      break;
-    default:
-      cudaFuncSetAttribute(reduce_convert_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      reduce_convert_kernel<float><<<grid, RC_THREADS, smem, st>>>(P);
-      break;
+    case ATTN_BF16: launch_rc<__nv_bfloat16>(P, (unsigned)work, st); break;
+    case ATTN_FP16: launch_rc<__half>(P, (unsigned)work, st); break;
+    default: launch_rc<float>(P, (unsigned)work, st); break;
   }
 }
 

@@ -63,7 +63,7 @@ struct Problem {
   int max_items;
   int* tile_off;     // group mode: first query-tile index of each segment [nseg+1]
   int ntiles;        // query tiles per (slice, head): B*ceil(Sq/BM) or an upper bound
-  float* dq_acc;     // [nsplits][Hq][ntiles] tiles of BM x dqk fp32 (see dq_tile)
+  float* dq_acc;     // [nsplits][Hq][ntiles] query-major tiles of BM x dqk fp32 (see dq_tile)
   long long n_lse;   // rows of the LSE layout = B*Hq*Sq or Hq*Tq
 };
 
@@ -147,9 +147,8 @@ __device__ __forceinline__ int qtile_index(const Problem& P, int b, int qt) {
   return P.group ? __ldg(P.tile_off + b) + qt : b * cdiv(P.sq, BM) + qt;
 }
 
-// First float of the dQ tile (slice j, head h, query tile t), BM x dqk fp32:
-// deterministic slices are query-major ([BM][dqk]), the single atomic slice
-// is d-major ([dqk][BM], the layout of the dQ^T accumulator).
+// First float of the dQ tile (slice j, head h, query tile t), BM x dqk fp32,
+// query-major ([BM][dqk]) in every slice.
 __device__ __forceinline__ float* dq_tile(const Problem& P, int j, int h, int t) {
   return P.dq_acc + (((long long)j * P.hq + h) * P.ntiles + t) * (long long)P.dqk * BM;
 }

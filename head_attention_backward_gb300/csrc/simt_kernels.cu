@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
         for (int rr = 0; rr < BN; ++rr) a += sdS[rr * (BM + 1) + c] * sK[rr * ks + e];
         float* tile = dq_tile(P, P.det ? kt : 0, h, qtile_index(P, b, qt));
         if (P.det) tile[c * dqk + e] = a;
-        else atomicAdd(tile + e * BM + c, a);
+        else atomicAdd(tile + c * dqk + e, a);
       }
     }
   }

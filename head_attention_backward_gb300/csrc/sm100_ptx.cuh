@@ -144,6 +144,11 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* desc, const
                : "memory");
 }
 
+// fp32 reduction into global memory (no return value)
+__device__ __forceinline__ void red_add_f32(float* gdst, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gdst), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until every committed bulk group has finished reading shared memory.

@@ -10,21 +10,22 @@
 //   S^T  = K Q^T                 (M = keys,  N = queries, K = d_qk)   SMEM x SMEM
 //   dP^T = V dO^T                (M = keys,  N = queries, K = d_v)    SMEM x SMEM
 //   P^T  = exp(s S^T - LSE),  dS^T = P^T o (dP^T - D)      (CUDA cores)
-//   dQ^T = K^T dS^T              (M = d_qk,  N = queries, K = keys)   SMEM x SMEM
 //   dV  += P^T dO                (M = keys,  N = d_v,     K = queries) TMEM x SMEM
-//   dK  += dS^T Q                (M = keys,  N = d_qk,    K = queries) TMEM x SMEM
+//   dK  += dS^T Q                (M = keys,  N = d_qk,    K = queries) SMEM x SMEM
+//   dQ^T = K^T dS^T              (M = d_qk,  N = queries, K = keys)   SMEM x SMEM
 //
-// dK and dV accumulate in TMEM across the item and are written once, scaled.
-// Each dQ^T partial (d_qk x 64 fp32) goes through a shared-memory staging
-// tile to one contiguous tile of the dq_acc workspace with a TMA bulk copy:
-// a plain store into the item's split slice (deterministic mode) or an fp32
-// bulk reduce-add into the single slice.  This is the persistent,
-// deterministic split-dQ design of aiter PR #2216 (Motivation) re-derived for
-// TMA + tcgen05 + TMEM.
+// P^T (TMEM) and dS^T (shared memory) are double-buffered by step parity, so
+// the P/dS warps fill one buffer while the MMAs of the previous step still
+// read the other.  dK and dV accumulate in TMEM across the item and are
+// written once, scaled.  Each dQ^T partial (d_qk x 64 fp32) is drained from
+// TMEM by four warps: stored query-major into the item's split slice of the
+// dq_acc workspace (deterministic mode), or added with fp32 vector reductions
+// into the single slice.  This is the persistent, deterministic split-dQ
+// design of aiter PR #2216 (Motivation) re-derived for TMA + tcgen05 + TMEM.
 //
 // Warp roles (736 threads): warp 0 loads (TMA for Q/dO/K/V plus the LSE/D
 // rows of each query tile) and fetches work items; warp 1 allocates TMEM and
-// one lane issues the dQ^T/dV/dK MMAs; warp 22's lane issues the S^T/dP^T
+// one lane issues the dV/dK/dQ^T MMAs; warp 22's lane issues the S^T/dP^T
 // MMAs; warps 2-17 turn S/dP into P/dS (one key row per thread, 16 query
 // columns per warp); warps 18-21 drain dQ partials and the final dK/dV.
 // Every mbarrier wait is
@@ -50,7 +51,6 @@ constexpr int FIRST_SOFTMAX_WARP = 2;
 constexpr int FIRST_EPI_WARP = FIRST_SOFTMAX_WARP + NUM_SOFTMAX_WARPS;
 constexpr int SDP_ISSUER_WARP = FIRST_EPI_WARP + NUM_EPI_WARPS;   // issues the S / dP MMAs
 constexpr int NUM_THREADS = 32 * (SDP_ISSUER_WARP + 1);
-constexpr int EPI_BARRIER_ID = 1;
 constexpr int NI = 2;                       // work-item ring slots
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t SLEEP_HINT_NS = 20000;   // longest single sleep inside a wait
@@ -58,7 +58,6 @@ constexpr uint32_t TMEM_COLS = 512;
 
 struct TmaMaps {
   CUtensorMap q, k, v, dout;
-  CUtensorMap acc;   // dq_acc as 2-D fp32 [rows][BM], boxes of 32 x 64, 128-byte swizzle
 };
 
 template <int DQK, int DV>
@@ -76,25 +75,24 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NCK_PAD * KCH;
   static constexpr int OFF_Q = OFF_V + NCV * KCH;
   static constexpr int OFF_DO = OFF_Q + ST * NCK * QCH;
-  static constexpr int OFF_DS = OFF_DO + ST * NCV * QCH;   // dS^T, bf16 [128 keys][64 queries]
-  static constexpr int OFF_STAGE = OFF_DS + BN * BM * 2;   // dQ^T staging: 2 x [128 rows][32 fp32], swizzled
-  static constexpr int OFF_L = OFF_STAGE + 128 * BM * 4;   // [ST][BM] -LSE*log2(e)
+  static constexpr int DS_BYTES = BN * BM * 2;            // one dS^T buffer, bf16 [128 keys][64 queries]
+  static constexpr int OFF_DS = OFF_DO + ST * NCV * QCH;   // two dS^T buffers (steps alternate)
+  static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;      // [ST][BM] -LSE*log2(e)
   static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
   static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
   static constexpr int NBAR = 16 + 2 * ST + 2 * NI;
   static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MISC = OFF_RING + NI * 16;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
-  // TMEM column map; P^T and dS^T (bf16, two per column) are MMA A operands
+  // TMEM column map; the two P^T buffers (bf16, two per column) are MMA A operands
   static constexpr int T_DK = 0;
   static constexpr int T_DV = DQK;
   static constexpr int T_S = DQK + DV;
   static constexpr int T_DP = T_S + BM;
   static constexpr bool ALIAS = T_DP + BM + NMB * BM + BM > (int)TMEM_COLS;
   static constexpr int T_DQ = ALIAS ? T_S : T_DP + BM;
-  static constexpr int T_P = ALIAS ? T_DP + BM : T_DQ + NMB * BM;
-  static constexpr int T_DS = T_P + BM / 2;
-  static_assert(T_DS + BM / 2 <= (int)TMEM_COLS, "TMEM overflow");
+  static constexpr int T_P = ALIAS ? T_DP + BM : T_DQ + NMB * BM;   // P^T buffers 0 and 1
+  static_assert(T_P + BM <= (int)TMEM_COLS, "TMEM overflow");
   static_assert(!ALIAS || T_S + NMB * BM <= T_P, "aliased dQ must fit in S and dP");
   static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
   static constexpr uint32_t KV_BYTES = (NCK + NCV) * KCH;
@@ -102,9 +100,10 @@ struct Cfg {
 };
 
 // barrier indices
+// (B_PDS_FULL and B_PDS_EMPTY are pairs: one barrier per P/dS buffer)
 enum {
-  B_KV_FULL = 0, B_KV_EMPTY, B_SDP_FULL, B_SDP_EMPTY, B_PDS_FULL, B_PDS_EMPTY,
-  B_DQ_FULL, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_DRAIN2, B_FIXED_END = 16
+  B_KV_FULL = 0, B_KV_EMPTY, B_SDP_FULL, B_SDP_EMPTY, B_PDS_FULL, B_PDS_EMPTY = B_PDS_FULL + 2,
+  B_DQ_FULL = B_PDS_EMPTY + 2, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_DRAIN2, B_FIXED_END = 16
 };
 
 struct Ctx {
@@ -218,8 +217,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     mbar_init(bar + B_KV_EMPTY, 1);
     mbar_init(bar + B_SDP_FULL, 1);
     mbar_init(bar + B_SDP_EMPTY, NUM_SOFTMAX_WARPS);
-    mbar_init(bar + B_PDS_FULL, NUM_SOFTMAX_WARPS);
-    mbar_init(bar + B_PDS_EMPTY, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar + B_PDS_FULL + b, NUM_SOFTMAX_WARPS);
+      mbar_init(bar + B_PDS_EMPTY + b, 1);
+    }
     mbar_init(bar + B_DQ_FULL, 1);
     mbar_init(bar + B_DQ_EMPTY, NUM_EPI_WARPS);
     mbar_init(bar + B_DKV_FULL, 1);
@@ -327,7 +328,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);          // K-major
       const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
       const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::KCH, 1024);     // MN-major
-      const uint64_t ddS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::KCH, 1024);
+      const uint64_t ddS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::KCH, 1024);   // dQ^T B operand
+      const uint64_t ddS_k = sdesc_sw128(smem_u32(smem + C::OFF_DS), 16, 1024);        // dK A operand
       const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
       const uint64_t ddO_k = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
       const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::QCH, 1024);
@@ -368,38 +370,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         stat_add(g_wait_stats, 9, 1ull);                                   // steps
 #endif
       };
-      // P^T / dS^T of step gs are in TMEM and smem (and the dQ TMEM is free).
-      auto wait_bwd = [&](uint32_t gs) -> bool {
-        return wait_bar(ctx, B_PDS_FULL, gs & 1, 15) &&
-               (C::ALIAS || wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16));
+      // P^T / dS^T of step gs are in their buffer (gs & 1): P^T in TMEM, dS^T
+      // in shared memory.
+      auto wait_pds = [&](uint32_t gs) -> bool {
+        return wait_bar(ctx, B_PDS_FULL + (gs & 1), (gs >> 1) & 1, 15);
       };
-      // dQ^T = K^T dS^T, dV += P^T dO, dK += dS^T Q of step gs.
-      auto mma_bwd = [&](uint32_t gs, uint32_t acc_first) {
+      // dV += P^T dO (P^T from TMEM) and dK += dS^T Q (dS^T from shared
+      // memory, K-major) of step gs; their commit frees the Q/dO stage.
+      auto mma_dvdk = [&](uint32_t gs, uint32_t acc_first) {
 #ifdef ATTN_WAIT_STATS
         const long long t0 = clock64();
 #endif
-        const uint32_t st = gs % C::ST;
+        const uint32_t st = gs % C::ST, pb = gs & 1;
+        const uint64_t q = dQ_mn + ((st * C::NCK * C::QCH) >> 4), d = ddO_mn + ((st * C::NCV * C::QCH) >> 4);
+        const uint64_t a_ds = ddS_k + ((pb * C::DS_BYTES) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          umma_ts(tmem + C::T_DV, tmem + C::T_P + pb * (BM / 2) + ks * 8, d + ((ks * 2048) >> 4), ID_DV,
+                  ks > 0 ? 1u : acc_first);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          umma_ss(tmem + C::T_DK, a_ds + ((ks * 32) >> 4), q + ((ks * 2048) >> 4), ID_DK, ks > 0 ? 1u : acc_first);
+        umma_commit(bar + B_Q_EMPTY + st);
+#ifdef ATTN_WAIT_STATS
+        stat_add(g_wait_stats, 5, (unsigned long long)(clock64() - t0));   // dV/dK group issue
+#endif
+      };
+      // The dQ^T TMEM of the previous step has been drained.
+      auto wait_dq = [&](uint32_t gs) -> bool {
+        return C::ALIAS || wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16);
+      };
+      // dQ^T = K^T dS^T of step gs; its commit also frees the P/dS buffer.
+      auto mma_dq = [&](uint32_t gs) {
+        const uint32_t pb = gs & 1;
+        const uint64_t b_ds = ddS_mn + ((pb * C::DS_BYTES) >> 4);
 #pragma unroll
         for (int mb = 0; mb < C::NMB; ++mb) {
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks) {
             umma_ss(tmem + C::T_DQ + mb * BM, dK_mn + ((mb * 2 * C::KCH + ks * 2048) >> 4),
-                    ddS_mn + ((ks * 2048) >> 4), ID_DQ, ks > 0);
+                    b_ds + ((ks * 2048) >> 4), ID_DQ, ks > 0);
           }
         }
         umma_commit(bar + B_DQ_FULL);
-        const uint64_t q = dQ_mn + ((st * C::NCK * C::QCH) >> 4), d = ddO_mn + ((st * C::NCV * C::QCH) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks)   // dV += P^T dO, P^T from TMEM
-          umma_ts(tmem + C::T_DV, tmem + C::T_P + ks * 8, d + ((ks * 2048) >> 4), ID_DV, ks > 0 ? 1u : acc_first);
-#pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks)   // dK += dS^T Q, dS^T from TMEM
-          umma_ts(tmem + C::T_DK, tmem + C::T_DS + ks * 8, q + ((ks * 2048) >> 4), ID_DK, ks > 0 ? 1u : acc_first);
-        umma_commit(bar + B_PDS_EMPTY);
-        umma_commit(bar + B_Q_EMPTY + st);
-#ifdef ATTN_WAIT_STATS
-        stat_add(g_wait_stats, 5, (unsigned long long)(clock64() - t0));   // dQ/dV/dK group issue
-#endif
+        umma_commit(bar + B_PDS_EMPTY + pb);
       };
       while (ok) {
         const int slot = n_item % NI;
@@ -421,9 +435,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
         } else {
           if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17))) break;
           for (uint32_t gs = g; gs <= last; ++gs) {
-            if (!(ok = wait_bwd(gs))) break;
+            if (!(ok = wait_pds(gs))) break;
             tc_fence_after();
-            mma_bwd(gs, gs != g);
+            mma_dvdk(gs, gs != g);
+            if (!(ok = wait_dq(gs))) break;
+            tc_fence_after();
+            mma_dq(gs);
           }
           if (!ok) break;
           // the item's last dQ/dV/dK followed its last P/dS, which followed
@@ -447,7 +464,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     constexpr int CW = SOFTMAX_COLS;
     const int c0 = grp * CW;
-    uint8_t* dsRow = smem + C::OFF_DS + r * 128;
+    uint8_t* dsRow = smem + C::OFF_DS + r * 128;         // row r of dS^T buffer 0
     const float2 sl2 = make_float2(P.scale_log2, P.scale_log2);
     uint32_t g = 0, n_item = 0;
     while (true) {
@@ -506,21 +523,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
             dk[c >> 1] = pack2(ds.x, ds.y, (T*)nullptr);
           }
         }
-        if (!(ok = wait_bar(ctx, B_PDS_EMPTY, (gs & 1) ^ 1, 23))) break;
+        // P^T and dS^T go to buffer gs & 1; the other one may still be read
+        // by the previous step's dV / dK / dQ^T MMAs
+        const uint32_t pb = gs & 1;
+        if (!(ok = wait_bar(ctx, B_PDS_EMPTY + pb, ((gs >> 1) & 1) ^ 1, 23))) break;
         tc_fence_after();
-        tmem_st8(lane_addr + C::T_P + c0 / 2, pk);
-        tmem_st8(lane_addr + C::T_DS + c0 / 2, dk);
+        tmem_st8(lane_addr + C::T_P + pb * (BM / 2) + c0 / 2, pk);
 #pragma unroll
         for (int j = 0; j < CW / 8; ++j) {
           const int ch = grp * (CW / 8) + j;
-          *reinterpret_cast<uint4*>(dsRow + ((ch ^ (r & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(dsRow + pb * C::DS_BYTES + ((ch ^ (r & 7)) << 4)) =
               make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
         }
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar + B_PDS_FULL);
+        if (lane == 0) mbar_arrive(bar + B_PDS_FULL + pb);
       }
       if (!ok) break;
       g += I.nsteps;
@@ -529,9 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     // ------------------------------------------------------ dQ / dK / dV out
     const int quarter = warp & 3;
     const int L = quarter * 32 + lane;                 // TMEM lane
-    const bool leader = warp == FIRST_EPI_WARP && lane == 0;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* stage = reinterpret_cast<float*>(smem + C::OFF_STAGE);
     T* dKg = static_cast<T*>(P.dk);
     T* dVg = static_cast<T*>(P.dv_out);
     uint32_t g = 0, it = 0, n_item = 0;
@@ -562,12 +579,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
 #pragma unroll 1
         for (int mb = 0; mb < C::NMB; ++mb) {
           const int rows = min(128, DQK - mb * 128);
-          if (!P.det) {
-            // atomic mode stages the tile for a bulk reduce-add: the staging
-            // buffer is free once the previous tensor copies have read it
-            if (leader) bulk_wait_read_all();
-            named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
-          }
 #pragma unroll 1
           for (int hx = 0; hx < 2; ++hx) {     // query columns 0-31, then 32-63
             uint32_t v[32];
@@ -578,38 +589,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
               __syncwarp();
               if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
             }
-            if (P.det) {
-              // deterministic slice, tile stored query-major ([BM][d_qk]): for
-              // each query the warp's 32 consecutive d values fill one 128-byte
-              // line, written straight from registers (a shared-memory staging
-              // round trip plus TMA store measured ~20% slower on the whole
-              // kernel, 16-byte row-segment stores slower still)
-              if (L < rows) {
-                float* dst = dst_tile + mb * 128 + L + hx * 32 * DQK;
+            if (L < rows) {
+              // tile stored query-major ([BM][d_qk]): for each query the warp's
+              // 32 consecutive d values fill one 128-byte line, written straight
+              // from registers -- a plain store into the item's split slice
+              // (deterministic) or an fp32 reduction into the single slice.  (A
+              // shared-memory staging round trip plus TMA store measured ~20%
+              // slower on the whole kernel, 16-byte row-segment stores slower
+              // still, d-major vector reductions slower again.)
+              float* dst = dst_tile + mb * 128 + L + hx * 32 * DQK;
+              if (P.det) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) __stcg(dst + c * DQK, __uint_as_float(v[c]));
-              }
-            } else {
-              // row L of the dQ^T block -> 128-byte row of staging half hx,
-              // 16-byte chunks XOR-swizzled by L & 7 as TMA expects
-              uint8_t* half_buf = smem + C::OFF_STAGE + hx * (128 * 128);
+              } else {
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(half_buf + L * 128 + ((c ^ (L & 7)) << 4)) =
-                    make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            }
-          }
-          if (!P.det) {
-            fence_proxy_async_smem();
-            named_bar_sync(EPI_BARRIER_ID, 32 * NUM_EPI_WARPS);
-            if (leader) {
-              const int row0 = (int)((dst_tile - P.dq_acc) / BM) + mb * 128;
-              for (int rg = 0; rg < rows; rg += 64) {
-#pragma unroll
-                for (int hx = 0; hx < 2; ++hx)
-                  tma_reduce_add_2d(&maps.acc, smem + C::OFF_STAGE + hx * (128 * 128) + rg * 128, hx * 32, row0 + rg);
+                for (int c = 0; c < 32; ++c) red_add_f32(dst + c * DQK, __uint_as_float(v[c]));
               }
-              bulk_commit();
             }
           }
         }
@@ -660,7 +655,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(bar + B_DKV_EMPTY);
       ++it;
     }
-    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -714,22 +708,6 @@ static bool make_map(CUtensorMap* m, const void* base, bool fp16, int dim, int h
   return r == CUDA_SUCCESS;
 }
 
-// dq_acc viewed as 2-D fp32 [nsplits * Hq * ntiles * d_qk rows][BM columns];
-// boxes of 32 columns x 64 rows with 128-byte swizzle (the staging layout).
-static bool make_acc_map(CUtensorMap* m, const Problem& P) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const unsigned long long rows = (unsigned long long)P.nsplits * P.hq * P.ntiles * P.dqk;
-  cuuint64_t dims[2] = {(cuuint64_t)BM, (cuuint64_t)(rows > 0 ? rows : 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)BM * 4};
-  cuuint32_t box[2] = {32, 64};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P.dq_acc, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int DQK, int DV, typename T>
 static int launch_typed(const Problem& P, cudaStream_t st) {
   using C = Cfg<DQK, DV>;
@@ -738,8 +716,7 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
   const long long rq = P.group ? P.tq : (long long)P.nseg * P.sq;
   const long long rk = P.group ? P.tk : (long long)P.nseg * P.sk;
   if (!make_map(&maps.q, P.q, fp16, DQK, P.hq, rq, BM) || !make_map(&maps.dout, P.dout, fp16, DV, P.hq, rq, BM) ||
-      !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, BN) || !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, BN) ||
-      !make_acc_map(&maps.acc, P))
+      !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, BN) || !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, BN))
     return ATTN_ERR_CUDA;
   auto kern = bwd_tc_kernel<DQK, DV, T>;
   // at least 120 KB so that two CTAs never share an SM (each holds all 512 TMEM columns)
