@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libattn_bwd.so")
 
 ATTN_BF16, ATTN_FP16, ATTN_FP32 = 0, 1, 2
 MASK_NONE, MASK_CAUSAL_TOP_LEFT, MASK_CAUSAL_BOTTOM_RIGHT, MASK_WINDOW = 0, 1, 2, 3
+DET_ATOMIC, DET_ORDERED, DET_SPLIT = 0, 1, 2   # attn_det_t
 STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED_HEADDIM",
           -3: "ATTN_ERR_WORKSPACE_TOO_SMALL", -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_DEVICE_FLAG",
           -6: "ATTN_ERR_TIMEOUT", -7: "ATTN_ERR_BAD_SEQLENS"}
@@ -164,7 +165,7 @@ def bwd_params(q, k, v, o, do, lse, dq, dk, dv, *, scale, mask=MASK_NONE, left=-
     p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
     p.mask, p.window_left, p.window_right = mask, left, right
     p.softmax_scale = scale
-    p.deterministic = 1 if deterministic else 0
+    p.deterministic = int(deterministic)   # False/True or an attn_det_t value (0, 1, 2)
     p.q, p.k, p.v, p.o, p.dout, p.lse = (_ptr(t) for t in (q, k, v, o, do, lse))
     p.dq, p.dk, p.dv = _ptr(dq), _ptr(dk), _ptr(dv)
     return p

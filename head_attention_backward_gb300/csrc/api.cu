@@ -48,6 +48,7 @@ static int validate_common(const Prm* p) {
 static int validate_bwd(const attn_bwd_params* p) {
   int st = validate_common(p);
   if (st != ATTN_OK) return st;
+  if (p->deterministic < ATTN_DET_ATOMIC || p->deterministic > ATTN_DET_SPLIT) return ATTN_ERR_INVALID_ARG;
   if (p->dtype == ATTN_FP32) {
     if (!simt_headdims(p->d_qk, p->d_v)) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   } else if (!tc_headdims(p->d_qk, p->d_v)) {
@@ -91,7 +92,8 @@ static Problem make_problem(const attn_bwd_params& p, void* ws) {
   P.right = p.mask == ATTN_MASK_WINDOW ? p.window_right : -1;
   P.scale = p.softmax_scale;
   P.scale_log2 = p.softmax_scale * 1.4426950408889634f;
-  P.det = p.deterministic ? 1 : 0;
+  P.det = p.deterministic != ATTN_DET_ATOMIC ? 1 : 0;
+  P.fold = L.fold ? 1 : 0;
   P.nsplits = L.nsplits;
   P.q = p.q; P.k = p.k; P.v = p.v; P.o = p.o; P.dout = p.dout; P.lse = p.lse;
   P.dq = p.dq; P.dk = p.dk; P.dv_out = p.dv;
@@ -104,6 +106,8 @@ static Problem make_problem(const attn_bwd_params& p, void* ws) {
   P.tile_off = reinterpret_cast<int*>(w + L.off_tiles);
   P.ntiles = L.ntiles;
   P.dq_acc = reinterpret_cast<float*>(w + L.off_dqacc);
+  P.turn = reinterpret_cast<unsigned*>(w + L.off_turn);
+  P.klo = reinterpret_cast<int*>(w + L.off_klo);
   P.n_lse = L.n_lse;
   return P;
 }
@@ -156,6 +160,7 @@ extern "C" int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes) 
   *bytes = 0;
   const int st = validate_common(p);
   if (st != ATTN_OK) return st;
+  if (p->deterministic < ATTN_DET_ATOMIC || p->deterministic > ATTN_DET_SPLIT) return ATTN_ERR_INVALID_ARG;
   *bytes = ws_layout(*p).total;
   return ATTN_OK;
 }

@@ -41,10 +41,13 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P) {
   }
   __syncthreads();
   if (s_bad) {
+    // no work items and no query tiles: nothing later in the call touches dQ
+    // rows derived from the rejected cu_seqlens
     if (tid == 0) {
       P.hdr[HDR_STATUS] = ATTN_ERR_BAD_SEQLENS;
       P.hdr[HDR_NITEMS] = 0;
     }
+    for (int b = tid; b <= P.nseg; b += blockDim.x) P.tile_off[b] = 0;
     return;
   }
   // KV-tile-major enumeration by warp 0: for kt, for segment, for kv head.
@@ -185,10 +188,24 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem P, long long nt
       if (lane == 0) write_row_stats(P, r, acc);
     }
   }
-  if (!P.det) {
+  if (!P.det || P.fold) {   // the single slice that partials are added into starts at zero
     float4* acc4 = reinterpret_cast<float4*>(P.dq_acc);
     const long long n4 = (long long)P.hq * P.ntiles * P.dqk * BM / 4;
     for (long long i = tid; i < n4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (P.fold) {
+    // ordered fold: no partial folded yet, and the first KV tile reaching
+    // each query tile (a partial's rank is its KV tile minus that one)
+    const long long n = (long long)P.hq * P.ntiles;
+    for (long long i = tid; i < n; i += nthreads) P.turn[i] = 0u;
+    for (long long t = tid; t < P.ntiles; t += nthreads) {
+      int b, qt, k = -1;
+      if (tile_coords(P, (int)t, b, qt)) {
+        const Seg sg = segment(P, b);
+        k = first_kv_tile(mask_args(P.mask, P.left, P.right, sg.lq, sg.lk), sg.lq, sg.lk, qt);
+      }
+      P.klo[t] = k;
+    }
   }
 }
 
@@ -210,9 +227,10 @@ void launch_preprocess(const Problem& P, cudaStream_t st) {
 }
 
 // ----------------------------------------------------------- reduce/convert
-// One block per (query head, query tile).  The query-major dQ tiles of the slices whose KV tile reaches this query tile
-// (the others were never written) are summed in ascending slice order; atomic
-// mode reads the single slice.  Each thread owns four consecutive d of one
+// One block per (query head, query tile).  Split mode: the query-major dQ
+// tiles of the slices whose KV tile reaches this query tile (the others were
+// never written) are summed in ascending slice order; atomic and ordered-fold
+// modes read the single slice.  Each thread owns four consecutive d of one
 // query row, so the scaled sum goes straight to dQ without a transpose.
 
 constexpr int RC_THREADS = 256;
@@ -220,31 +238,18 @@ constexpr int RC_THREADS = 256;
 // NACC = float4 accumulators per thread = ceil(d_qk * BM / 4 / RC_THREADS).
 template <typename T, int NACC>
 __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
+  // a rejected problem (bad cu_seqlens, expired wait) leaves dQ untouched
+  if (*(volatile const int*)(P.hdr + HDR_STATUS) != 0) return;
   const int dqk = P.dqk;
   const int nv4 = dqk * BM / 4;      // float4 per dQ tile
-  const int ntq = cdiv(P.sq, BM);
   T* dQ = static_cast<T*>(P.dq);
   // block -> (head, tile), head-major (measured a few percent faster than
   // interleaving heads or putting the most-loaded causal tiles first)
   const long long w = blockIdx.x;
   const int h = (int)(w / P.ntiles);
-  const int r = (int)(w % P.ntiles);
-  int b, qt, t;
-  if (P.group) {
-    t = r;
-    if (t >= __ldg(P.tile_off + P.nseg)) return;   // beyond the last segment's tiles
-    int lo = 0, hi = P.nseg;                        // largest b with tile_off[b] <= t
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(P.tile_off + mid) <= t) lo = mid; else hi = mid;
-    }
-    b = lo;
-    qt = t - __ldg(P.tile_off + b);
-  } else {
-    qt = r % ntq;
-    b = r / ntq;
-    t = r;
-  }
+  const int t = (int)(w % P.ntiles);
+  int b, qt;
+  if (!tile_coords(P, t, b, qt)) return;   // beyond the last segment's tiles
   const Seg s = segment(P, b);
   const int nvalid = min(BM, s.lq - qt * BM);
   if (nvalid <= 0) return;
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
       }
     }
   };
-  if (P.det) {
+  if (P.det && !P.fold) {
     const MaskArgs m = mask_args(P.mask, P.left, P.right, s.lq, s.lk);
     int nkv = cdiv(s.lk, BN);
     if (nkv > P.nsplits) nkv = P.nsplits;   // guards cu_seqlens that broke their bound
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
       add_tiles(dq_tile(P, k0, h, t), k1 < nkv ? dq_tile(P, k1, h, t) : nullptr);
       k0 = k1 < nkv ? next(k1 + 1) : nkv;
     }
-  } else if (s.lk > 0) {
+  } else if (s.lk > 0) {   // atomic and ordered fold: the single, pre-zeroed slice
     add_tiles(dq_tile(P, 0, h, t), nullptr);
   }
 #pragma unroll

@@ -26,7 +26,7 @@ enum HeaderWord : int {
   HDR_NITEMS = 1,     // number of work items written by the scheduler
   HDR_NEXT = 2,       // dynamic work counter of the persistent kernel
   HDR_DIAG = 3,       // diagnostic word (where a bounded wait expired)
-  HDR_WORDS = 64
+  HDR_WORDS = 128     // words 16+: optional 64-bit wait counters of instrumented builds
 };
 
 struct Problem {
@@ -43,8 +43,9 @@ struct Problem {
   int mask, left, right;
   float scale;
   float scale_log2;  // scale * log2(e)
-  int det;
-  int nsplits;       // dq_acc slices (1 in atomic mode)
+  int det;           // 1: bitwise-repeatable dQ (ordered fold or split slices)
+  int fold;          // 1: ordered fold into one slice (see attn_det_t)
+  int nsplits;       // dq_acc slices (1 unless split slices are used)
   // tensors
   const void* q;
   const void* k;
@@ -64,12 +65,15 @@ struct Problem {
   int* tile_off;     // group mode: first query-tile index of each segment [nseg+1]
   int ntiles;        // query tiles per (slice, head): B*ceil(Sq/BM) or an upper bound
   float* dq_acc;     // [nsplits][Hq][ntiles] query-major tiles of BM x dqk fp32 (see dq_tile)
+  unsigned* turn;    // fold mode: [Hq][ntiles] partials folded so far per query tile
+  int* klo;          // fold mode: [ntiles] first KV tile that reaches each query tile
   long long n_lse;   // rows of the LSE layout = B*Hq*Sq or Hq*Tq
 };
 
 struct WsLayout {
-  size_t off_hdr, off_lse2, off_dvec, off_items, off_tiles, off_dqacc, total;
+  size_t off_hdr, off_lse2, off_dvec, off_items, off_tiles, off_turn, off_klo, off_dqacc, total;
   int max_items, nsplits, ntiles;
+  bool fold;
   long long n_lse;
 };
 
@@ -78,12 +82,19 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Workspace layout: pure function of the scalar problem fields, used by both
 // attn_bwd_workspace_size and attn_bwd.
+// Deterministic dQ by the ordered fold: the tensor-core kernel in
+// ATTN_DET_ORDERED mode (the fp32 kernel always uses split slices).
+inline bool det_fold(const attn_bwd_params& p) {
+  return p.deterministic == ATTN_DET_ORDERED && p.dtype != ATTN_FP32;
+}
+
 inline WsLayout ws_layout(const attn_bwd_params& p) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   WsLayout L{};
   const bool group = p.cu_seqlens_q != nullptr;
   L.n_lse = group ? (long long)p.nhead_q * p.total_q : (long long)p.batch * p.nhead_q * p.seqlen_q;
-  L.nsplits = p.deterministic ? cdiv(p.seqlen_k > 0 ? p.seqlen_k : 1, BN) : 1;
+  L.fold = det_fold(p);
+  L.nsplits = p.deterministic && !L.fold ? cdiv(p.seqlen_k > 0 ? p.seqlen_k : 1, BN) : 1;
   long long nkv_tiles;
   if (group) {
     long long a = (long long)p.total_k / BN + p.batch;
@@ -107,6 +118,8 @@ inline WsLayout ws_layout(const attn_bwd_params& p) {
   L.off_dvec = o;  o = up(o + (size_t)L.n_lse * sizeof(float));
   L.off_items = o; o = up(o + (size_t)(L.max_items > 0 ? L.max_items : 1) * sizeof(int4));
   L.off_tiles = o; o = up(o + (size_t)(p.batch + 1) * sizeof(int));
+  L.off_turn = o;  o = up(o + (L.fold ? (size_t)p.nhead_q * L.ntiles : 1) * sizeof(unsigned));
+  L.off_klo = o;   o = up(o + (L.fold ? (size_t)L.ntiles : 1) * sizeof(int));
   L.off_dqacc = o;
   o = up(o + (size_t)L.nsplits * p.nhead_q * (size_t)L.ntiles * p.d_qk * BM * sizeof(float));
   L.total = o;
@@ -151,6 +164,27 @@ __device__ __forceinline__ int qtile_index(const Problem& P, int b, int qt) {
 // query-major ([BM][dqk]) in every slice.
 __device__ __forceinline__ float* dq_tile(const Problem& P, int j, int h, int t) {
   return P.dq_acc + (((long long)j * P.hq + h) * P.ntiles + t) * (long long)P.dqk * BM;
+}
+
+// Global query-tile index t -> (segment b, segment-local query tile qt); false
+// for indices past the last segment's tiles.  Batch mode: t = b * ceil(Sq /
+// BM) + qt; group mode: the tile_off prefix written by the scheduler.
+__device__ __forceinline__ bool tile_coords(const Problem& P, int t, int& b, int& qt) {
+  if (P.group) {
+    if (t >= __ldg(P.tile_off + P.nseg)) return false;
+    int lo = 0, hi = P.nseg;                 // largest b with tile_off[b] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(P.tile_off + mid) <= t) lo = mid; else hi = mid;
+    }
+    b = lo;
+    qt = t - __ldg(P.tile_off + b);
+  } else {
+    const int ntq = cdiv(P.sq, BM);
+    b = t / ntq;
+    qt = t - b * ntq;
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------------- mask
@@ -203,6 +237,32 @@ __host__ __device__ inline void qtile_range(const MaskArgs& m, int lq, int lk, i
   if (qlo > qhi) return;
   lo = (int)(qlo / BM);
   hi = (int)(qhi / BM) + 1;
+}
+
+// First KV tile whose range (qtile_range) holds query tile qt, or -1 if none
+// does.  Ranges only move forward with the KV tile: the tiles before the
+// reached ones end at or before qt (hi <= qt), the ones after start past it or
+// are empty past the last query or key.  Binary search for the first tile that
+// is not "before", then check that it reaches qt.
+__host__ __device__ inline int first_kv_tile(const MaskArgs& m, int lq, int lk, int qt) {
+  const int nkv = (lk + BN - 1) / BN;
+  auto before = [&](int kt) {
+    int lo, hi;
+    qtile_range(m, lq, lk, kt, lo, hi);
+    if (lo < hi) return hi <= qt;
+    // empty range: before the reached tiles when no query reaches this far
+    // back (the left window ends before the tile), after them otherwise
+    return m.left >= 0 && (long long)(kt * BN + BN - 1) - m.off + m.left < 0;
+  };
+  int lo = 0, hi = nkv;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (before(mid)) lo = mid + 1; else hi = mid;
+  }
+  if (lo >= nkv) return -1;
+  int a, b;
+  qtile_range(m, lq, lk, lo, a, b);
+  return (a <= qt && qt < b) ? lo : -1;
 }
 
 // ------------------------------------------------------------------- types

@@ -144,6 +144,24 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* desc, const
                : "memory");
 }
 
+// gpu-scope acquire load / release store of a 32-bit flag in global memory
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // fp32 reduction into global memory (no return value)
 __device__ __forceinline__ void red_add_f32(float* gdst, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gdst), "f"(v) : "memory");

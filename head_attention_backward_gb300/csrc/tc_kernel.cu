@@ -51,6 +51,17 @@ constexpr int FIRST_SOFTMAX_WARP = 2;
 constexpr int FIRST_EPI_WARP = FIRST_SOFTMAX_WARP + NUM_SOFTMAX_WARPS;
 constexpr int SDP_ISSUER_WARP = FIRST_EPI_WARP + NUM_EPI_WARPS;   // issues the S / dP MMAs
 constexpr int NUM_THREADS = 32 * (SDP_ISSUER_WARP + 1);
+// ordered fold only: one more warp, whose lane 0 acquires the turns of
+// upcoming dQ partials and passes them on once the drain warps' adds are
+// issued (a 25th warp would cut the per-thread register budget from 80 to 72)
+constexpr int TURN_WARP = SDP_ISSUER_WARP + 1;
+constexpr int NUM_THREADS_FOLD = 32 * (TURN_WARP + 1);
+// dQ accumulation of a kernel instantiation (each carries only its own path)
+enum : int { DQ_ATOMIC = 0, DQ_FOLD = 1, DQ_SPLIT = 2 };
+template <int DQM> constexpr int kernel_threads() { return DQM == DQ_FOLD ? NUM_THREADS_FOLD : NUM_THREADS; }
+constexpr int NT = 2;                       // turn slots between the acquirer and the drain
+constexpr int NR = 4;                       // release slots between the drain and the turn thread
+constexpr int ND = 8;                       // turn-thread records of acquired, unreleased steps
 constexpr int NI = 2;                       // work-item ring slots
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t SLEEP_HINT_NS = 20000;   // longest single sleep inside a wait
@@ -80,10 +91,10 @@ struct Cfg {
   static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;      // [ST][BM] -LSE*log2(e)
   static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
   static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
-  static constexpr int NBAR = 16 + 2 * ST + 2 * NI;
+  static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NT + 2 * NR;
   static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MISC = OFF_RING + NI * 16;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + ND * 8 + 1024;  // + alignment slack
   // TMEM column map; the two P^T buffers (bf16, two per column) are MMA A operands
   static constexpr int T_DK = 0;
   static constexpr int T_DV = DQK;
@@ -113,14 +124,14 @@ struct Ctx {
 };
 
 #ifdef ATTN_WAIT_STATS
-__shared__ unsigned long long g_wait_stats[24];
+__shared__ unsigned long long g_wait_stats[48];
 #endif
 
 #ifdef ATTN_WAIT_STATS
 // Optional instrumentation (off in normal builds): cycles each warp's lane 0
 // spent blocked at every wait site, summed per CTA in shared memory and added
 // to workspace header words [16 + 2*site] as 64-bit counters at exit.
-constexpr int N_WAIT_SITES = 24;
+constexpr int N_WAIT_SITES = 48;
 __device__ __forceinline__ void stat_add(unsigned long long* s, int where, unsigned long long v) {
   if ((threadIdx.x & 31) == 0) atomicAdd(s + (where % N_WAIT_SITES), v);
 }
@@ -171,6 +182,16 @@ __device__ __forceinline__ ItemInfo item_info(const Problem& P, int4 it) {
   return I;
 }
 
+// Step s of an item -> (query head h, query tile qt).  The G query heads of
+// the kv head are the inner loop and query tiles run from the last down, so
+// that under the KV-tile-major item order the dQ partials of one query tile
+// reach the ordered fold roughly in ascending KV-tile order.
+__device__ __forceinline__ void step_coords(const Problem& P, const ItemInfo& I, int s, int& h, int& qt) {
+  const int j = s / P.g;
+  h = I.hk * P.g + (s - j * P.g);
+  qt = I.qlo + I.nq - 1 - j;
+}
+
 template <typename T> struct IsHalf { static constexpr bool value = false; };
 template <> struct IsHalf<__half> { static constexpr bool value = true; };
 
@@ -183,9 +204,10 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int DQK, int DV, typename T>
-__global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_constant__ TmaMaps maps, const Problem P) {
+template <int DQK, int DV, typename T, int DQM>
+__global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const __grid_constant__ TmaMaps maps, const Problem P) {
   using C = Cfg<DQK, DV>;
+  constexpr bool FOLD = DQM == DQ_FOLD;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -199,11 +221,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
   const Ctx ctx{bar, abort_flag, P.hdr};
   const int B_Q_FULL = B_FIXED_END, B_Q_EMPTY = B_FIXED_END + C::ST;
   const int B_IT_FULL = B_FIXED_END + 2 * C::ST, B_IT_EMPTY = B_IT_FULL + NI;
+  // ordered fold: turn acquired (acquirer -> drain) / slot free (drain ->
+  // acquirer); adds issued (drain -> releaser) / slot free (releaser -> drain)
+  const int B_TURN_OK = B_IT_EMPTY + NI, B_TURN_FREE = B_TURN_OK + NT;
+  const int B_REDS_DONE = B_TURN_FREE + NT, B_REDS_FREE = B_REDS_DONE + NR;
+  constexpr int NTHREADS = kernel_threads<DQM>();
 
   // zero the k padding chunks read by the dQ^T MMA of padded head dims
   if (C::NCK_PAD > C::NCK) {
     uint4* z = reinterpret_cast<uint4*>(smem + C::OFF_K + C::NCK * C::KCH);
-    for (int i = threadIdx.x; i < (C::NCK_PAD - C::NCK) * C::KCH / 16; i += NUM_THREADS)
+    for (int i = threadIdx.x; i < (C::NCK_PAD - C::NCK) * C::KCH / 16; i += NTHREADS)
       z[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
@@ -233,7 +260,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
     }
     for (int s = 0; s < NI; ++s) {
       mbar_init(bar + B_IT_FULL + s, 1);
-      mbar_init(bar + B_IT_EMPTY + s, 2 + NUM_SOFTMAX_WARPS + NUM_EPI_WARPS);
+      mbar_init(bar + B_IT_EMPTY + s, 2 + NUM_SOFTMAX_WARPS + NUM_EPI_WARPS + (FOLD ? 1 : 0));
+    }
+    if (FOLD) {
+      for (int s = 0; s < NT; ++s) {
+        mbar_init(bar + B_TURN_OK + s, 1);
+        mbar_init(bar + B_TURN_FREE + s, NUM_EPI_WARPS);
+      }
+      for (int s = 0; s < NR; ++s) {
+        mbar_init(bar + B_REDS_DONE + s, NUM_EPI_WARPS);
+        mbar_init(bar + B_REDS_FREE + s, 1);
+      }
     }
     fence_mbar_init();
   }
@@ -283,7 +320,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       bool ok = true;
       for (int s = 0; s < I.nsteps; ++s) {
         const uint32_t gs = g + s, st = gs % C::ST;
-        const int h = I.hk * P.g + s / I.nq, qt = I.qlo + s % I.nq;
+        int h, qt;
+        step_coords(P, I, s, h, qt);
         if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
         // -LSE*log2(e) and D of the tile's 64 query rows, copied asynchronously;
         // rows past the segment end read as zeros (their columns are masked)
@@ -482,7 +520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       bool ok = true;
       for (int s = 0; s < I.nsteps; ++s) {
         const uint32_t gs = g + s, st = gs % C::ST;
-        const int qt = I.qlo + s % I.nq;
+        int h, qt;
+        step_coords(P, I, s, h, qt);
         if (!(ok = wait_bar(ctx, B_SDP_FULL, gs & 1, 21))) break;
         tc_fence_after();
         uint32_t sv[CW], dpv[CW];
@@ -544,7 +583,91 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       if (!ok) break;
       g += I.nsteps;
     }
-  } else {
+  } else if (FOLD && warp == TURN_WARP) {
+    // ------------------------------------------- ordered fold: turn thread
+    // Two frontiers, serviced without blocking each other: `rel` passes on the
+    // turn of every step whose adds the drain warps reported (gpu-scope fence,
+    // then the tile's counter), `acq` walks the work items ahead of the drain
+    // warps (at most NT steps) and signals each step once the tile's counter
+    // shows that the partials of all lower KV tiles are folded.  A release
+    // never waits for an acquisition, and every acquisition waits for a lower
+    // KV tile, which an earlier work item holds: the waits cannot form a cycle.
+    if (lane == 0) {
+      uint2* rec = reinterpret_cast<uint2*>(smem + C::OFF_MISC + 64);   // [ND] (counter index, value)
+      uint32_t acq = 0, rel = 0, n_item = 0;
+      ItemInfo I{};
+      int s = 0;
+      bool have_item = false, items_done = false;
+      uint64_t last = globaltimer();
+      while (true) {
+        bool progress = false;
+        if (rel < acq && mbar_test_wait(smem_u32(bar + B_REDS_DONE + rel % NR), (rel / NR) & 1)) {
+          const uint2 r = rec[rel % ND];
+#ifdef ATTN_WAIT_STATS
+          const long long c0 = clock64();
+#endif
+          __threadfence();
+          st_relaxed_gpu(P.turn + r.x, r.y);
+#ifdef ATTN_WAIT_STATS
+          stat_add(g_wait_stats, 34, (unsigned long long)(clock64() - c0));   // release fence
+#endif
+          mbar_arrive(bar + B_REDS_FREE + rel % NR);
+          ++rel;
+          progress = true;
+        }
+        if (!have_item && !items_done) {
+          const int slot = n_item % NI;
+          if (mbar_test_wait(smem_u32(bar + B_IT_FULL + slot), (n_item / NI) & 1)) {
+            const int4 item = ring[slot];
+            mbar_arrive(bar + B_IT_EMPTY + slot);
+            ++n_item;
+            if (item.x < 0) {
+              items_done = true;
+            } else {
+              I = item_info(P, item);
+              s = 0;
+              have_item = I.nsteps > 0;
+            }
+            progress = true;
+          }
+        }
+        if (have_item && acq - rel < ND &&
+            mbar_test_wait(smem_u32(bar + B_TURN_FREE + acq % NT), ((acq / NT) & 1) ^ 1)) {
+          int h, qt;
+          step_coords(P, I, s, h, qt);
+          const int tile = qtile_index(P, I.b, qt);
+          const uint32_t idx = (uint32_t)(h * P.ntiles + tile);
+          const uint32_t rank = (uint32_t)(I.kt - __ldg(P.klo + tile));   // KV tiles before this one
+          if (ld_acquire_gpu(P.turn + idx) == rank) {
+            rec[acq % ND] = make_uint2(idx, rank + 1);
+            mbar_arrive(bar + B_TURN_OK + acq % NT);
+            ++acq;
+            have_item = ++s < I.nsteps;
+            progress = true;
+          }
+#ifdef ATTN_WAIT_STATS
+          else stat_add(g_wait_stats, 35, 1ull);   // turn not there yet at this look
+#endif
+        }
+        if (items_done && !have_item && rel == acq) break;
+        if (progress) {
+          last = globaltimer();
+        } else {
+          if (*(volatile int*)abort_flag || *(volatile int*)(P.hdr + HDR_STATUS) != 0) {
+            *(volatile int*)abort_flag = 1;
+            break;
+          }
+          if (globaltimer() - last > WAIT_LIMIT_NS) {
+            *(volatile int*)abort_flag = 1;
+            atomicCAS(P.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
+            atomicExch(P.hdr + HDR_DIAG, 33);
+            break;
+          }
+          __nanosleep(20);
+        }
+      }
+    }
+  } else if (warp < SDP_ISSUER_WARP) {
     // ------------------------------------------------------ dQ / dK / dV out
     const int quarter = warp & 3;
     const int L = quarter * 32 + lane;                 // TMEM lane
@@ -572,12 +695,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
       bool ok = true;
       for (int s = 0; s < I.nsteps; ++s) {
         const uint32_t gs = g + s;
-        const int h = I.hk * P.g + s / I.nq, qt = I.qlo + s % I.nq;
+        int h, qt;
+        step_coords(P, I, s, h, qt);
+        const int tile = qtile_index(P, I.b, qt);
         if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
         tc_fence_after();
-        float* dst_tile = dq_tile(P, P.det ? I.kt : 0, h, qtile_index(P, I.b, qt));
+        float* dst_tile = dq_tile(P, DQM == DQ_SPLIT ? I.kt : 0, h, tile);
 #pragma unroll 1
-        for (int mb = 0; mb < C::NMB; ++mb) {
+        for (int mb = 0; mb < C::NMB && ok; ++mb) {
           const int rows = min(128, DQK - mb * 128);
 #pragma unroll 1
           for (int hx = 0; hx < 2; ++hx) {     // query columns 0-31, then 32-63
@@ -589,24 +714,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_tc_kernel(const __grid_con
               __syncwarp();
               if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
             }
+            if (FOLD && mb == 0 && hx == 0) {
+              // ordered fold: the partials before this one are in the sum (the
+              // acquirer saw the tile's turn counter reach `rank`)
+              if (!(ok = wait_bar(ctx, B_TURN_OK + gs % NT, (gs / NT) & 1, 36))) break;
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar + B_TURN_FREE + gs % NT);
+            }
             if (L < rows) {
               // tile stored query-major ([BM][d_qk]): for each query the warp's
               // 32 consecutive d values fill one 128-byte line, written straight
-              // from registers -- a plain store into the item's split slice
-              // (deterministic) or an fp32 reduction into the single slice.  (A
-              // shared-memory staging round trip plus TMA store measured ~20%
-              // slower on the whole kernel, 16-byte row-segment stores slower
-              // still, d-major vector reductions slower again.)
+              // from registers.  (A shared-memory staging round trip plus TMA
+              // store measured ~20% slower on the whole kernel, 16-byte
+              // row-segment stores slower still, d-major vector reductions
+              // slower again.)
               float* dst = dst_tile + mb * 128 + L + hx * 32 * DQK;
-              if (P.det) {
+              if constexpr (DQM == DQ_SPLIT) {   // plain store into this KV tile's slice
 #pragma unroll
                 for (int c = 0; c < 32; ++c) __stcg(dst + c * DQK, __uint_as_float(v[c]));
-              } else {
+              } else {   // fp32 reductions into the zeroed slice: in arrival order
+                         // (atomic) or while holding the tile's turn (ordered fold)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) red_add_f32(dst + c * DQK, __uint_as_float(v[c]));
               }
             }
           }
+        }
+        if (!ok) break;
+        if (FOLD) {
+          // this warp's adds of the partial are issued: the releaser passes the
+          // turn on (after a gpu-scope fence) once all four warps report
+          __syncwarp();
+          if (lane == 0) {
+            ok = wait_bar(ctx, B_REDS_FREE + gs % NR, ((gs / NR) & 1) ^ 1, 37);
+            if (ok) mbar_arrive(bar + B_REDS_DONE + gs % NR);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
       }
       if (!ok) break;
@@ -708,7 +852,7 @@ static bool make_map(CUtensorMap* m, const void* base, bool fp16, int dim, int h
   return r == CUDA_SUCCESS;
 }
 
-template <int DQK, int DV, typename T>
+template <int DQK, int DV, typename T, int DQM>
 static int launch_typed(const Problem& P, cudaStream_t st) {
   using C = Cfg<DQK, DV>;
   const bool fp16 = IsHalf<T>::value;
@@ -718,7 +862,7 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
   if (!make_map(&maps.q, P.q, fp16, DQK, P.hq, rq, BM) || !make_map(&maps.dout, P.dout, fp16, DV, P.hq, rq, BM) ||
       !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, BN) || !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, BN))
     return ATTN_ERR_CUDA;
-  auto kern = bwd_tc_kernel<DQK, DV, T>;
+  auto kern = bwd_tc_kernel<DQK, DV, T, DQM>;
   // at least 120 KB so that two CTAs never share an SM (each holds all 512 TMEM columns)
   const int smem = C::SMEM_BYTES > 120 * 1024 ? C::SMEM_BYTES : 120 * 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -729,23 +873,42 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
   int grid = sms > 0 ? sms : 1;
   if (P.max_items < grid) grid = P.max_items;
   if (grid <= 0) return ATTN_OK;
-  kern<<<grid, NUM_THREADS, smem, st>>>(maps, P);
+  // The ordered fold makes CTAs wait for one another (a partial waits for the
+  // partials of lower KV tiles, which items dealt earlier hold), so that mode
+  // is a cooperative launch: all CTAs are co-resident or the launch fails.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kernel_threads<DQM>());
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = DQM == DQ_FOLD ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, maps, P) != cudaSuccess) return ATTN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <typename T>
+template <typename T, int DQM>
 static int launch_dims(const Problem& P, cudaStream_t st) {
-  if (P.dqk == 128 && P.dv == 128) return launch_typed<128, 128, T>(P, st);
-  if (P.dqk == 64 && P.dv == 64) return launch_typed<64, 64, T>(P, st);
-  if (P.dqk == 192 && P.dv == 128) return launch_typed<192, 128, T>(P, st);
+  if (P.dqk == 128 && P.dv == 128) return launch_typed<128, 128, T, DQM>(P, st);
+  if (P.dqk == 64 && P.dv == 64) return launch_typed<64, 64, T, DQM>(P, st);
+  if (P.dqk == 192 && P.dv == 128) return launch_typed<192, 128, T, DQM>(P, st);
   return ATTN_ERR_UNSUPPORTED_HEADDIM;
+}
+
+template <typename T>
+static int launch_mode(const Problem& P, cudaStream_t st) {
+  if (P.fold) return launch_dims<T, DQ_FOLD>(P, st);
+  return P.det ? launch_dims<T, DQ_SPLIT>(P, st) : launch_dims<T, DQ_ATOMIC>(P, st);
 }
 
 }  // namespace tc
 
 int launch_bwd_tc(const Problem& P, cudaStream_t st) {
-  if (P.dtype == ATTN_FP16) return tc::launch_dims<__half>(P, st);
-  return tc::launch_dims<__nv_bfloat16>(P, st);
+  if (P.dtype == ATTN_FP16) return tc::launch_mode<__half>(P, st);
+  return tc::launch_mode<__nv_bfloat16>(P, st);
 }
 
 }  // namespace attn

@@ -95,8 +95,8 @@ typedef struct {
   int32_t window_left;    /* ATTN_MASK_WINDOW only; -1 = unbounded                 */
   int32_t window_right;   /* ATTN_MASK_WINDOW only; -1 = unbounded                 */
   float softmax_scale;    /* s in S = s * Q K^T                                    */
-  int32_t deterministic;  /* 1: split dq_acc + fixed-order reduction (bitwise
-                             repeatable); 0: fp32 atomic accumulation           */
+  int32_t deterministic;  /* attn_det_t: 0 fp32 atomics; 1 and 2 bitwise
+                             repeatable fixed-order dQ reduction              */
   const void* q;          /* device inputs, layouts above                          */
   const void* k;
   const void* v;
@@ -135,13 +135,30 @@ typedef struct {
   float* lse;             /* device output, fp32 natural log                       */
 } attn_fwd_params;
 
+/* dQ accumulation modes (attn_bwd_params.deterministic).  The per-KV-tile dQ
+ * partials of one query tile are summed
+ *   ATTN_DET_ATOMIC: with fp32 atomics in arrival order (not repeatable);
+ *   ATTN_DET_ORDERED: in ascending KV-tile order, each partial added into one
+ *     fp32 dq_acc tile in turn (a per-tile turn counter serialises the adds,
+ *     so the sum is bitwise repeatable; partials never leave the L2 cache
+ *     as separate slices).  FP32 inputs use the split slices instead;
+ *   ATTN_DET_SPLIT: each partial stored to its own dq_acc slice, nsplits =
+ *     ceil(seqlen_k / 128), then summed in ascending slice order by a
+ *     reduction kernel -- the split workspace of aiter PR #2216 (Motivation).
+ * ORDERED and SPLIT perform the same fp32 additions in the same order and
+ * give the same bits, except that ORDERED flushes subnormal partial sums to
+ * zero (fp32 global reductions do). */
+typedef enum { ATTN_DET_ATOMIC = 0, ATTN_DET_ORDERED = 1, ATTN_DET_SPLIT = 2 } attn_det_t;
+
 /* Workspace bytes attn_bwd needs for *p.  Pure host arithmetic on the scalar
  * fields (no device access, no GPU probe), using the same layout function as
  * attn_bwd, so the sizing and the launch cannot disagree (the sizing-pass
  * lesson of TransformerEngine PR #671, review reply on is_v3_api_check).
- * In deterministic mode the workspace holds nsplits = ceil(seqlen_k / 128)
- * fp32 dq_acc slices of [B][Hq][Sq][d_qk] (group mode: [Hq][Tq][d_qk], row =
- * packed token, the fp32-packed layout of PR #671, Root cause), otherwise one.
+ * In ATTN_DET_SPLIT mode (and ATTN_DET_ORDERED with FP32 inputs) the
+ * workspace holds nsplits = ceil(seqlen_k / 128) fp32 dq_acc slices of
+ * [B][Hq][Sq][d_qk] (group mode: [Hq][Tq][d_qk], row = packed token, the
+ * fp32-packed layout of PR #671, Root cause), otherwise one slice (plus one
+ * turn counter per query tile and head in ATTN_DET_ORDERED mode).
  * Writes the size to *bytes.  Returns ATTN_OK or an error code. */
 int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes);
 

@@ -85,12 +85,26 @@ def make(**kw):
     return p
 
 
-def test_workspace_size_deterministic_holds_all_splits(lib):
-    st, n = B.attn_bwd_workspace_size(make())
+def test_workspace_size_split_holds_all_splits(lib):
+    st, n = B.attn_bwd_workspace_size(make(deterministic=B.DET_SPLIT))
     assert st == 0
     nsplits = 4096 // 128
     dq_acc = nsplits * 2 * 32 * 4096 * 128 * 4
     assert dq_acc <= n < dq_acc + 16 * 2**20
+
+
+def test_workspace_size_ordered_fold_one_slice_plus_turns(lib):
+    st, n = B.attn_bwd_workspace_size(make(deterministic=B.DET_ORDERED))
+    assert st == 0
+    one = 2 * 32 * 4096 * 128 * 4
+    turns = 32 * 2 * (4096 // 64) * 4
+    assert one + turns <= n < one + 16 * 2**20
+
+
+def test_workspace_size_fp32_ordered_uses_split_slices(lib):
+    st, n = B.attn_bwd_workspace_size(make(dtype=B.ATTN_FP32, d_qk=64, d_v=64, deterministic=B.DET_ORDERED))
+    assert st == 0
+    assert n >= (4096 // 128) * 2 * 32 * 4096 * 64 * 4
 
 
 def test_workspace_size_atomic_one_slice(lib):
@@ -101,7 +115,7 @@ def test_workspace_size_atomic_one_slice(lib):
 
 
 def test_workspace_size_group_mode(lib):
-    p = make(deterministic=1, batch=3, seqlen_q=300, seqlen_k=300, total_q=700, total_k=700)
+    p = make(deterministic=B.DET_SPLIT, batch=3, seqlen_q=300, seqlen_k=300, total_q=700, total_k=700)
     p.cu_seqlens_q = 0x1000
     p.cu_seqlens_k = 0x2000
     st, n = B.attn_bwd_workspace_size(p)
@@ -128,6 +142,8 @@ ERR = dict(inv=-1, hd=-2, ws=-3)
     (dict(batch=0), "inv"),
     (dict(dtype=7), "inv"),
     (dict(mask=9), "inv"),
+    (dict(deterministic=3), "inv"),
+    (dict(deterministic=-1), "inv"),
     (dict(mask=3, window_left=-2), "inv"),
     (dict(softmax_scale=float("nan")), "inv"),
     (dict(seqlen_q=-1), "inv"),

@@ -71,10 +71,11 @@ def test_mha_causal_B4_H16_S2048(B):
         assert_all_ok(_check_batch(wl, x, got, [(0, 0), (3, 15), (1, 7)], [(0, 0), (3, 15)], 1), f"det={det}")
 
 
-def test_gqa_causal_det_B2_Hq32_Hkv8_S4096(B):
+@pytest.mark.parametrize("det", [1, 2], ids=["ordered", "split"])
+def test_gqa_causal_det_B2_Hq32_Hkv8_S4096(B, det):
     wl = W.gqa_causal_det()
-    x, _, got = _run(B, wl, True)
-    assert_all_ok(_check_batch(wl, x, got, [(0, 0), (1, 31), (0, 13)], [(0, 0), (1, 7)], 2), "gqa det")
+    x, _, got = _run(B, wl, det)
+    assert_all_ok(_check_batch(wl, x, got, [(0, 0), (1, 31), (0, 13)], [(0, 0), (1, 7)], 2), f"gqa det={det}")
 
 
 @pytest.mark.parametrize("det", [True, False], ids=["det", "atomic"])

@@ -79,13 +79,16 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("det", [True, False], ids=["det", "atomic"])
+DET_MODES = dict(argvalues=[1, 2, 0], ids=["ordered", "split", "atomic"])
+
+
+@pytest.mark.parametrize("det", **DET_MODES)
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
 def test_small_backward(B, wl, det):
     assert_all_ok(run_backward_vs_oracle(B, wl, det), wl.name)
 
 
-@pytest.mark.parametrize("det", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("det", **DET_MODES)
 @pytest.mark.parametrize("segs", W.PAGE_SPLITS + [[1, 1, 130, 1], [5, 0, 7], [2048]], ids=str)
 def test_thd_splits_per_segment(B, segs, det):
     """Packed THD, padding-causal within segments, llama3-shaped GQA heads
@@ -148,18 +151,39 @@ def test_gpu_forward_then_backward_end_to_end(B):
     assert_all_ok(reps, "e2e")
 
 
-def test_deterministic_bitwise_repeatable(B):
-    wl = _wl("det_rep", torch.bfloat16, 2, 8, 2, 1000, 1000, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=41)
+def _bwd_runs(B, wl, modes, repeats):
     x = {k: v.cuda() for k, v in wl.inputs().items()}
-    o, lse = B.attn_forward(x["q"], x["k"], x["v"], scale=wl.scale, mask=wl.mask)
-    first = B.attn_backward(x["q"], x["k"], x["v"], o, x["do"], lse, scale=wl.scale, mask=wl.mask,
-                            deterministic=True)
-    first = [t.clone() for t in first]
-    for _ in range(9):
-        again = B.attn_backward(x["q"], x["k"], x["v"], o, x["do"], lse, scale=wl.scale, mask=wl.mask,
-                                deterministic=True)
-        for a, b in zip(first, again):
-            assert torch.equal(a, b)
+    cu = wl.cu_seqlens()
+    cu_d = None if cu is None else cu.cuda()
+    kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
+              cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+    o, lse = B.attn_forward(x["q"], x["k"], x["v"], **kw)
+    out = {}
+    for m in modes:
+        out[m] = [[t.clone() for t in B.attn_backward(x["q"], x["k"], x["v"], o, x["do"], lse,
+                                                       deterministic=m, **kw)] for _ in range(repeats)]
+    return out
+
+
+DET_CASES = [
+    _wl("det_rep", torch.bfloat16, 2, 8, 2, 1000, 1000, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=41),
+    _wl("det_win192", torch.bfloat16, 1, 4, 2, 700, 700, 192, 128, W.MASK_WINDOW, 200, 0, seed=42),
+    _wl("det_br_short_k", torch.bfloat16, 1, 4, 4, 500, 300, 128, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, seed=43),
+    W.thd("det_thd", [700, 1, 129, 300, 64], hq=8, hkv=2, seed=44),
+]
+
+
+@pytest.mark.parametrize("wl", DET_CASES, ids=lambda w: w.name)
+def test_deterministic_bitwise_repeatable(B, wl):
+    """Both deterministic modes give the same bits on 10 runs, and the ordered
+    fold gives the same bits as the split slices (same additions, same order)."""
+    runs = _bwd_runs(B, wl, (B.DET_ORDERED, B.DET_SPLIT), 10)
+    for m, rs in runs.items():
+        for again in rs[1:]:
+            for a, b in zip(rs[0], again):
+                assert torch.equal(a, b), f"mode {m} not repeatable"
+    for a, b in zip(runs[B.DET_ORDERED][0], runs[B.DET_SPLIT][0]):
+        assert torch.equal(a, b), "ordered fold differs from split slices"
 
 
 def test_bad_cu_seqlens_reported_by_device(B):
@@ -189,7 +213,7 @@ def test_outputs_and_workspace_guard_bands(B):
         big = torch.full((t.numel() + 2 * g,), float("nan"), dtype=t.dtype, device="cuda")
         bufs.append(big)
     outs = tuple(b[g:g + t.numel()].view(t.shape) for b, t in zip(bufs, (x["q"], x["k"], x["v"])))
-    for det in (True, False):
+    for det in (0, 1, 2):
         p = B.bwd_params(x["q"], x["k"], x["v"], o, x["do"], lse, *outs, scale=wl.scale, mask=wl.mask,
                          deterministic=det)
         need = B.workspace_bytes(p)
