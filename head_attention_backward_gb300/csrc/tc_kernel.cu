@@ -51,17 +51,15 @@ constexpr int FIRST_SOFTMAX_WARP = 2;
 constexpr int FIRST_EPI_WARP = FIRST_SOFTMAX_WARP + NUM_SOFTMAX_WARPS;
 constexpr int SDP_ISSUER_WARP = FIRST_EPI_WARP + NUM_EPI_WARPS;   // issues the S / dP MMAs
 constexpr int NUM_THREADS = 32 * (SDP_ISSUER_WARP + 1);
-// ordered fold only: one more warp, whose lane 0 acquires the turns of
-// upcoming dQ partials and passes them on once the drain warps' adds are
-// issued (a 25th warp would cut the per-thread register budget from 80 to 72)
+// ordered fold only: one more warp, whose lane 0 passes a tile's turn on once
+// the drain warps' adds are issued (a 25th warp would cut the per-thread
+// register budget from 80 to 72)
 constexpr int TURN_WARP = SDP_ISSUER_WARP + 1;
 constexpr int NUM_THREADS_FOLD = 32 * (TURN_WARP + 1);
 // dQ accumulation of a kernel instantiation (each carries only its own path)
 enum : int { DQ_ATOMIC = 0, DQ_FOLD = 1, DQ_SPLIT = 2 };
 template <int DQM> constexpr int kernel_threads() { return DQM == DQ_FOLD ? NUM_THREADS_FOLD : NUM_THREADS; }
-constexpr int NT = 2;                       // turn slots between the acquirer and the drain
 constexpr int NR = 4;                       // release slots between the drain and the turn thread
-constexpr int ND = 8;                       // turn-thread records of acquired, unreleased steps
 constexpr int NI = 2;                       // work-item ring slots
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t SLEEP_HINT_NS = 20000;   // longest single sleep inside a wait
@@ -91,10 +89,19 @@ struct Cfg {
   static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;      // [ST][BM] -LSE*log2(e)
   static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
   static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
-  static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NT + 2 * NR;
+  static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NR;
   static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MISC = OFF_RING + NI * 16;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + ND * 8 + 1024;  // + alignment slack
+  // ordered fold: a dQ partial waiting for its turn can be parked here (the
+  // whole 64 x d_qk block), freeing its TMEM for the next step
+  static constexpr int OFF_STASH = OFF_MISC + 64 + NR * 8;
+  static constexpr int STASH_BYTES = BM * DQK * 4;
+  static constexpr bool STASH_FITS = OFF_STASH + STASH_BYTES + 1024 <= 232448;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + NR * 8 + 1024;  // + alignment slack
+  template <bool FOLD> static constexpr bool stash() { return FOLD && NMB == 1 && STASH_FITS; }
+  template <bool FOLD> static constexpr int smem_bytes() {
+    return stash<FOLD>() ? OFF_STASH + STASH_BYTES + 1024 : SMEM_BYTES;
+  }
   // TMEM column map; the two P^T buffers (bf16, two per column) are MMA A operands
   static constexpr int T_DK = 0;
   static constexpr int T_DV = DQK;
@@ -192,6 +199,31 @@ __device__ __forceinline__ void step_coords(const Problem& P, const ItemInfo& I,
   qt = I.qlo + I.nq - 1 - j;
 }
 
+// Ordered fold: poll until `rank` partials of the tile have been folded
+// (bounded by %globaltimer, and given up as soon as another CTA has failed).
+// The acquire load orders this warp's adds after those partials'.
+__device__ __forceinline__ bool acquire_turn(const Ctx& c, const uint32_t* turn, uint32_t rank) {
+  if (ld_acquire_gpu(turn) == rank) return true;
+#ifdef ATTN_WAIT_STATS
+  stat_add(g_wait_stats, 35, 1ull);   // turn not yet there at the second look
+#endif
+  const uint64_t t0 = globaltimer();
+  while (ld_acquire_gpu(turn) != rank) {
+    if (*(volatile int*)c.abort_flag || *(volatile int*)(c.hdr + HDR_STATUS) != 0) {
+      *(volatile int*)c.abort_flag = 1;
+      return false;
+    }
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      *(volatile int*)c.abort_flag = 1;
+      atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
+      atomicExch(c.hdr + HDR_DIAG, 33);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
 template <typename T> struct IsHalf { static constexpr bool value = false; };
 template <> struct IsHalf<__half> { static constexpr bool value = true; };
 
@@ -208,6 +240,7 @@ template <int DQK, int DV, typename T, int DQM>
 __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const __grid_constant__ TmaMaps maps, const Problem P) {
   using C = Cfg<DQK, DV>;
   constexpr bool FOLD = DQM == DQ_FOLD;
+  constexpr bool STASH = C::template stash<FOLD>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -221,10 +254,9 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
   const Ctx ctx{bar, abort_flag, P.hdr};
   const int B_Q_FULL = B_FIXED_END, B_Q_EMPTY = B_FIXED_END + C::ST;
   const int B_IT_FULL = B_FIXED_END + 2 * C::ST, B_IT_EMPTY = B_IT_FULL + NI;
-  // ordered fold: turn acquired (acquirer -> drain) / slot free (drain ->
-  // acquirer); adds issued (drain -> releaser) / slot free (releaser -> drain)
-  const int B_TURN_OK = B_IT_EMPTY + NI, B_TURN_FREE = B_TURN_OK + NT;
-  const int B_REDS_DONE = B_TURN_FREE + NT, B_REDS_FREE = B_REDS_DONE + NR;
+  // ordered fold: a partial's adds issued (drain -> turn thread) / release
+  // slot free again (turn thread -> drain)
+  const int B_REDS_DONE = B_IT_EMPTY + NI, B_REDS_FREE = B_REDS_DONE + NR;
   constexpr int NTHREADS = kernel_threads<DQM>();
 
   // zero the k padding chunks read by the dQ^T MMA of padded head dims
@@ -263,10 +295,6 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       mbar_init(bar + B_IT_EMPTY + s, 2 + NUM_SOFTMAX_WARPS + NUM_EPI_WARPS + (FOLD ? 1 : 0));
     }
     if (FOLD) {
-      for (int s = 0; s < NT; ++s) {
-        mbar_init(bar + B_TURN_OK + s, 1);
-        mbar_init(bar + B_TURN_FREE + s, NUM_EPI_WARPS);
-      }
       for (int s = 0; s < NR; ++s) {
         mbar_init(bar + B_REDS_DONE + s, NUM_EPI_WARPS);
         mbar_init(bar + B_REDS_FREE + s, 1);
@@ -585,24 +613,27 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
     }
   } else if (FOLD && warp == TURN_WARP) {
     // ------------------------------------------- ordered fold: turn thread
-    // Two frontiers, serviced without blocking each other: `rel` passes on the
-    // turn of every step whose adds the drain warps reported (gpu-scope fence,
-    // then the tile's counter), `acq` walks the work items ahead of the drain
-    // warps (at most NT steps) and signals each step once the tile's counter
-    // shows that the partials of all lower KV tiles are folded.  A release
-    // never waits for an acquisition, and every acquisition waits for a lower
-    // KV tile, which an earlier work item holds: the waits cannot form a cycle.
+    // Passes on the turn of every partial whose adds all four drain warps
+    // have issued: a gpu-scope fence (which waits for those adds), then the
+    // tile's counter.  The drain warps acquire turns themselves; this thread
+    // never waits for another CTA, so a CTA never holds back a release while
+    // it waits, and every wait is for a lower KV tile, which an earlier work
+    // item holds: the waits cannot form a cycle.
     if (lane == 0) {
-      uint2* rec = reinterpret_cast<uint2*>(smem + C::OFF_MISC + 64);   // [ND] (counter index, value)
-      uint32_t acq = 0, rel = 0, n_item = 0;
-      ItemInfo I{};
-      int s = 0;
-      bool have_item = false, items_done = false;
-      uint64_t last = globaltimer();
-      while (true) {
-        bool progress = false;
-        if (rel < acq && mbar_test_wait(smem_u32(bar + B_REDS_DONE + rel % NR), (rel / NR) & 1)) {
-          const uint2 r = rec[rel % ND];
+      const uint2* rec = reinterpret_cast<const uint2*>(smem + C::OFF_MISC + 64);   // [NR] (counter, value)
+      uint32_t gs = 0, n_item = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = n_item % NI;
+        if (!wait_bar(ctx, B_IT_FULL + slot, (n_item / NI) & 1, 38)) break;
+        const int4 item = ring[slot];
+        mbar_arrive(bar + B_IT_EMPTY + slot);
+        ++n_item;
+        if (item.x < 0) break;
+        const ItemInfo I = item_info(P, item);
+        for (int s = 0; s < I.nsteps; ++s, ++gs) {
+          if (!(ok = wait_bar(ctx, B_REDS_DONE + gs % NR, (gs / NR) & 1, 40))) break;
+          const uint2 r = rec[gs % NR];
 #ifdef ATTN_WAIT_STATS
           const long long c0 = clock64();
 #endif
@@ -611,59 +642,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
 #ifdef ATTN_WAIT_STATS
           stat_add(g_wait_stats, 34, (unsigned long long)(clock64() - c0));   // release fence
 #endif
-          mbar_arrive(bar + B_REDS_FREE + rel % NR);
-          ++rel;
-          progress = true;
-        }
-        if (!have_item && !items_done) {
-          const int slot = n_item % NI;
-          if (mbar_test_wait(smem_u32(bar + B_IT_FULL + slot), (n_item / NI) & 1)) {
-            const int4 item = ring[slot];
-            mbar_arrive(bar + B_IT_EMPTY + slot);
-            ++n_item;
-            if (item.x < 0) {
-              items_done = true;
-            } else {
-              I = item_info(P, item);
-              s = 0;
-              have_item = I.nsteps > 0;
-            }
-            progress = true;
-          }
-        }
-        if (have_item && acq - rel < ND &&
-            mbar_test_wait(smem_u32(bar + B_TURN_FREE + acq % NT), ((acq / NT) & 1) ^ 1)) {
-          int h, qt;
-          step_coords(P, I, s, h, qt);
-          const int tile = qtile_index(P, I.b, qt);
-          const uint32_t idx = (uint32_t)(h * P.ntiles + tile);
-          const uint32_t rank = (uint32_t)(I.kt - __ldg(P.klo + tile));   // KV tiles before this one
-          if (ld_acquire_gpu(P.turn + idx) == rank) {
-            rec[acq % ND] = make_uint2(idx, rank + 1);
-            mbar_arrive(bar + B_TURN_OK + acq % NT);
-            ++acq;
-            have_item = ++s < I.nsteps;
-            progress = true;
-          }
-#ifdef ATTN_WAIT_STATS
-          else stat_add(g_wait_stats, 35, 1ull);   // turn not there yet at this look
-#endif
-        }
-        if (items_done && !have_item && rel == acq) break;
-        if (progress) {
-          last = globaltimer();
-        } else {
-          if (*(volatile int*)abort_flag || *(volatile int*)(P.hdr + HDR_STATUS) != 0) {
-            *(volatile int*)abort_flag = 1;
-            break;
-          }
-          if (globaltimer() - last > WAIT_LIMIT_NS) {
-            *(volatile int*)abort_flag = 1;
-            atomicCAS(P.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
-            atomicExch(P.hdr + HDR_DIAG, 33);
-            break;
-          }
-          __nanosleep(20);
+          mbar_arrive(bar + B_REDS_FREE + gs % NR);
         }
       }
     }
@@ -698,9 +677,67 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         int h, qt;
         step_coords(P, I, s, h, qt);
         const int tile = qtile_index(P, I.b, qt);
+        // ordered fold: this partial is number `rank` of the tile's sum; lane 0
+        // of each warp reads the tile's counter before the dQ tile is ready
+        uint32_t idx = 0, rank = 0, seen = ~0u;
+        if (FOLD && lane == 0) {
+          idx = (uint32_t)(h * P.ntiles + tile);
+          rank = (uint32_t)(I.kt - __ldg(P.klo + tile));
+          seen = ld_acquire_gpu(P.turn + idx);
+        }
         if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
         tc_fence_after();
         float* dst_tile = dq_tile(P, DQM == DQ_SPLIT ? I.kt : 0, h, tile);
+        if constexpr (STASH) {
+          // One 128-row dQ^T block.  If the tile's turn has come, add the
+          // partial straight from TMEM; if not, park it in shared memory (each
+          // thread its own column of the block), free the TMEM for the next
+          // step, and add it once lane 0 has seen the turn arrive.
+          float* dst = dst_tile + L;
+          float* stash = reinterpret_cast<float*>(smem + C::OFF_STASH) + L;
+          uint32_t v[32];
+          tmem_ld32(lane_addr + C::T_DQ, v);
+          tmem_wait_ld();
+          const bool ready = __shfl_sync(0xffffffffu, seen == rank, 0);
+          if (ready) {
+            __syncwarp();   // the other lanes' adds come after lane 0's acquire
+            if (L < DQK) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) red_add_f32(dst + c * DQK, __uint_as_float(v[c]));
+            }
+            tmem_ld32(lane_addr + C::T_DQ + 32, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
+            if (L < DQK) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) red_add_f32(dst + (32 + c) * DQK, __uint_as_float(v[c]));
+            }
+          } else {
+            if (L < DQK) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) stash[c * DQK] = __uint_as_float(v[c]);
+            }
+            tmem_ld32(lane_addr + C::T_DQ + 32, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
+            if (L < DQK) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) stash[(32 + c) * DQK] = __uint_as_float(v[c]);
+            }
+            if (lane == 0) ok = acquire_turn(ctx, P.turn + idx, rank);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();   // the other lanes' adds come after lane 0's acquire
+            if (L < DQK) {
+#pragma unroll 8
+              for (int c = 0; c < BM; ++c) red_add_f32(dst + c * DQK, stash[c * DQK]);
+            }
+          }
+        } else {
 #pragma unroll 1
         for (int mb = 0; mb < C::NMB && ok; ++mb) {
           const int rows = min(128, DQK - mb * 128);
@@ -715,11 +752,12 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
               if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
             }
             if (FOLD && mb == 0 && hx == 0) {
-              // ordered fold: the partials before this one are in the sum (the
-              // acquirer saw the tile's turn counter reach `rank`)
-              if (!(ok = wait_bar(ctx, B_TURN_OK + gs % NT, (gs / NT) & 1, 36))) break;
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar + B_TURN_FREE + gs % NT);
+              // ordered fold: wait (holding the TMEM) until the partials of the
+              // lower KV tiles are in the sum
+              if (lane == 0 && seen != rank) ok = acquire_turn(ctx, P.turn + idx, rank);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              if (!ok) break;
+              __syncwarp();   // the other lanes' adds come after lane 0's acquire
             }
             if (L < rows) {
               // tile stored query-major ([BM][d_qk]): for each query the warp's
@@ -740,13 +778,16 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
             }
           }
         }
+        }
         if (!ok) break;
         if (FOLD) {
-          // this warp's adds of the partial are issued: the releaser passes the
-          // turn on (after a gpu-scope fence) once all four warps report
+          // this warp's adds of the partial are issued: the turn thread passes
+          // the turn on (after a gpu-scope fence) once all four warps report
           __syncwarp();
           if (lane == 0) {
             ok = wait_bar(ctx, B_REDS_FREE + gs % NR, ((gs / NR) & 1) ^ 1, 37);
+            if (ok && warp == FIRST_EPI_WARP)
+              reinterpret_cast<uint2*>(smem + C::OFF_MISC + 64)[gs % NR] = make_uint2(idx, rank + 1);
             if (ok) mbar_arrive(bar + B_REDS_DONE + gs % NR);
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -864,7 +905,9 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
     return ATTN_ERR_CUDA;
   auto kern = bwd_tc_kernel<DQK, DV, T, DQM>;
   // at least 120 KB so that two CTAs never share an SM (each holds all 512 TMEM columns)
-  const int smem = C::SMEM_BYTES > 120 * 1024 ? C::SMEM_BYTES : 120 * 1024;
+  constexpr int need = C::template smem_bytes<DQM == DQ_FOLD>();
+  static_assert(need <= 232448, "shared memory overflow");
+  const int smem = need > 120 * 1024 ? need : 120 * 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
   int dev = 0, sms = 0;
