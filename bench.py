@@ -1,8 +1,10 @@
 """Benchmark of the FMHA backward on the Llama-3-8B-shaped GQA workload.
 
 Default workload: B=2, Hq=32, Hkv=8, S=4096, d=128, causal, deterministic
-(nsplits = 32 dq_acc slices), bf16 inputs ~ N(0, 1), O/LSE from the forward
-helper.  One step = one whole attn_bwd call (schedule, preprocess, main
+dQ (the per-KV-tile partials summed in ascending KV-tile order: the ordered
+fold by default; the split workspace of nsplits = 32 dq_acc slices plus a
+reduction kernel is timed beside it and gives the same bits), bf16 inputs
+~ N(0, 1), O/LSE from the forward helper.  One step = one whole attn_bwd call (schedule, preprocess, main
 kernel, dQ reduce/convert) on inputs resident in HBM; L2 is flushed (256 MB
 write) before every timed step.  Metric: mask-adjusted TFLOP/s.
 
@@ -72,7 +74,11 @@ def peaks():
 # change to the kernel makes the figure stale, and then ``traffic`` is null.
 KERNEL_SOURCES = ("tc_kernel.cu", "common.cuh", "sm100_ptx.cuh")
 KERNEL_TRAFFIC = {
-    "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det": {
+    "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:ordered": {
+        "bytes": 621.25e6 + 279.25e6,
+        "src": "af006fa446a5c341",
+        "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
+    "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:split": {
         "bytes": 551.55e6 + 2.19e9,
         "src": "523903848972bbd9",
         "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
@@ -88,17 +94,28 @@ def kernel_src_hash():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload_name):
-    t = KERNEL_TRAFFIC.get(workload_name)
+def measured_traffic(key):
+    t = KERNEL_TRAFFIC.get(key)
     if t is None or t["src"] != kernel_src_hash():
         return None, None
     return t["bytes"], t["profile"]
 
 
+DQ_MODES = {"atomic": 0, "ordered": 1, "split": 2}
+DQ_MODE_NAMES = {0: "atomic fp32 reductions", 1: "ordered fold (ascending KV tile)",
+                 2: "split slices + fixed-order reduction"}
+
+
+def dq_mode(wl):
+    """attn_det_t value of a workload: False/True or an explicit mode."""
+    return int(wl.deterministic)
+
+
 def config_of(wl):
     c = {"workload": wl.name, "batch": wl.batch, "nhead_q": wl.hq, "nhead_kv": wl.hkv,
          "seqlen": wl.sq, "d_qk": wl.d_qk, "d_v": wl.d_v, "mask": wl.mask,
-         "window": [wl.left, wl.right], "deterministic": wl.deterministic,
+         "window": [wl.left, wl.right], "deterministic": bool(wl.deterministic),
+         "dq_mode": DQ_MODE_NAMES[dq_mode(wl)],
          "l2": "flushed (256 MB write) before every timed step"}
     if wl.group_mode:
         c["segments"] = len(wl.seqlens)
@@ -245,7 +262,7 @@ def run_ours(args, wl):
               cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
     o, lse = B.attn_forward(d["q"], d["k"], d["v"], **kw)
     outs = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]))
-    p = B.bwd_params(d["q"], d["k"], d["v"], o, d["do"], lse, *outs, deterministic=wl.deterministic, **kw)
+    p = B.bwd_params(d["q"], d["k"], d["v"], o, d["do"], lse, *outs, deterministic=dq_mode(wl), **kw)
     nbytes = B.workspace_bytes(p)
     ws = B.alloc_workspace(nbytes, dev)
     flush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device=dev)
@@ -281,6 +298,28 @@ def run_ours(args, wl):
     main_avg = sum(main_ms) / len(main_ms)
     ms_per_step, main_avg = max_over_ranks([ms_per_step, main_avg], pg, dev)
 
+    # the pages' split-slice workspace on the same workload (same bits as the
+    # ordered fold), timed beside it for reference
+    split_leg = None
+    if dq_mode(wl) == DQ_MODES["ordered"] and not args.no_split_leg:
+        ps = B.bwd_params(d["q"], d["k"], d["v"], o, d["do"], lse, *outs, deterministic=DQ_MODES["split"], **kw)
+        nb = B.workspace_bytes(ps)
+        wss = B.alloc_workspace(nb, dev)
+        sms = []
+        for i in range(3 + min(args.steps, 20)):
+            flush.fill_(1.0)
+            st, ms = B.attn_bwd_timed(ps, wss.data_ptr(), nb, stream)
+            if st != 0:
+                raise B.AttnError(st, "attn_bwd_timed (split)")
+            if i >= 3:
+                sms.append(ms)
+        del wss
+        sp_ms = max_over_ranks([sum(m[3] for m in sms) / len(sms)], pg, dev)[0]
+        split_leg = {"dq_mode": DQ_MODE_NAMES[DQ_MODES["split"]], "ms_per_step": sp_ms,
+                     "value": job_throughput(world, fl, sp_ms), "steps": len(sms),
+                     "step_stage_ms": [sum(m[k] for m in sms) / len(sms) for k in range(4)],
+                     "workspace_bytes": nb}
+
     # end to end through the C ABI: pinned host inputs in, results back out
     e2e_avg, h2d, d2h = float("nan"), 0, 0
     if not args.no_e2e:
@@ -309,7 +348,7 @@ def run_ours(args, wl):
         e2e_avg = max_over_ranks([sum(e2e_ms) / len(e2e_ms)], pg, dev)[0]
 
     peak_tf, peak_hbm, peak_src = peaks()
-    traffic, traffic_src = measured_traffic(wl.name)
+    traffic, traffic_src = measured_traffic(f"{wl.name}:{[k for k, v in DQ_MODES.items() if v == dq_mode(wl)][0]}")
     value = job_throughput(world, fl, ms_per_step)
     achieved = fl / (main_avg * 1e-3) / 1e12
     out = {
@@ -327,6 +366,7 @@ def run_ours(args, wl):
                                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                          "ms_per_step": e2e_avg},
         "gpu_launches": 4 * args.steps,
+        "split_slices": split_leg,
         "clocks": clk,
         "workspace_bytes": nbytes,
         "wall_s_timed_region": wall,
@@ -353,15 +393,22 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch of a batch-mode workload")
-    ap.add_argument("--atomic", action="store_true", help="fp32 atomic dQ accumulation instead of split slices")
+    ap.add_argument("--atomic", action="store_true", help="same as --dq-mode atomic")
+    ap.add_argument("--dq-mode", choices=sorted(DQ_MODES), default=None,
+                    help="dQ accumulation: ordered fold, split slices or fp32 atomics (default: the workload's)")
+    ap.add_argument("--no-split-leg", action="store_true",
+                    help="skip timing the split-slice path beside the ordered fold")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]()
     if args.batch and not wl.group_mode:
         wl.batch = args.batch
         wl.name += f"_batch{args.batch}"
     if args.atomic:
-        wl.deterministic = False
-        wl.name += "_atomic"
+        args.dq_mode = "atomic"
+    if args.dq_mode is not None:
+        wl.deterministic = DQ_MODES[args.dq_mode]
+        if args.dq_mode == "atomic":
+            wl.name += "_atomic"
     if args.impl == "reference":
         run_reference(args, wl)
     else:
