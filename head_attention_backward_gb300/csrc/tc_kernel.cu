@@ -92,16 +92,7 @@ struct Cfg {
   static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NR;
   static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MISC = OFF_RING + NI * 16;
-  // ordered fold: a dQ partial waiting for its turn can be parked here (the
-  // whole 64 x d_qk block), freeing its TMEM for the next step
-  static constexpr int OFF_STASH = OFF_MISC + 64 + NR * 8;
-  static constexpr int STASH_BYTES = BM * DQK * 4;
-  static constexpr bool STASH_FITS = OFF_STASH + STASH_BYTES + 1024 <= 232448;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + NR * 8 + 1024;  // + alignment slack
-  template <bool FOLD> static constexpr bool stash() { return FOLD && NMB == 1 && STASH_FITS; }
-  template <bool FOLD> static constexpr int smem_bytes() {
-    return stash<FOLD>() ? OFF_STASH + STASH_BYTES + 1024 : SMEM_BYTES;
-  }
   // TMEM column map; the two P^T buffers (bf16, two per column) are MMA A operands
   static constexpr int T_DK = 0;
   static constexpr int T_DV = DQK;
@@ -240,7 +231,6 @@ template <int DQK, int DV, typename T, int DQM>
 __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const __grid_constant__ TmaMaps maps, const Problem P) {
   using C = Cfg<DQK, DV>;
   constexpr bool FOLD = DQM == DQ_FOLD;
-  constexpr bool STASH = C::template stash<FOLD>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -688,56 +678,6 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
         tc_fence_after();
         float* dst_tile = dq_tile(P, DQM == DQ_SPLIT ? I.kt : 0, h, tile);
-        if constexpr (STASH) {
-          // One 128-row dQ^T block.  If the tile's turn has come, add the
-          // partial straight from TMEM; if not, park it in shared memory (each
-          // thread its own column of the block), free the TMEM for the next
-          // step, and add it once lane 0 has seen the turn arrive.
-          float* dst = dst_tile + L;
-          float* stash = reinterpret_cast<float*>(smem + C::OFF_STASH) + L;
-          uint32_t v[32];
-          tmem_ld32(lane_addr + C::T_DQ, v);
-          tmem_wait_ld();
-          const bool ready = __shfl_sync(0xffffffffu, seen == rank, 0);
-          if (ready) {
-            __syncwarp();   // the other lanes' adds come after lane 0's acquire
-            if (L < DQK) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) red_add_f32(dst + c * DQK, __uint_as_float(v[c]));
-            }
-            tmem_ld32(lane_addr + C::T_DQ + 32, v);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
-            if (L < DQK) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) red_add_f32(dst + (32 + c) * DQK, __uint_as_float(v[c]));
-            }
-          } else {
-            if (L < DQK) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) stash[c * DQK] = __uint_as_float(v[c]);
-            }
-            tmem_ld32(lane_addr + C::T_DQ + 32, v);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
-            if (L < DQK) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) stash[(32 + c) * DQK] = __uint_as_float(v[c]);
-            }
-            if (lane == 0) ok = acquire_turn(ctx, P.turn + idx, rank);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            __syncwarp();   // the other lanes' adds come after lane 0's acquire
-            if (L < DQK) {
-#pragma unroll 8
-              for (int c = 0; c < BM; ++c) red_add_f32(dst + c * DQK, stash[c * DQK]);
-            }
-          }
-        } else {
 #pragma unroll 1
         for (int mb = 0; mb < C::NMB && ok; ++mb) {
           const int rows = min(128, DQK - mb * 128);
@@ -752,8 +692,9 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
               if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
             }
             if (FOLD && mb == 0 && hx == 0) {
-              // ordered fold: wait (holding the TMEM) until the partials of the
-              // lower KV tiles are in the sum
+              // ordered fold: wait until the partials of the lower KV tiles are
+              // in the sum (the counter read before the dQ tile was ready
+              // usually shows it already)
               if (lane == 0 && seen != rank) ok = acquire_turn(ctx, P.turn + idx, rank);
               ok = __shfl_sync(0xffffffffu, ok, 0);
               if (!ok) break;
@@ -777,7 +718,6 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
               }
             }
           }
-        }
         }
         if (!ok) break;
         if (FOLD) {
@@ -905,9 +845,7 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
     return ATTN_ERR_CUDA;
   auto kern = bwd_tc_kernel<DQK, DV, T, DQM>;
   // at least 120 KB so that two CTAs never share an SM (each holds all 512 TMEM columns)
-  constexpr int need = C::template smem_bytes<DQM == DQ_FOLD>();
-  static_assert(need <= 232448, "shared memory overflow");
-  const int smem = need > 120 * 1024 ? need : 120 * 1024;
+  const int smem = C::SMEM_BYTES > 120 * 1024 ? C::SMEM_BYTES : 120 * 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
   int dev = 0, sms = 0;
