@@ -135,6 +135,23 @@ __device__ __forceinline__ void stat_add(unsigned long long* s, int where, unsig
 }
 #endif
 
+// Whether a bounded wait must give up: this CTA aborted, or the wait began
+// more than WAIT_LIMIT_NS ago (then the timeout is recorded).  Out of line:
+// it only runs when a suspended try_wait returns without the phase.
+__device__ __noinline__ bool wait_expired(const Ctx& c, uint64_t t0, int where) {
+  if (*(volatile int*)c.abort_flag) return true;
+  if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+    *(volatile int*)c.abort_flag = 1;
+    atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
+    atomicExch(c.hdr + HDR_DIAG, where);
+    return true;
+  }
+  return false;
+}
+
+// Bounded mbarrier wait: one test, then suspending try_waits (the common path
+// stays small at each of the many call sites: instruction-fetch stalls were
+// measured to grow with the kernel's code).
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity, int where) {
   const uint32_t a = smem_u32(c.bar + idx);
   if (mbar_test_wait(a, parity)) return true;
@@ -146,16 +163,9 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity,
     __device__ ~Guard() { stat_add(g_wait_stats, where, (unsigned long long)(clock64() - c0)); }
   } guard{c0, where};
 #endif
-  while (true) {
-    if (mbar_try_wait_sleep(a, parity, SLEEP_HINT_NS)) return true;
-    if (*(volatile int*)c.abort_flag) return false;
-    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-      *(volatile int*)c.abort_flag = 1;
-      atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
-      atomicExch(c.hdr + HDR_DIAG, where);
-      return false;
-    }
-  }
+  while (!mbar_try_wait_sleep(a, parity, SLEEP_HINT_NS))
+    if (wait_expired(c, t0, where)) return false;
+  return true;
 }
 
 // Work item and the per-item quantities every role derives identically.
