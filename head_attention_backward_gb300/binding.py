@@ -48,7 +48,7 @@ class AttnFwdParams(ctypes.Structure):
 
 
 EXPORTS = ["attn_bwd_workspace_size", "attn_bwd", "attn_bwd_timed", "attn_bwd_read_status",
-           "attn_fwd", "attn_status_string", "attn_bwd_static_ws"]
+           "attn_fwd", "attn_status_string", "attn_bwd_static_ws", "attn_selftest_waits"]
 
 _lib = None
 
@@ -117,6 +117,20 @@ def attn_status_string(st: int) -> str:
 
 
 STATIC_WS_BYTES = 64 << 20
+
+
+SELFTEST_SCRATCH_BYTES = 3 * 128 * 4 + 16
+
+
+def attn_selftest_waits(scratch_ptr: int, scratch_bytes: int, stream: int = 0):
+    """Runs the bounded-wait self-test; returns (rc, [status0, status1, status2])."""
+    lib = load()
+    fn = lib.attn_selftest_waits
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+    fn.restype = ctypes.c_int
+    out = (ctypes.c_int * 3)()
+    rc = fn(ctypes.c_void_p(scratch_ptr), ctypes.c_size_t(scratch_bytes), ctypes.c_void_p(stream), out)
+    return rc, list(out)
 
 
 def attn_bwd_static_ws(p: AttnBwdParams, stream: int = 0) -> int:

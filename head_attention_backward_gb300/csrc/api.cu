@@ -219,3 +219,8 @@ extern "C" const char* attn_status_string(int status) {
     default: return "unknown status";
   }
 }
+
+extern "C" int attn_selftest_waits(void* scratch, size_t scratch_bytes, cudaStream_t stream, int status[3]) {
+  if (!status) return ATTN_ERR_INVALID_ARG;
+  return selftest_waits(scratch, scratch_bytes, stream, status);
+}

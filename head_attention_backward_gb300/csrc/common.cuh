@@ -298,6 +298,7 @@ void launch_preprocess(const Problem& P, cudaStream_t st);
 void launch_reduce_convert(const Problem& P, cudaStream_t st);
 void launch_bwd_simt(const Problem& P, cudaStream_t st);
 int launch_bwd_tc(const Problem& P, cudaStream_t st);   // returns ATTN_* status
+int selftest_waits(void* scratch, size_t bytes, cudaStream_t st, int status[3]);
 void launch_fwd(const attn_fwd_params& p, cudaStream_t st);
 
 }  // namespace attn

@@ -136,11 +136,12 @@ __device__ __forceinline__ void stat_add(unsigned long long* s, int where, unsig
 #endif
 
 // Whether a bounded wait must give up: this CTA aborted, or the wait began
-// more than WAIT_LIMIT_NS ago (then the timeout is recorded).  Out of line:
-// it only runs when a suspended try_wait returns without the phase.
+// more than LIMIT ns ago (then the timeout is recorded).  Out of line: it only
+// runs when a suspended try_wait returns without the phase.
+template <uint64_t LIMIT>
 __device__ __noinline__ bool wait_expired(const Ctx& c, uint64_t t0, int where) {
   if (*(volatile int*)c.abort_flag) return true;
-  if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+  if (globaltimer() - t0 > LIMIT) {
     *(volatile int*)c.abort_flag = 1;
     atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
     atomicExch(c.hdr + HDR_DIAG, where);
@@ -152,6 +153,7 @@ __device__ __noinline__ bool wait_expired(const Ctx& c, uint64_t t0, int where) 
 // Bounded mbarrier wait: one test, then suspending try_waits (the common path
 // stays small at each of the many call sites: instruction-fetch stalls were
 // measured to grow with the kernel's code).
+template <uint64_t LIMIT = WAIT_LIMIT_NS>
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity, int where) {
   const uint32_t a = smem_u32(c.bar + idx);
   if (mbar_test_wait(a, parity)) return true;
@@ -164,7 +166,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity,
   } guard{c0, where};
 #endif
   while (!mbar_try_wait_sleep(a, parity, SLEEP_HINT_NS))
-    if (wait_expired(c, t0, where)) return false;
+    if (wait_expired<LIMIT>(c, t0, where)) return false;
   return true;
 }
 
@@ -203,6 +205,7 @@ __device__ __forceinline__ void step_coords(const Problem& P, const ItemInfo& I,
 // Ordered fold: poll until `rank` partials of the tile have been folded
 // (bounded by %globaltimer, and given up as soon as another CTA has failed).
 // The acquire load orders this warp's adds after those partials'.
+template <uint64_t LIMIT = WAIT_LIMIT_NS>
 __device__ __forceinline__ bool acquire_turn(const Ctx& c, const uint32_t* turn, uint32_t rank) {
   if (ld_acquire_gpu(turn) == rank) return true;
 #ifdef ATTN_WAIT_STATS
@@ -214,7 +217,7 @@ __device__ __forceinline__ bool acquire_turn(const Ctx& c, const uint32_t* turn,
       *(volatile int*)c.abort_flag = 1;
       return false;
     }
-    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > LIMIT) {
       *(volatile int*)c.abort_flag = 1;
       atomicCAS(c.hdr + HDR_STATUS, 0, ATTN_ERR_TIMEOUT);
       atomicExch(c.hdr + HDR_DIAG, 33);
@@ -812,6 +815,49 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
   }
 }
 
+// ---------------------------------------------------------- wait self-test
+// The bounded waits of the backward kernel, run on waits that can never end:
+// an mbarrier whose phase nobody completes, a turn counter nobody advances,
+// and a turn wait entered after another CTA has already failed.  Each gives up
+// (within `limit_ns`, or at once in the last case) and records its status in
+// its own header, as the backward kernel does; no fault, trap or hang.
+constexpr uint64_t SELFTEST_LIMIT_NS = 1000000ull;   // 1 ms
+
+__global__ void __launch_bounds__(32) selftest_waits_kernel(int* hdrs, uint32_t* counter) {
+  constexpr uint64_t limit_ns = SELFTEST_LIMIT_NS;
+  __shared__ __align__(8) uint64_t bar[1];
+  __shared__ int abort_flag[3];
+  if (threadIdx.x != 0) return;
+  abort_flag[0] = abort_flag[1] = abort_flag[2] = 0;
+  mbar_init(bar, 1);
+  fence_mbar_init();
+  const Ctx c0{bar, abort_flag + 0, hdrs};
+  const Ctx c1{bar, abort_flag + 1, hdrs + HDR_WORDS};
+  const Ctx c2{bar, abort_flag + 2, hdrs + 2 * HDR_WORDS};
+  if (wait_bar<limit_ns>(c0, 0, 0, 42)) hdrs[HDR_DIAG] = -1;                 // must not succeed
+  if (acquire_turn<limit_ns>(c1, counter, 1u)) hdrs[HDR_WORDS + HDR_DIAG] = -1;
+  hdrs[2 * HDR_WORDS + HDR_STATUS] = ATTN_ERR_DEVICE_FLAG;          // "another CTA failed"
+  const uint64_t t0 = globaltimer();
+  const bool got = acquire_turn<limit_ns>(c2, counter, 1u);
+  hdrs[2 * HDR_WORDS + HDR_DIAG] = (!got && globaltimer() - t0 < limit_ns / 2) ? 1 : 0;
+}
+
+int selftest_waits(void* scratch, size_t bytes, cudaStream_t st, int status[3]) {
+  const size_t need = 3 * HDR_WORDS * sizeof(int) + 16;
+  if (!scratch || bytes < need || (reinterpret_cast<uintptr_t>(scratch) & 15u) != 0) return ATTN_ERR_INVALID_ARG;
+  int* hdrs = static_cast<int*>(scratch);
+  uint32_t* counter = reinterpret_cast<uint32_t*>(hdrs + 3 * HDR_WORDS);
+  if (cudaMemsetAsync(scratch, 0, need, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  selftest_waits_kernel<<<1, 32, 0, st>>>(hdrs, counter);
+  int h[3 * HDR_WORDS];
+  if (cudaMemcpyAsync(h, scratch, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
+  status[0] = h[HDR_DIAG] == 42 ? h[HDR_STATUS] : ATTN_ERR_DEVICE_FLAG;
+  status[1] = h[HDR_WORDS + HDR_DIAG] == 33 ? h[HDR_WORDS + HDR_STATUS] : ATTN_ERR_DEVICE_FLAG;
+  status[2] = h[2 * HDR_WORDS + HDR_DIAG] == 1 ? ATTN_OK : ATTN_ERR_DEVICE_FLAG;
+  return ATTN_OK;
+}
+
 // ------------------------------------------------------------------ host side
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -896,6 +942,10 @@ static int launch_mode(const Problem& P, cudaStream_t st) {
 }
 
 }  // namespace tc
+
+int selftest_waits(void* scratch, size_t bytes, cudaStream_t st, int status[3]) {
+  return tc::selftest_waits(scratch, bytes, st, status);
+}
 
 int launch_bwd_tc(const Problem& P, cudaStream_t st) {
   if (P.dtype == ATTN_FP16) return tc::launch_mode<__half>(P, st);

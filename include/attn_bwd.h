@@ -212,6 +212,20 @@ const char* attn_status_string(int status);
  *   use attn_bwd with a caller workspace when that status is needed. */
 int attn_bwd_static_ws(const attn_bwd_params* p, cudaStream_t stream);
 
+/* Self-test of the bounded waits the backward kernels rely on (the pages ask
+ * for loud failure instead of silent corruption: aiter PR #2216's launcher
+ * returns an error, TE PR #671's check aborts).  One CTA runs, each bounded
+ * at 1 ms:
+ *   status[0]: an mbarrier wait whose phase never completes -> ATTN_ERR_TIMEOUT;
+ *   status[1]: a wait for a turn counter that nobody advances -> ATTN_ERR_TIMEOUT;
+ *   status[2]: the same wait entered after another CTA recorded an error,
+ *              which must give up at once -> ATTN_OK when it did.
+ * No GPU fault, trap or unbounded wait is involved.  `scratch` is a device
+ * buffer of at least 3 * 128 * 4 + 16 bytes, 16-byte aligned, owned by the
+ * caller; its contents are overwritten.  Synchronises `stream`.  Returns
+ * ATTN_OK when the test ran (the results are in status), an error otherwise. */
+int attn_selftest_waits(void* scratch, size_t scratch_bytes, cudaStream_t stream, int status[3]);
+
 #ifdef __cplusplus
 }
 #endif

@@ -224,3 +224,16 @@ def test_outputs_and_workspace_guard_bands(B):
         for b, t in zip(bufs, outs):
             assert torch.isnan(b[:g]).all() and torch.isnan(b[-g:]).all()
             assert torch.isfinite(t).all()
+
+
+def test_bounded_waits_expire_into_a_status(B):
+    """Failure detection without a GPU fault: waits that can never end give up
+    within their bound and report ATTN_ERR_TIMEOUT; a turn wait gives up at once
+    when another CTA has already failed.  The context stays usable afterwards."""
+    scratch = torch.zeros(B.SELFTEST_SCRATCH_BYTES, dtype=torch.uint8, device="cuda")
+    rc, status = B.attn_selftest_waits(scratch.data_ptr(), scratch.numel(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    assert status == [-6, -6, 0], status
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum()) == 8.0   # the device still works
+
