@@ -75,8 +75,8 @@ def peaks():
 KERNEL_SOURCES = ("tc_kernel.cu", "common.cuh", "sm100_ptx.cuh")
 KERNEL_TRAFFIC = {
     "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:ordered": {
-        "bytes": 621.25e6 + 279.25e6,
-        "src": "af006fa446a5c341",
+        "bytes": 621.21e6 + 282.95e6,
+        "src": "90fdca785860b58d",
         "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
     "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:split": {
         "bytes": 551.55e6 + 2.19e9,
