@@ -20,7 +20,6 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_bwd.so")
-STAMP = os.path.join(OUT_DIR, "stamp.txt")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
@@ -52,19 +51,34 @@ def _digest(extra_flags) -> str:
     return h.hexdigest()
 
 
-def build_library(verbose: bool = False, extra_flags=(), force: bool = False) -> str:
-    """Compile (if needed) and return the path of libattn_bwd.so."""
-    os.makedirs(OUT_DIR, exist_ok=True)
+# Named builds besides the release library: "debug" compiles every kernel with
+# -DATTN_DEBUG (device-side index checks that record a failing check in the
+# workspace header and skip the access).
+VARIANTS = {"": (), "debug": ("-DATTN_DEBUG",)}
+
+
+def library_path(variant: str = "") -> str:
+    return LIB if not variant else os.path.join(PKG, f"libattn_bwd_{variant}.so")
+
+
+def build_library(verbose: bool = False, extra_flags=(), force: bool = False, variant: str = "") -> str:
+    """Compile (if needed) and return the path of libattn_bwd.so (or of a named
+    variant, e.g. "debug")."""
+    extra_flags = tuple(VARIANTS[variant]) + tuple(extra_flags)
+    lib_path = library_path(variant)
+    out_dir = OUT_DIR if not variant else os.path.join(OUT_DIR, variant)
+    stamp = os.path.join(out_dir, "stamp.txt")
+    os.makedirs(out_dir, exist_ok=True)
     digest = _digest(extra_flags)
-    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
-        with open(STAMP) as f:
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
+        with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
+                return lib_path
     cc = nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = [cc] + NVCC_FLAGS + list(extra_flags) + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -76,15 +90,15 @@ def build_library(verbose: bool = False, extra_flags=(), force: bool = False) ->
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib_path)
+    with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

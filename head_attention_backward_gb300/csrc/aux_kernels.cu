@@ -122,6 +122,7 @@ __device__ __forceinline__ void write_row_stats(const Problem& P, long long r, f
     const long long b = tok / P.sq, q = tok - b * P.sq;
     li = (b * P.hq + h) * P.sq + q;
   }
+  if (!ATTN_INDEX_OK(P, li >= 0 && li < P.n_lse, 8)) return;
   const float l = P.lse[li];
   P.dvec[li] = acc;
   P.nlse2[li] = (l == -INFINITY) ? -INFINITY : -l * LOG2E;
@@ -292,7 +293,8 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
     };
     for (int k0 = next(0); k0 < nkv;) {
       const int k1 = next(k0 + 1);
-      add_tiles(dq_tile(P, k0, h, t), k1 < nkv ? dq_tile(P, k1, h, t) : nullptr);
+      if (ATTN_INDEX_OK(P, k0 < P.nsplits && t < P.ntiles, 10))
+        add_tiles(dq_tile(P, k0, h, t), k1 < nkv ? dq_tile(P, k1, h, t) : nullptr);
       k0 = k1 < nkv ? next(k1 + 1) : nkv;
     }
   } else if (s.lk > 0) {   // atomic and ordered fold: the single, pre-zeroed slice
@@ -302,7 +304,8 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
   for (int i = 0; i < NACC; ++i) {
     const int v = threadIdx.x + i * RC_THREADS;
     const int c = (4 * v) / dqk, e = (4 * v) - c * dqk;   // query row, first d
-    if (v < nv4 && c < nvalid) {
+    if (v < nv4 && c < nvalid &&
+        ATTN_INDEX_OK(P, s.q0 + qt * BM + c >= 0 && s.q0 + qt * BM + c < rows_q(P) && h < P.hq, 9)) {
       T* row = dQ + ((long long)(s.q0 + qt * BM + c) * P.hq + h) * dqk + e;
       T o4[4] = {TypeOps<T>::from_f(acc[i].x * P.scale), TypeOps<T>::from_f(acc[i].y * P.scale),
                  TypeOps<T>::from_f(acc[i].z * P.scale), TypeOps<T>::from_f(acc[i].w * P.scale)};

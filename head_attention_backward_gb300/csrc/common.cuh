@@ -285,6 +285,26 @@ __device__ __forceinline__ void set_status(const Problem& P, int code) {
   atomicCAS(P.hdr + HDR_STATUS, 0, code);
 }
 
+// Debug builds (-DATTN_DEBUG): every computed index is checked against the
+// buffer it addresses before the access.  A failing check records
+// ATTN_ERR_DEVICE_FLAG and its id (HDR_DIAG = 1000 + id, first failure wins)
+// in the workspace header and the access is skipped: no trap and no fault.
+// Release builds compile the checks away.
+#ifdef ATTN_DEBUG
+static __device__ __noinline__ bool debug_index_fail(int* hdr, int id) {
+  atomicCAS(hdr + HDR_STATUS, 0, ATTN_ERR_DEVICE_FLAG);
+  atomicCAS(hdr + HDR_DIAG, 0, 1000 + id);
+  return false;
+}
+#define ATTN_INDEX_OK(P, cond, id) ((cond) ? true : ::attn::debug_index_fail((P).hdr, (id)))
+#else
+#define ATTN_INDEX_OK(P, cond, id) true
+#endif
+
+// Rows of the q / k tensors (packed tokens in group mode).
+__host__ __device__ inline long long rows_q(const Problem& P) { return P.group ? (long long)P.tq : (long long)P.nseg * P.sq; }
+__host__ __device__ inline long long rows_k(const Problem& P) { return P.group ? (long long)P.tk : (long long)P.nseg * P.sk; }
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

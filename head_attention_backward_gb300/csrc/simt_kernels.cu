@@ -245,17 +245,19 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
         if (qs + c >= sg.lq) continue;
         float a = 0.f;
         for (int rr = 0; rr < BN; ++rr) a += sdS[rr * (BM + 1) + c] * sK[rr * ks + e];
-        float* tile = dq_tile(P, P.det ? kt : 0, h, qtile_index(P, b, qt));
+        const int tix = qtile_index(P, b, qt);
+        if (!ATTN_INDEX_OK(P, tix >= 0 && tix < P.ntiles && (!P.det || kt < P.nsplits), 11)) continue;
+        float* tile = dq_tile(P, P.det ? kt : 0, h, tix);
         if (P.det) tile[c * dqk + e] = a;
         else atomicAdd(tile + c * dqk + e, a);
       }
     }
   }
   __syncthreads();
-  if (r < klen) {
+  const long long krow = (long long)(sg.k0 + kv0 + r) * P.hkv + hk;
+  if (r < klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P) * P.hkv, 12)) {
     T* dK = static_cast<T*>(P.dk);
     T* dV = static_cast<T*>(P.dv_out);
-    const long long krow = (long long)(sg.k0 + kv0 + r) * P.hkv + hk;
     for (int e = 0; e < dqk; ++e) dK[krow * dqk + e] = TypeOps<T>::from_f(sdK[r * ks + e] * P.scale);
     for (int e = 0; e < dv; ++e) dV[krow * dv + e] = TypeOps<T>::from_f(sdV[r * vs + e]);
   }

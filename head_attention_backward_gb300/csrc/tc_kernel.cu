@@ -228,6 +228,11 @@ __device__ __forceinline__ bool acquire_turn(const Ctx& c, const uint32_t* turn,
   return true;
 }
 
+// Ordered fold: (query head, query tile) addresses a turn counter.
+__device__ __forceinline__ bool dq_ok_turn(const Problem& P, int h, int tile) {
+  return h >= 0 && h < P.hq && tile >= 0 && tile < P.ntiles;
+}
+
 template <typename T> struct IsHalf { static constexpr bool value = false; };
 template <> struct IsHalf<__half> { static constexpr bool value = true; };
 
@@ -342,7 +347,8 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       if (!wait_bar(ctx, B_KV_EMPTY, (it & 1) ^ 1, 2)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar + B_KV_FULL, C::KV_BYTES);
-        const int krow = I.sg.k0 + I.kt * BN;
+        int krow = I.sg.k0 + I.kt * BN;
+        if (!ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P) && I.hk >= 0 && I.hk < P.hkv, 4)) krow = 0;
         for (int c = 0; c < C::NCK; ++c)
           tma_load_3d(smem + C::OFF_K + c * C::KCH, &maps.k, bar + B_KV_FULL, c * 64, I.hk, krow);
         for (int c = 0; c < C::NCV; ++c)
@@ -359,14 +365,17 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         for (int c = lane; c < BM; c += 32) {
           const int q = qt * BM + c;
           const bool valid = q < I.sg.lq;
-          const long long li = valid ? lse_row(P, I.b, h, I.sg, q) : 0;
-          cp_async_4(sL + st * BM + c, P.nlse2 + li, valid ? 4u : 0u);
-          cp_async_4(sD + st * BM + c, P.dvec + li, valid ? 4u : 0u);
+          long long li = valid ? lse_row(P, I.b, h, I.sg, q) : 0;
+          const bool li_ok = !valid || ATTN_INDEX_OK(P, li >= 0 && li < P.n_lse, 3);
+          if (!li_ok) li = 0;
+          cp_async_4(sL + st * BM + c, P.nlse2 + li, valid && li_ok ? 4u : 0u);
+          cp_async_4(sD + st * BM + c, P.dvec + li, valid && li_ok ? 4u : 0u);
         }
         cp_async_arrive_noinc(bar + B_Q_FULL + st);
         if (lane == 0) {
           mbar_arrive_expect_tx(bar + B_Q_FULL + st, C::QDO_BYTES);
-          const int qrow = I.sg.q0 + qt * BM;
+          int qrow = I.sg.q0 + qt * BM;
+          if (!ATTN_INDEX_OK(P, qrow >= 0 && qrow < rows_q(P) && h >= 0 && h < P.hq, 4)) qrow = 0;
           for (int c = 0; c < C::NCK; ++c)
             tma_load_3d(smem + C::OFF_Q + (st * C::NCK + c) * C::QCH, &maps.q, bar + B_Q_FULL + st, c * 64, h, qrow);
           for (int c = 0; c < C::NCV; ++c)
@@ -668,7 +677,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       const ItemInfo I = item_info(P, item);
       const long long krow = (long long)(I.sg.k0 + I.kt * BN + L) * P.hkv + I.hk;
       if (I.nsteps == 0) {
-        if (L < I.klen) {
+        if (L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P) * P.hkv, 2)) {
           for (int e = 0; e < DQK; ++e) dKg[krow * DQK + e] = TypeOps<T>::from_f(0.f);
           for (int e = 0; e < DV; ++e) dVg[krow * DV + e] = TypeOps<T>::from_f(0.f);
         }
@@ -683,14 +692,17 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         // ordered fold: this partial is number `rank` of the tile's sum; lane 0
         // of each warp reads the tile's counter before the dQ tile is ready
         uint32_t idx = 0, rank = 0, seen = ~0u;
-        if (FOLD && lane == 0) {
+        if (FOLD && lane == 0 && ATTN_INDEX_OK(P, dq_ok_turn(P, h, tile), 5)) {
           idx = (uint32_t)(h * P.ntiles + tile);
-          rank = (uint32_t)(I.kt - __ldg(P.klo + tile));
-          seen = ld_acquire_gpu(P.turn + idx);
+          const int k0 = __ldg(P.klo + tile);
+          rank = (uint32_t)(I.kt - k0);
+          if (ATTN_INDEX_OK(P, k0 >= 0 && k0 <= I.kt, 6)) seen = ld_acquire_gpu(P.turn + idx);
         }
         if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
         tc_fence_after();
         float* dst_tile = dq_tile(P, DQM == DQ_SPLIT ? I.kt : 0, h, tile);
+        const bool dq_ok = ATTN_INDEX_OK(P, h >= 0 && h < P.hq && tile >= 0 && tile < P.ntiles &&
+                                                (DQM != DQ_SPLIT || (I.kt >= 0 && I.kt < P.nsplits)), 1);
 #pragma unroll 1
         for (int mb = 0; mb < C::NMB && ok; ++mb) {
           const int rows = min(128, DQK - mb * 128);
@@ -713,7 +725,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
               if (!ok) break;
               __syncwarp();   // the other lanes' adds come after lane 0's acquire
             }
-            if (L < rows) {
+            if (L < rows && dq_ok) {
               // tile stored query-major ([BM][d_qk]): for each query the warp's
               // 32 consecutive d values fill one 128-byte line, written straight
               // from registers.  (A shared-memory staging round trip plus TMA
@@ -751,7 +763,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       g += I.nsteps;
       if (!wait_bar(ctx, B_DKV_FULL, it & 1, 32)) break;
       tc_fence_after();
-      const bool row_ok = L < I.klen;
+      const bool row_ok = L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P) * P.hkv, 2);
 #pragma unroll 1
       for (int ch = 0; ch < DQK / 32; ++ch) {
         uint32_t x[32];

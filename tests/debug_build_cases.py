@@ -1,0 +1,56 @@
+"""Small ragged, windowed and GQA cases run on the -DATTN_DEBUG build of the
+library (device-side index checks at every computed address).  Run as a
+child process by tests/test_gpu_debug_build.py, so that the debug library is
+the only one loaded in it.  Exits non-zero on the first failed case."""
+import sys
+
+import torch
+
+sys.path.insert(0, __file__.rsplit("/tests/", 1)[0])
+from head_attention_backward_gb300 import binding as B  # noqa: E402
+from head_attention_backward_gb300 import build, workloads as W  # noqa: E402
+from oracle import attn_ref as R  # noqa: E402
+from tests.parity import assert_all_ok, compare, per_segment_report, tolerances  # noqa: E402
+
+
+def case_list():
+    wl = lambda *a, **k: W.Workload(*a, **k)
+    return [
+        W.thd("thd_ragged", [1, 1, 130, 1, 100, 80, 76], hq=4, hkv=2, seed=91),
+        wl("win192", torch.bfloat16, 1, 2, 2, 300, 300, 192, 128, W.MASK_WINDOW, 70, 0, False, 92, None),
+        wl("br_short_k", torch.bfloat16, 1, 2, 1, 200, 90, 128, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, -1, -1, False, 93, None),
+        wl("nomask_sq_ne_sk", torch.bfloat16, 2, 2, 2, 70, 150, 64, 64, W.MASK_NONE, -1, -1, False, 94, None),
+        wl("fp32", torch.float32, 1, 2, 1, 150, 150, 64, 64, W.MASK_CAUSAL_TOP_LEFT, -1, -1, False, 95, None),
+    ]
+
+
+def main():
+    B.load(build.build_library(variant="debug"))
+    for w in case_list():
+        x = w.inputs()
+        cu = w.cu_seqlens()
+        kw = dict(mask=w.mask, left=w.left, right=w.right, cu_seqlens_q=cu, cu_seqlens_k=cu)
+        o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], w.scale, **kw)
+        o_in, lse_in = o64.to(w.dtype), lse64.to(torch.float32)
+        ref = R.attn_backward(x["q"], x["k"], x["v"], o_in, x["do"], lse_in, w.scale, **kw)
+        d = {k: v.cuda() for k, v in x.items()}
+        cu_d = None if cu is None else cu.cuda()
+        tol, mcos = tolerances(w.dtype)
+        for mode in (0, 1, 2):
+            got = B.attn_backward(d["q"], d["k"], d["v"], o_in.cuda(), d["do"], lse_in.cuda(), scale=w.scale,
+                                  mask=w.mask, left=w.left, right=w.right, deterministic=mode,
+                                  cu_seqlens_q=cu_d, cu_seqlens_k=cu_d, max_seqlen_q=w.sq, max_seqlen_k=w.sk)
+            torch.cuda.synchronize()
+            reps = []
+            for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+                rep = compare(g.cpu(), r, tol, mcos)
+                rep["tensor"] = name
+                reps.append(rep)
+                if cu is not None:
+                    reps.extend(per_segment_report(g.cpu(), r, cu.tolist(), name, tol, mcos))
+            assert_all_ok(reps, f"{w.name} mode {mode} (debug build)")
+            print(f"ok {w.name} mode {mode}")
+
+
+if __name__ == "__main__":
+    main()
