@@ -258,8 +258,10 @@ def run_ours(args, wl):
     d = {k: v.to(dev) for k, v in x.items()}
     cu = wl.cu_seqlens()
     cu_d = None if cu is None else cu.to(dev)
+    cuk = wl.cu_seqlens_k()
+    cuk_d = None if cuk is None else cuk.to(dev)
     kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
-              cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+              cu_seqlens_k=cuk_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
     o, lse = B.attn_forward(d["q"], d["k"], d["v"], **kw)
     outs = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]))
     p = B.bwd_params(d["q"], d["k"], d["v"], o, d["do"], lse, *outs, deterministic=dq_mode(wl), **kw)

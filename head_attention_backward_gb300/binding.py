@@ -9,6 +9,7 @@ not been built: there is no fallback path.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 from typing import Optional
 
@@ -33,7 +34,7 @@ class AttnBwdParams(ctypes.Structure):
     _fields_ = [("dtype", _i32), ("batch", _i32), ("nhead_q", _i32), ("nhead_kv", _i32),
                 ("seqlen_q", _i32), ("seqlen_k", _i32), ("total_q", _i32), ("total_k", _i32),
                 ("d_qk", _i32), ("d_v", _i32), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
-                ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
+                ("cu_seqlens_q_padded", _vp), ("cu_seqlens_k_padded", _vp), ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
                 ("softmax_scale", _f32), ("deterministic", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("dout", _vp), ("lse", _vp),
                 ("dq", _vp), ("dk", _vp), ("dv", _vp)]
@@ -43,7 +44,7 @@ class AttnFwdParams(ctypes.Structure):
     _fields_ = [("dtype", _i32), ("batch", _i32), ("nhead_q", _i32), ("nhead_kv", _i32),
                 ("seqlen_q", _i32), ("seqlen_k", _i32), ("total_q", _i32), ("total_k", _i32),
                 ("d_qk", _i32), ("d_v", _i32), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
-                ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
+                ("cu_seqlens_q_padded", _vp), ("cu_seqlens_k_padded", _vp), ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
                 ("softmax_scale", _f32), ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp)]
 
 
@@ -171,12 +172,13 @@ def _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k):
 
 def bwd_params(q, k, v, o, do, lse, dq, dk, dv, *, scale, mask=MASK_NONE, left=-1, right=-1,
                deterministic=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0,
-               max_seqlen_k=0) -> AttnBwdParams:
+               max_seqlen_k=0, cu_seqlens_q_padded=None, cu_seqlens_k_padded=None) -> AttnBwdParams:
     p = AttnBwdParams()
     p.dtype = _DTYPES[q.dtype]
     for name, val in _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k).items():
         setattr(p, name, val)
     p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    p.cu_seqlens_q_padded, p.cu_seqlens_k_padded = _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_k_padded)
     p.mask, p.window_left, p.window_right = mask, left, right
     p.softmax_scale = scale
     p.deterministic = int(deterministic)   # False/True or an attn_det_t value (0, 1, 2)
@@ -186,12 +188,14 @@ def bwd_params(q, k, v, o, do, lse, dq, dk, dv, *, scale, mask=MASK_NONE, left=-
 
 
 def fwd_params(q, k, v, o, lse, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlens_q=None,
-               cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0) -> AttnFwdParams:
+               cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, cu_seqlens_q_padded=None,
+               cu_seqlens_k_padded=None) -> AttnFwdParams:
     p = AttnFwdParams()
     p.dtype = _DTYPES[q.dtype]
     for name, val in _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k).items():
         setattr(p, name, val)
     p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    p.cu_seqlens_q_padded, p.cu_seqlens_k_padded = _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_k_padded)
     p.mask, p.window_left, p.window_right = mask, left, right
     p.softmax_scale = scale
     p.q, p.k, p.v, p.o, p.lse = (_ptr(t) for t in (q, k, v, o, lse))
@@ -210,17 +214,21 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def attn_forward(q, k, v, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlens_q=None,
-                 cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, stream=None):
-    """O and LSE from the library's forward helper (outputs allocated here)."""
+                 cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, cu_seqlens_q_padded=None,
+                 cu_seqlens_k_padded=None, stream=None):
+    """O and LSE from the library's forward helper (outputs allocated here; the
+    padding rows of a padded layout, which the helper leaves alone, hold O = 0
+    and LSE = -inf)."""
     if cu_seqlens_q is None:
         o = torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
         lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
     else:
-        o = torch.empty(q.shape[:2] + (v.shape[-1],), dtype=q.dtype, device=q.device)
-        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+        o = torch.zeros(q.shape[:2] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+        lse = torch.full((q.shape[1], q.shape[0]), -math.inf, dtype=torch.float32, device=q.device)
     p = fwd_params(q, k, v, o, lse, scale=scale, mask=mask, left=left, right=right,
                    cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
-                   max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
+                   max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                   cu_seqlens_q_padded=cu_seqlens_q_padded, cu_seqlens_k_padded=cu_seqlens_k_padded)
     st = attn_fwd(p, _stream(stream))
     if st != 0:
         raise AttnError(st, "attn_fwd")
@@ -229,14 +237,16 @@ def attn_forward(q, k, v, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlen
 
 def attn_backward(q, k, v, o, do, lse, *, scale, mask=MASK_NONE, left=-1, right=-1,
                   deterministic=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0,
-                  max_seqlen_k=0, workspace=None, out=None, stream=None, check_status=True):
+                  max_seqlen_k=0, cu_seqlens_q_padded=None, cu_seqlens_k_padded=None,
+                  workspace=None, out=None, stream=None, check_status=True):
     """dQ, dK, dV through attn_bwd (outputs and workspace allocated here unless given)."""
     if out is None:
         out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     dq, dk, dv = out
     p = bwd_params(q, k, v, o, do, lse, dq, dk, dv, scale=scale, mask=mask, left=left, right=right,
                    deterministic=deterministic, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
-                   max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
+                   max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                   cu_seqlens_q_padded=cu_seqlens_q_padded, cu_seqlens_k_padded=cu_seqlens_k_padded)
     n = workspace_bytes(p)
     if workspace is None or workspace.numel() < n:
         workspace = alloc_workspace(n, q.device)

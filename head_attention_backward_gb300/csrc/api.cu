@@ -32,6 +32,8 @@ static int validate_common(const Prm* p) {
   if (p->seqlen_q < 0 || p->seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
   const bool gq = p->cu_seqlens_q != nullptr, gk = p->cu_seqlens_k != nullptr;
   if (gq != gk) return ATTN_ERR_INVALID_ARG;   // group mode needs both seqstart arrays
+  // padded starts only refine group mode
+  if (!gq && (p->cu_seqlens_q_padded || p->cu_seqlens_k_padded)) return ATTN_ERR_INVALID_ARG;
   if (gq && (p->total_q < 0 || p->total_k < 0)) return ATTN_ERR_INVALID_ARG;
   if (p->mask < ATTN_MASK_NONE || p->mask > ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;
   if (p->mask == ATTN_MASK_WINDOW && (p->window_left < -1 || p->window_right < -1))
@@ -87,6 +89,9 @@ static Problem make_problem(const attn_bwd_params& p, void* ws) {
   P.dv = p.d_v;
   P.cu_q = p.cu_seqlens_q;
   P.cu_k = p.cu_seqlens_k;
+  P.st_q = p.cu_seqlens_q_padded ? p.cu_seqlens_q_padded : p.cu_seqlens_q;
+  P.st_k = p.cu_seqlens_k_padded ? p.cu_seqlens_k_padded : p.cu_seqlens_k;
+  P.padded = P.group && (p.cu_seqlens_q_padded || p.cu_seqlens_k_padded) ? 1 : 0;
   P.mask = p.mask;
   P.left = p.mask == ATTN_MASK_WINDOW ? p.window_left : -1;
   P.right = p.mask == ATTN_MASK_WINDOW ? p.window_right : -1;
@@ -121,7 +126,9 @@ static void log_config(const attn_bwd_params& p, const WsLayout& L) {
   std::fprintf(stderr,
                "[attn_bwd] dtype=%d mode=%s batch=%d hq=%d hkv=%d sq=%d sk=%d tq=%d tk=%d d_qk=%d d_v=%d "
                "mask=%d window=(%d,%d) scale=%g det=%d nsplits=%d items<=%d workspace=%zu\n",
-               p.dtype, p.cu_seqlens_q ? "group" : "batch", p.batch, p.nhead_q, p.nhead_kv, p.seqlen_q,
+               p.dtype,
+               p.cu_seqlens_q ? (p.cu_seqlens_q_padded || p.cu_seqlens_k_padded ? "group-padded" : "group")
+                              : "batch", p.batch, p.nhead_q, p.nhead_kv, p.seqlen_q,
                p.seqlen_k, p.total_q, p.total_k, p.d_qk, p.d_v, p.mask, p.window_left, p.window_right,
                p.softmax_scale, p.deterministic, L.nsplits, L.max_items, L.total);
 }

@@ -30,12 +30,22 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P) {
   if (tid >= 16 && tid < HDR_WORDS) P.hdr[tid] = 0;   // optional per-site wait counters
   __syncthreads();
   if (P.group) {
+    // lengths from the logical offsets; each segment's physical rows
+    // [start, start + length) lie before the next segment's start and inside
+    // the tensor (without padding the starts are the offsets themselves and
+    // the last one must equal the row total)
     for (int b = tid; b < P.nseg; b += blockDim.x) {
-      const int q0 = P.cu_q[b], q1 = P.cu_q[b + 1];
-      const int k0 = P.cu_k[b], k1 = P.cu_k[b + 1];
-      bool bad = q1 < q0 || k1 < k0 || q1 - q0 > P.sq || k1 - k0 > P.sk;
-      if (b == 0) bad |= q0 != 0 || k0 != 0;
-      if (b == P.nseg - 1) bad |= q1 != P.tq || k1 != P.tk;
+      const int lq = P.cu_q[b + 1] - P.cu_q[b], lk = P.cu_k[b + 1] - P.cu_k[b];
+      bool bad = lq < 0 || lk < 0 || lq > P.sq || lk > P.sk;
+      const long long sq0 = P.st_q[b], sq1 = P.st_q[b + 1];
+      const long long sk0 = P.st_k[b], sk1 = P.st_k[b + 1];
+      bad |= sq0 + lq > sq1 || sk0 + lk > sk1;
+      if (b == 0) bad |= P.cu_q[0] != 0 || P.cu_k[0] != 0 || sq0 < 0 || sk0 < 0;
+      if (b == P.nseg - 1) {
+        bad |= sq1 > P.tq || sk1 > P.tk;
+        if (P.st_q == P.cu_q) bad |= sq1 != P.tq;
+        if (P.st_k == P.cu_k) bad |= sk1 != P.tk;
+      }
       if (bad) s_bad = 1;
     }
   }
@@ -154,6 +164,20 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, __half*) {
   return s;
 }
 
+// Padded group layout: gradient rows that belong to no segment are zero.
+// Gap g in [0, nseg] holds the rows from the end of segment g-1 (row 0 for
+// g = 0) up to the start of segment g (the row total for g = nseg); the
+// schedule kernel has checked that the gaps are well formed.  Row sizes are
+// whole 4-byte words for every supported dtype and head dim.
+__device__ void zero_padding_rows(const int* st, const int* cu, int nseg, int total,
+                                  int row_words, uint32_t* out) {
+  for (int g = blockIdx.x; g <= nseg; g += gridDim.x) {
+    const long long a = g == 0 ? 0 : (long long)st[g - 1] + (cu[g] - cu[g - 1]);
+    const long long e = g == nseg ? total : st[g];
+    for (long long i = a * row_words + threadIdx.x; i < e * row_words; i += blockDim.x) out[i] = 0u;
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) preprocess_kernel(Problem P, long long ntok) {
   const int lane = threadIdx.x & 31;
@@ -188,6 +212,12 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem P, long long nt
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (lane == 0) write_row_stats(P, r, acc);
     }
+  }
+  if (P.padded && *(volatile const int*)(P.hdr + HDR_STATUS) == 0) {
+    const int w = (int)sizeof(T);
+    zero_padding_rows(P.st_q, P.cu_q, P.nseg, P.tq, P.hq * P.dqk * w / 4, static_cast<uint32_t*>(P.dq));
+    zero_padding_rows(P.st_k, P.cu_k, P.nseg, P.tk, P.hkv * P.dqk * w / 4, static_cast<uint32_t*>(P.dk));
+    zero_padding_rows(P.st_k, P.cu_k, P.nseg, P.tk, P.hkv * P.dv * w / 4, static_cast<uint32_t*>(P.dv_out));
   }
   if (!P.det || P.fold) {   // the single slice that partials are added into starts at zero
     float4* acc4 = reinterpret_cast<float4*>(P.dq_acc);

@@ -35,11 +35,14 @@ struct Problem {
   int nseg;          // B (batch) or number of segments (group)
   int hq, hkv, g;    // g = hq / hkv
   int sq, sk;        // batch: lengths; group: upper bounds
-  int tq, tk;        // group: packed totals
+  int tq, tk;        // group: physical row totals
   int dqk, dv;
   int group;         // 1 = THD group mode
-  const int* cu_q;
+  int padded;        // group mode with a padded start array on either side
+  const int* cu_q;   // logical offsets: segment lengths are their differences
   const int* cu_k;
+  const int* st_q;   // physical start row of each segment (cu_q unless padded)
+  const int* st_k;
   int mask, left, right;
   float scale;
   float scale_log2;  // scale * log2(e)
@@ -129,17 +132,17 @@ inline WsLayout ws_layout(const attn_bwd_params& p) {
 // ------------------------------------------------------------------ segments
 
 struct Seg {
-  int q0, lq;   // first packed row and length of the query segment
+  int q0, lq;   // first physical row and length of the query segment
   int k0, lk;   // same for keys
 };
 
 __device__ __forceinline__ Seg segment(const Problem& P, int b) {
   Seg s;
   if (P.group) {
-    s.q0 = __ldg(P.cu_q + b);
-    s.lq = __ldg(P.cu_q + b + 1) - s.q0;
-    s.k0 = __ldg(P.cu_k + b);
-    s.lk = __ldg(P.cu_k + b + 1) - s.k0;
+    s.q0 = __ldg(P.st_q + b);
+    s.lq = __ldg(P.cu_q + b + 1) - __ldg(P.cu_q + b);
+    s.k0 = __ldg(P.st_k + b);
+    s.lk = __ldg(P.cu_k + b + 1) - __ldg(P.cu_k + b);
   } else {
     s.q0 = b * P.sq;
     s.lq = P.sq;

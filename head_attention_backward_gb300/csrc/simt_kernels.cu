@@ -30,8 +30,10 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, int
   const int g = p.nhead_q / p.nhead_kv, hk = h / g;
   int q0, lq, k0, lk;
   if (group) {
-    q0 = p.cu_seqlens_q[b]; lq = p.cu_seqlens_q[b + 1] - q0;
-    k0 = p.cu_seqlens_k[b]; lk = p.cu_seqlens_k[b + 1] - k0;
+    lq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
+    lk = p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b];
+    q0 = p.cu_seqlens_q_padded ? p.cu_seqlens_q_padded[b] : p.cu_seqlens_q[b];
+    k0 = p.cu_seqlens_k_padded ? p.cu_seqlens_k_padded[b] : p.cu_seqlens_k[b];
   } else {
     q0 = b * p.seqlen_q; lq = p.seqlen_q; k0 = b * p.seqlen_k; lk = p.seqlen_k;
   }

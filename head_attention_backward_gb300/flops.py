@@ -33,7 +33,8 @@ def bwd_flops(wl) -> float:
     """FLOPs of one backward pass of a `workloads.Workload`."""
     per_pair = 2.0 * (3 * wl.d_qk + 2 * wl.d_v)
     if wl.group_mode:
-        pairs = sum(visible_pairs(n, n, wl.mask, wl.left, wl.right) for n in wl.seqlens)
+        pairs = sum(visible_pairs(nq, nk, wl.mask, wl.left, wl.right)
+                    for nq, nk in zip(wl.seqlens, wl.key_lengths))
     else:
         pairs = wl.batch * visible_pairs(wl.sq, wl.sk, wl.mask, wl.left, wl.right)
     return per_pair * pairs * wl.hq

@@ -38,6 +38,11 @@ class Workload:
     deterministic: bool = False
     seed: int = 0
     seqlens: Optional[List[int]] = None   # group (THD) mode when set
+    seqlens_k: Optional[List[int]] = None # key lengths per segment when they differ from seqlens
+    # padded group layout: gaps[g] = padding rows in front of segment g, the
+    # last entry after the last segment (nseg + 1 entries); None = packed
+    gaps_q: Optional[List[int]] = None
+    gaps_k: Optional[List[int]] = None
 
     @property
     def group_mode(self) -> bool:
@@ -48,22 +53,73 @@ class Workload:
         return 1.0 / math.sqrt(self.d_qk)
 
     @property
-    def total(self) -> int:
-        return sum(self.seqlens) if self.group_mode else self.batch * self.sq
-
-    def cu_seqlens(self) -> Optional[torch.Tensor]:
+    def key_lengths(self) -> Optional[List[int]]:
         if not self.group_mode:
             return None
+        return self.seqlens if self.seqlens_k is None else self.seqlens_k
+
+    @property
+    def total(self) -> int:
+        """Query rows of the tensors (padding rows included)."""
+        if not self.group_mode:
+            return self.batch * self.sq
+        return sum(self.seqlens) + (sum(self.gaps_q) if self.gaps_q else 0)
+
+    @property
+    def total_k(self) -> int:
+        if not self.group_mode:
+            return self.batch * self.sk
+        return sum(self.key_lengths) + (sum(self.gaps_k) if self.gaps_k else 0)
+
+    @staticmethod
+    def _starts(lengths, gaps) -> torch.Tensor:
+        """Physical start row of every segment, then the row total."""
+        st, r = [], 0
+        for b, n in enumerate(lengths):
+            r += gaps[b]
+            st.append(r)
+            r += n
+        st.append(r + gaps[len(lengths)])
+        return torch.tensor(st, dtype=torch.int32)
+
+    def cu_seqlens_q_padded(self) -> Optional[torch.Tensor]:
+        return self._starts(self.seqlens, self.gaps_q) if self.group_mode and self.gaps_q else None
+
+    def cu_seqlens_k_padded(self) -> Optional[torch.Tensor]:
+        return self._starts(self.key_lengths, self.gaps_k) if self.group_mode and self.gaps_k else None
+
+    def padding_rows(self, side: str) -> List[int]:
+        """Rows of the q ("q") or k ("k") tensors that belong to no segment."""
+        st = self.cu_seqlens_q_padded() if side == "q" else self.cu_seqlens_k_padded()
+        if st is None:
+            return []
+        lens = self.seqlens if side == "q" else self.key_lengths
+        inside = set()
+        for b, n in enumerate(lens):
+            inside.update(range(int(st[b]), int(st[b]) + n))
+        total = self.total if side == "q" else self.total_k
+        return [r for r in range(total) if r not in inside]
+
+    @staticmethod
+    def _offsets(lengths) -> torch.Tensor:
         cu = [0]
-        for n in self.seqlens:
+        for n in lengths:
             cu.append(cu[-1] + n)
         return torch.tensor(cu, dtype=torch.int32)
 
+    def cu_seqlens(self) -> Optional[torch.Tensor]:
+        """Query segment offsets (group mode), else None."""
+        return self._offsets(self.seqlens) if self.group_mode else None
+
+    def cu_seqlens_k(self) -> Optional[torch.Tensor]:
+        """Key segment offsets (group mode), else None."""
+        return self._offsets(self.key_lengths) if self.group_mode else None
+
     def shapes(self):
         if self.group_mode:
-            t = self.total
-            return dict(q=(t, self.hq, self.d_qk), k=(t, self.hkv, self.d_qk),
-                        v=(t, self.hkv, self.d_v), o=(t, self.hq, self.d_v),
+            t, tk = self.total, self.total_k
+            return dict(q=(t, self.hq, self.d_qk), k=(tk, self.hkv, self.d_qk),
+                        v=(tk, self.hkv, self.d_v), o=(t, self.hq, self.d_v),
                         lse=(self.hq, t))
         b = self.batch
         return dict(q=(b, self.sq, self.hq, self.d_qk), k=(b, self.sk, self.hkv, self.d_qk),
@@ -97,10 +153,22 @@ def random_segments(total: int, max_len: int, seed: int) -> List[int]:
 
 def thd(name: str, seqlens: List[int], hq=32, hkv=8, d_qk=128, d_v=128,
         mask=MASK_CAUSAL_TOP_LEFT, left=-1, right=-1, deterministic=False, seed=3,
-        dtype=torch.bfloat16) -> Workload:
+        dtype=torch.bfloat16, seqlens_k=None, gaps_q=None, gaps_k=None) -> Workload:
+    """THD workload; `seqlens_k` gives per-segment key lengths when they differ
+    from the query lengths (cross attention); `gaps_q` / `gaps_k` (one entry
+    per segment plus one) place padding rows around the segments."""
+    if seqlens_k is not None and len(seqlens_k) != len(seqlens):
+        raise ValueError("seqlens and seqlens_k need one entry per segment")
+    for gaps in (gaps_q, gaps_k):
+        if gaps is not None and len(gaps) != len(seqlens) + 1:
+            raise ValueError("gaps need one entry per segment plus one")
     mx = max(seqlens) if seqlens else 0
-    return Workload(name, dtype, len(seqlens), hq, hkv, mx, mx, d_qk, d_v, mask, left, right,
-                    deterministic, seed, list(seqlens))
+    mk = max(seqlens_k) if seqlens_k else mx
+    return Workload(name, dtype, len(seqlens), hq, hkv, mx, mk, d_qk, d_v, mask, left, right,
+                    deterministic, seed, list(seqlens),
+                    None if seqlens_k is None else list(seqlens_k),
+                    None if gaps_q is None else list(gaps_q),
+                    None if gaps_k is None else list(gaps_k))
 
 
 # The five workloads of the benchmark specification.

@@ -31,6 +31,19 @@
  *   q [Tq,Hq,d_qk], k [Tk,Hkv,d_qk], v [Tk,Hkv,d_v], lse [Hq,Tq]; segment b
  *   owns rows cu_seqlens_q[b]..cu_seqlens_q[b+1] and keys
  *   cu_seqlens_k[b]..cu_seqlens_k[b+1] and attends only within itself.
+ * - Padded group mode (cu_seqlens_q_padded / cu_seqlens_k_padded set): the
+ *   logical length of segment b still comes from cu_seqlens (Lq_b =
+ *   cu_seqlens_q[b+1] - cu_seqlens_q[b]), but its rows start at the
+ *   physical row cu_seqlens_q_padded[b], so segment b owns rows
+ *   padded[b] .. padded[b] + Lq_b - 1 and the rows up to padded[b+1] are
+ *   padding (the seqstart convention of TransformerEngine PR #446, review of
+ *   ck_fused_attn_fwd.cpp / ck_fused_attn_bwd.cpp, and of the "physical
+ *   seqstart" in aiter PR #2216's unified-workspace follow-up commit).
+ *   total_q / total_k then count physical rows, and lse is [Hq, total_q]
+ *   indexed by physical row.  Rows that belong to no segment are written
+ *   zero in dq, dk and dv.  Values in padding rows never reach a result,
+ *   but those of q, k, v and dout must be finite (tiles that overlap padding
+ *   multiply them by exact zeros).  Either side may be padded alone.
  * - Query head h reads kv head h / (Hq / Hkv) (GQA, contiguous groups).
  * - LSE is the natural-log log-sum-exp of the scaled scores, fp32; -inf
  *   marks a row with no visible key (its gradients are zero).
@@ -55,7 +68,8 @@ typedef enum {
   ATTN_ERR_CUDA = -4,                /* a CUDA runtime/driver call failed           */
   ATTN_ERR_DEVICE_FLAG = -5,         /* kernels reported an error (see read_status) */
   ATTN_ERR_TIMEOUT = -6,             /* a bounded in-kernel wait expired            */
-  ATTN_ERR_BAD_SEQLENS = -7          /* cu_seqlens not monotone / exceed the bounds */
+  ATTN_ERR_BAD_SEQLENS = -7          /* cu_seqlens (or the padded starts) not
+                                        monotone, overlapping or beyond the bounds */
 } attn_status_t;
 
 /* Mask kinds: the AITER mask enum reviewed in TransformerEngine PR #446
@@ -91,6 +105,11 @@ typedef struct {
   int32_t d_v;            /* head dim of v and o                                   */
   const int32_t* cu_seqlens_q; /* device, [batch+1], or NULL (batch mode)          */
   const int32_t* cu_seqlens_k; /* device, [batch+1], or NULL (batch mode)          */
+  const int32_t* cu_seqlens_q_padded; /* device, [batch+1]: physical start row of
+                             each query segment, or NULL (start = cu_seqlens_q);
+                             group mode only.  Must satisfy padded[b] + Lq_b <=
+                             padded[b+1] and padded[batch] <= total_q       */
+  const int32_t* cu_seqlens_k_padded; /* same for keys and total_k            */
   int32_t mask;           /* attn_mask_t                                           */
   int32_t window_left;    /* ATTN_MASK_WINDOW only; -1 = unbounded                 */
   int32_t window_right;   /* ATTN_MASK_WINDOW only; -1 = unbounded                 */
@@ -124,6 +143,8 @@ typedef struct {
   int32_t d_v;
   const int32_t* cu_seqlens_q;
   const int32_t* cu_seqlens_k;
+  const int32_t* cu_seqlens_q_padded;
+  const int32_t* cu_seqlens_k_padded;
   int32_t mask;
   int32_t window_left;
   int32_t window_right;
@@ -131,8 +152,9 @@ typedef struct {
   const void* q;
   const void* k;
   const void* v;
-  void* o;                /* device output [.., Hq, d_v], dtype                    */
-  float* lse;             /* device output, fp32 natural log                       */
+  void* o;                /* device output [.., Hq, d_v], dtype; padding rows of a
+                             padded group layout are left untouched            */
+  float* lse;             /* device output, fp32 natural log (padding rows likewise) */
 } attn_fwd_params;
 
 /* dQ accumulation modes (attn_bwd_params.deterministic).  The per-KV-tile dQ

@@ -34,6 +34,11 @@ Readings where the pages are silent (each is also listed in the design doc):
 5. GQA: query head h reads kv head h // (Hq / Hkv) (contiguous groups).
 6. Group (THD) mode: segment b owns query rows cu_q[b]:cu_q[b+1] and key rows
    cu_k[b]:cu_k[b+1]; the result is the block-diagonal one.
+7. Padded group mode (TransformerEngine PR #446, review of
+   ck_fused_attn_fwd.cpp / ck_fused_attn_bwd.cpp: the segment start comes
+   from the padded offsets when they are given, the length from cu_seqlens):
+   segment b owns rows st[b] : st[b] + (cu[b+1] - cu[b]).  Rows of no segment
+   get zero gradients, O = 0 and LSE = -inf.
 
 Layouts (the same as the C ABI): batch mode q [B,Sq,Hq,d], k [B,Sk,Hkv,d],
 v [B,Sk,Hkv,dv], o/do [B,Sq,Hq,dv], lse [B,Hq,Sq]; group mode drops B and
@@ -89,15 +94,22 @@ def visible(lq: int, lk: int, mask: int, left: int = -1, right: int = -1) -> tor
     return ok
 
 
-def _segments(batch_mode: bool, nseg: int, sq: int, sk: int, cu_q, cu_k):
+def _rows(cu, st, b):
+    """Physical rows of segment b: start st[b] (cu[b] when unpadded), length
+    cu[b+1] - cu[b] (reading 7)."""
+    n = int(cu[b + 1]) - int(cu[b])
+    r0 = int(cu[b]) if st is None else int(st[b])
+    return slice(r0, r0 + n)
+
+
+def _segments(batch_mode: bool, nseg: int, sq: int, sk: int, cu_q, cu_k, st_q=None, st_k=None):
     """(query slice, key slice) per batch entry or packed segment."""
     out = []
     for b in range(nseg):
         if batch_mode:
             out.append((b, slice(0, sq), slice(0, sk)))
         else:
-            out.append((b, slice(int(cu_q[b]), int(cu_q[b + 1])),
-                        slice(int(cu_k[b]), int(cu_k[b + 1]))))
+            out.append((b, _rows(cu_q, st_q, b), _rows(cu_k, st_k, b)))
     return out
 
 
@@ -131,7 +143,8 @@ def _probs(s, lse):
 
 
 def attn_forward(q, k, v, scale, mask=MASK_NONE, left=-1, right=-1,
-                 cu_seqlens_q=None, cu_seqlens_k=None):
+                 cu_seqlens_q=None, cu_seqlens_k=None, cu_seqlens_q_padded=None,
+                 cu_seqlens_k_padded=None):
     """Forward pass: returns (O, LSE) in fp64 with the layouts of the header."""
     batch_mode = cu_seqlens_q is None
     q, k, v = _as64(q), _as64(k), _as64(v)
@@ -146,10 +159,11 @@ def attn_forward(q, k, v, scale, mask=MASK_NONE, left=-1, right=-1,
         o = torch.zeros(q.shape[:2] + (v.shape[-1],), dtype=F64)
         lse = torch.full((hq, q.shape[0]), -math.inf, dtype=F64)
     g = hq // hkv
-    for b, rq, rk in _segments(batch_mode, nseg, sq, sk, cu_seqlens_q, cu_seqlens_k):
+    for b, rq, rk in _segments(batch_mode, nseg, sq, sk, cu_seqlens_q, cu_seqlens_k,
+                               cu_seqlens_q_padded, cu_seqlens_k_padded):
         qb, kb, vb = _views(q, batch_mode, b, rq), _views(k, batch_mode, b, rk), _views(v, batch_mode, b, rk)
         lq, lk = qb.shape[0], kb.shape[0]
-        if lq == 0:
+        if lq == 0 or lk == 0:   # no keys: every row keeps LSE = -inf and O = 0 (reading 2)
             continue
         vis = visible(lq, lk, mask, left, right)
         for h in range(hq):
@@ -164,7 +178,8 @@ def attn_forward(q, k, v, scale, mask=MASK_NONE, left=-1, right=-1,
 
 
 def attn_backward(q, k, v, o, do, lse, scale, mask=MASK_NONE, left=-1, right=-1,
-                  cu_seqlens_q=None, cu_seqlens_k=None):
+                  cu_seqlens_q=None, cu_seqlens_k=None, cu_seqlens_q_padded=None,
+                  cu_seqlens_k_padded=None):
     """Backward pass given the forward's O and LSE: returns (dQ, dK, dV) fp64.
 
     Per (segment, query head h, kv head g = h // G):
@@ -180,7 +195,8 @@ def attn_backward(q, k, v, o, do, lse, scale, mask=MASK_NONE, left=-1, right=-1,
     else:
         nseg, sq, sk, hq, hkv = len(cu_seqlens_q) - 1, None, None, q.shape[1], k.shape[1]
     g = hq // hkv
-    for b, rq, rk in _segments(batch_mode, nseg, sq, sk, cu_seqlens_q, cu_seqlens_k):
+    for b, rq, rk in _segments(batch_mode, nseg, sq, sk, cu_seqlens_q, cu_seqlens_k,
+                               cu_seqlens_q_padded, cu_seqlens_k_padded):
         qb, kb, vb = _views(q, batch_mode, b, rq), _views(k, batch_mode, b, rk), _views(v, batch_mode, b, rk)
         ob, dob = _views(o, batch_mode, b, rq), _views(do, batch_mode, b, rq)
         dqb, dkb, dvb = _views(dq, batch_mode, b, rq), _views(dk, batch_mode, b, rk), _views(dv, batch_mode, b, rk)

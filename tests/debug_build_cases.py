@@ -21,6 +21,11 @@ def case_list():
         wl("br_short_k", torch.bfloat16, 1, 2, 1, 200, 90, 128, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, -1, -1, False, 93, None),
         wl("nomask_sq_ne_sk", torch.bfloat16, 2, 2, 2, 70, 150, 64, 64, W.MASK_NONE, -1, -1, False, 94, None),
         wl("fp32", torch.float32, 1, 2, 1, 150, 150, 64, 64, W.MASK_CAUSAL_TOP_LEFT, -1, -1, False, 95, None),
+        W.thd("thd_cross_br", [100, 0, 37, 250, 5], hq=4, hkv=2, mask=W.MASK_CAUSAL_BOTTOM_RIGHT,
+              seed=96, seqlens_k=[300, 64, 0, 129, 200]),
+        W.thd("thd_padded", [100, 0, 37, 250, 5], hq=4, hkv=2, mask=W.MASK_CAUSAL_BOTTOM_RIGHT,
+              seed=97, seqlens_k=[300, 64, 0, 129, 200], gaps_q=[3, 0, 17, 140, 2, 9],
+              gaps_k=[0, 5, 131, 7, 1, 30]),
     ]
 
 
@@ -28,18 +33,20 @@ def main():
     B.load(build.build_library(variant="debug"))
     for w in case_list():
         x = w.inputs()
-        cu = w.cu_seqlens()
-        kw = dict(mask=w.mask, left=w.left, right=w.right, cu_seqlens_q=cu, cu_seqlens_k=cu)
+        cu, cuk = w.cu_seqlens(), w.cu_seqlens_k()
+        stq, stk = w.cu_seqlens_q_padded(), w.cu_seqlens_k_padded()
+        kw = dict(mask=w.mask, left=w.left, right=w.right, cu_seqlens_q=cu, cu_seqlens_k=cuk)
+        if stq is not None or stk is not None:
+            kw.update(cu_seqlens_q_padded=stq, cu_seqlens_k_padded=stk)
         o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], w.scale, **kw)
         o_in, lse_in = o64.to(w.dtype), lse64.to(torch.float32)
         ref = R.attn_backward(x["q"], x["k"], x["v"], o_in, x["do"], lse_in, w.scale, **kw)
         d = {k: v.cuda() for k, v in x.items()}
-        cu_d = None if cu is None else cu.cuda()
+        dkw = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
         tol, mcos = tolerances(w.dtype)
         for mode in (0, 1, 2):
             got = B.attn_backward(d["q"], d["k"], d["v"], o_in.cuda(), d["do"], lse_in.cuda(), scale=w.scale,
-                                  mask=w.mask, left=w.left, right=w.right, deterministic=mode,
-                                  cu_seqlens_q=cu_d, cu_seqlens_k=cu_d, max_seqlen_q=w.sq, max_seqlen_k=w.sk)
+                                  deterministic=mode, max_seqlen_q=w.sq, max_seqlen_k=w.sk, **dkw)
             torch.cuda.synchronize()
             reps = []
             for name, g, r in zip(("dq", "dk", "dv"), got, ref):
@@ -47,7 +54,9 @@ def main():
                 rep["tensor"] = name
                 reps.append(rep)
                 if cu is not None:
-                    reps.extend(per_segment_report(g.cpu(), r, cu.tolist(), name, tol, mcos))
+                    offs, st = (cu, stq) if name == "dq" else (cuk, stk)
+                    reps.extend(per_segment_report(g.cpu(), r, offs.tolist(), name, tol, mcos,
+                                                   None if st is None else st.tolist()))
             assert_all_ok(reps, f"{w.name} mode {mode} (debug build)")
             print(f"ok {w.name} mode {mode}")
 

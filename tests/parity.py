@@ -50,14 +50,18 @@ def compare(got, ref, tol_rel, min_cos, scale_floor=0.0):
     return dict(ok=ok, cos=cos, max_err=err, max_ref=max_ref, finite=finite)
 
 
-def per_segment_report(got, ref, cu, name, tol_rel, min_cos):
-    """One comparison per packed segment of a [T, H, D] tensor."""
+def per_segment_report(got, ref, cu, name, tol_rel, min_cos, starts=None):
+    """One comparison per segment of a [T, H, D] tensor; segment b has length
+    cu[b+1] - cu[b] and starts at row starts[b] (cu[b] when packed)."""
     out = []
     cu = [int(x) for x in cu]
+    starts = cu if starts is None else [int(x) for x in starts]
     floor = float(ref.detach().abs().max()) if ref.numel() else 0.0
     for b in range(len(cu) - 1):
-        r = compare(got[cu[b]:cu[b + 1]], ref[cu[b]:cu[b + 1]], tol_rel, min_cos, floor)
-        r.update(tensor=name, segment=b, length=cu[b + 1] - cu[b])
+        n = cu[b + 1] - cu[b]
+        rows = slice(starts[b], starts[b] + n)
+        r = compare(got[rows], ref[rows], tol_rel, min_cos, floor)
+        r.update(tensor=name, segment=b, length=n)
         out.append(r)
     return out
 

@@ -38,9 +38,10 @@ def _c_layout():
 int main(void) {
   printf("attn_bwd_params.size %zu\n", sizeof(attn_bwd_params));
   printf("attn_fwd_params.size %zu\n", sizeof(attn_fwd_params));
-  F(attn_bwd_params, cu_seqlens_q) F(attn_bwd_params, mask) F(attn_bwd_params, softmax_scale)
+  F(attn_bwd_params, cu_seqlens_q) F(attn_bwd_params, cu_seqlens_q_padded)
+  F(attn_bwd_params, cu_seqlens_k_padded) F(attn_bwd_params, mask) F(attn_bwd_params, softmax_scale)
   F(attn_bwd_params, deterministic) F(attn_bwd_params, q) F(attn_bwd_params, lse) F(attn_bwd_params, dv)
-  F(attn_fwd_params, cu_seqlens_k) F(attn_fwd_params, softmax_scale) F(attn_fwd_params, q) F(attn_fwd_params, lse)
+  F(attn_fwd_params, cu_seqlens_k) F(attn_fwd_params, cu_seqlens_k_padded) F(attn_fwd_params, softmax_scale) F(attn_fwd_params, q) F(attn_fwd_params, lse)
   return 0;
 }
 """
@@ -163,6 +164,16 @@ def test_group_mode_needs_both_seqstart_arrays(lib):
     p = make(total_q=100, total_k=100)
     p.cu_seqlens_q = 0x1000           # cu_seqlens_k left NULL
     assert B.attn_bwd_workspace_size(p)[0] == -1
+    assert B.attn_bwd(p, 0x100000, 1 << 40, 0) == -1
+
+
+def test_padded_starts_only_in_group_mode(lib):
+    p = make()                        # batch mode
+    p.cu_seqlens_q_padded = 0x1000
+    assert B.attn_bwd_workspace_size(p)[0] == -1
+    assert B.attn_bwd(p, 0x100000, 1 << 40, 0) == -1
+    p = make()
+    p.cu_seqlens_k_padded = 0x1000
     assert B.attn_bwd(p, 0x100000, 1 << 40, 0) == -1
 
 

@@ -34,8 +34,10 @@ def _run(B, wl, det):
     cu = wl.cu_seqlens()
     d = {k: v.cuda() for k, v in x.items()}
     cu_d = None if cu is None else cu.cuda()
+    cuk = wl.cu_seqlens_k()
+    cuk_d = None if cuk is None else cuk.cuda()
     kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
-              cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+              cu_seqlens_k=cuk_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
     o, lse = B.attn_forward(d["q"], d["k"], d["v"], **kw)
     got = B.attn_backward(d["q"], d["k"], d["v"], o, d["do"], lse, deterministic=det, **kw)
     torch.cuda.synchronize()

@@ -38,17 +38,21 @@ def run_backward_vs_oracle(B, wl, deterministic, ref_fwd=True):
     """Oracle forward -> rounded O / fp32 LSE -> GPU backward and oracle backward
     on identical inputs; returns reports per tensor (and per segment)."""
     x = wl.inputs()
-    cu = wl.cu_seqlens()
-    kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cu)
+    cu, cuk = wl.cu_seqlens(), wl.cu_seqlens_k()
+    stq, stk = wl.cu_seqlens_q_padded(), wl.cu_seqlens_k_padded()
+    kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cuk)
+    if stq is not None or stk is not None:
+        kw.update(cu_seqlens_q_padded=stq, cu_seqlens_k_padded=stk)
     o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, **kw)
     o_in, lse_in = o64.to(wl.dtype), lse64.to(torch.float32)
     ref = R.attn_backward(x["q"], x["k"], x["v"], o_in, x["do"], lse_in, wl.scale, **kw)
     dev = {k: v.cuda() for k, v in x.items()}
-    cu_d = None if cu is None else cu.cuda()
+    dkw = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
+    # outputs start as NaN: every row, padding included, must be written
+    out = tuple(torch.full_like(dev[n], float("nan")) for n in ("q", "k", "v"))
     got = B.attn_backward(dev["q"], dev["k"], dev["v"], o_in.cuda(), dev["do"], lse_in.cuda(),
-                          scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right,
-                          deterministic=deterministic, cu_seqlens_q=cu_d, cu_seqlens_k=cu_d,
-                          max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+                          scale=wl.scale, deterministic=deterministic, max_seqlen_q=wl.sq,
+                          max_seqlen_k=wl.sk, out=out, **dkw)
     torch.cuda.synchronize()
     tol, mcos = tolerances(wl.dtype)
     reps = []
@@ -58,7 +62,13 @@ def run_backward_vs_oracle(B, wl, deterministic, ref_fwd=True):
         rep["tensor"] = name
         reps.append(rep)
         if cu is not None:
-            reps.extend(per_segment_report(g, r, cu.tolist(), name, tol, mcos))
+            offs, st = (cu, stq) if name == "dq" else (cuk, stk)
+            reps.extend(per_segment_report(g, r, offs.tolist(), name, tol, mcos,
+                                           None if st is None else st.tolist()))
+            pad = wl.padding_rows("q" if name == "dq" else "k")
+            if pad:
+                zero = bool((g[pad] == 0).all())
+                reps.append(dict(ok=zero, tensor=name, padding_rows=len(pad), all_zero=zero))
     return reps
 
 
@@ -98,6 +108,58 @@ def test_thd_splits_per_segment(B, segs, det):
     assert_all_ok(reps, f"segments {segs}")
 
 
+# Cross-attention varlen: every segment has its own query and key length,
+# including segments with no keys (their dQ is zero) and no queries (their
+# dK, dV are zero), lengths off the 128-row tile and segments longer than one
+# KV tile on one side only.
+ASYM_Q = [100, 0, 37, 250, 5, 129, 300]
+ASYM_K = [300, 64, 0, 129, 200, 128, 17]
+
+
+@pytest.mark.parametrize("det", **DET_MODES)
+@pytest.mark.parametrize("mask,left,right", [(W.MASK_NONE, -1, -1),
+                                             (W.MASK_CAUSAL_BOTTOM_RIGHT, -1, -1),
+                                             (W.MASK_CAUSAL_TOP_LEFT, -1, -1),
+                                             (W.MASK_WINDOW, 40, 8)],
+                         ids=["nomask", "causal_br", "causal_tl", "window"])
+def test_thd_cross_attention_lengths(B, mask, left, right, det):
+    """Separate query and key offsets per packed segment (cu_seqlens_q differs
+    from cu_seqlens_k), compared per segment on each side."""
+    wl = W.thd("thd_cross", ASYM_Q, hq=4, hkv=2, mask=mask, left=left, right=right,
+               seed=101 + mask, seqlens_k=ASYM_K)
+    assert_all_ok(run_backward_vs_oracle(B, wl, det), f"cross-attention varlen mask {mask}")
+
+
+# Padded THD: segment rows start at the padded offsets, lengths come from
+# cu_seqlens; gaps before the first segment, between segments (longer than a
+# tile, and zero) and after the last one, on either side alone or both.
+PAD_Q = [100, 0, 37, 250, 5, 129]
+PAD_K = [300, 64, 0, 129, 200, 128]
+PADDED = [
+    dict(name="both", gaps_q=[3, 0, 17, 1, 140, 2, 9], gaps_k=[0, 5, 0, 131, 7, 1, 30]),
+    dict(name="q_only", gaps_q=[0, 1, 2, 3, 4, 5, 6], gaps_k=None),
+    dict(name="k_only", gaps_q=None, gaps_k=[8, 0, 0, 0, 0, 0, 0]),
+]
+
+
+@pytest.mark.parametrize("det", **DET_MODES)
+@pytest.mark.parametrize("pad", PADDED, ids=lambda c: c["name"])
+@pytest.mark.parametrize("mask", [W.MASK_CAUSAL_BOTTOM_RIGHT, W.MASK_NONE], ids=["causal_br", "nomask"])
+def test_thd_padded_layout(B, pad, mask, det):
+    """cu_seqlens_q_padded / cu_seqlens_k_padded (TransformerEngine PR #446,
+    review of ck_fused_attn_bwd.cpp): per-segment parity on the physical rows
+    and exact zeros in every padding row of dQ, dK, dV."""
+    wl = W.thd("thd_padded", PAD_Q, hq=4, hkv=2, mask=mask, seed=131 + mask, seqlens_k=PAD_K,
+               gaps_q=pad["gaps_q"], gaps_k=pad["gaps_k"])
+    assert_all_ok(run_backward_vs_oracle(B, wl, det), f"padded THD {pad['name']} mask {mask}")
+
+
+def test_thd_padded_fp32(B):
+    wl = W.thd("thd_padded_fp32", [70, 5, 130], hq=2, hkv=1, d_qk=64, d_v=64, dtype=torch.float32,
+               seed=141, gaps_q=[2, 3, 0, 4], gaps_k=[0, 1, 64, 3])
+    assert_all_ok(run_backward_vs_oracle(B, wl, 1), "padded THD fp32")
+
+
 def test_thd_window_and_d192(B):
     wl = W.thd("thd_win", [100, 300, 37], hq=4, hkv=4, d_qk=192, d_v=128, mask=W.MASK_WINDOW,
                left=64, right=0, seed=77)
@@ -105,15 +167,19 @@ def test_thd_window_and_d192(B):
 
 
 def test_forward_helper_matches_oracle(B):
-    for wl in (SMALL[0], SMALL[2], SMALL[3], SMALL[8], SMALL[11], W.thd("t", [100, 80, 76], hq=4, hkv=2, seed=3)):
+    cross = W.thd("t_cross_padded", PAD_Q, hq=4, hkv=2, mask=W.MASK_CAUSAL_BOTTOM_RIGHT, seed=4,
+                  seqlens_k=PAD_K, gaps_q=PADDED[0]["gaps_q"], gaps_k=PADDED[0]["gaps_k"])
+    for wl in (SMALL[0], SMALL[2], SMALL[3], SMALL[8], SMALL[11], W.thd("t", [100, 80, 76], hq=4, hkv=2, seed=3),
+               cross):
         x = wl.inputs()
-        cu = wl.cu_seqlens()
-        kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cu)
+        kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=wl.cu_seqlens(),
+                  cu_seqlens_k=wl.cu_seqlens_k())
+        if wl.gaps_q or wl.gaps_k:
+            kw.update(cu_seqlens_q_padded=wl.cu_seqlens_q_padded(), cu_seqlens_k_padded=wl.cu_seqlens_k_padded())
         o_ref, lse_ref = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, **kw)
-        cu_d = None if cu is None else cu.cuda()
-        o, lse = B.attn_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), scale=wl.scale, mask=wl.mask,
-                                left=wl.left, right=wl.right, cu_seqlens_q=cu_d, cu_seqlens_k=cu_d,
-                                max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+        dkw = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
+        o, lse = B.attn_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), scale=wl.scale,
+                                max_seqlen_q=wl.sq, max_seqlen_k=wl.sk, **dkw)
         torch.cuda.synchronize()
         tol, mcos = tolerances(wl.dtype)
         assert compare(o.cpu(), o_ref, tol, mcos)["ok"], wl.name
@@ -200,6 +266,19 @@ def test_bad_cu_seqlens_reported_by_device(B):
         B.attn_backward(x["q"], x["k"], x["v"], x["do"], x["do"], lse, scale=wl.scale, mask=1,
                         cu_seqlens_q=too_long, cu_seqlens_k=too_long, max_seqlen_q=100, max_seqlen_k=100)
     assert e.value.status == -7
+    # padded starts that overlap a segment, run past the rows, or start before row 0
+    cu = torch.tensor([0, 100, 180, 256], dtype=torch.int32, device="cuda")
+    for starts in ([0, 90, 190, 256], [0, 100, 180, 300], [-4, 100, 180, 256], [0, 100, 181, 256]):
+        st = torch.tensor(starts, dtype=torch.int32, device="cuda")
+        for side in ("cu_seqlens_q_padded", "cu_seqlens_k_padded"):
+            out = tuple(torch.full_like(t, 7.0) for t in (x["q"], x["k"], x["v"]))
+            with pytest.raises(B.AttnError) as e:
+                B.attn_backward(x["q"], x["k"], x["v"], x["do"], x["do"], lse, scale=wl.scale, mask=1,
+                                cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=100, max_seqlen_k=100,
+                                out=out, **{side: st})
+            assert e.value.status == -7, (starts, side)
+            torch.cuda.synchronize()
+            assert all(bool((t == 7.0).all()) for t in out), "outputs touched after a rejected layout"
 
 
 def test_outputs_and_workspace_guard_bands(B):

@@ -143,6 +143,23 @@ def test_finite_differences_varlen():
         assert rel_err(g, fd_grad(x, f)) < 1e-6
 
 
+def test_finite_differences_cross_attention_varlen():
+    """Separate query and key offsets per segment, bottom-right causal: one
+    segment with more keys than queries, one with fewer, one with no keys
+    (its rows see nothing) and one with no queries."""
+    scale = 0.6
+    cu_q = torch.tensor([0, 3, 8, 10, 10], dtype=torch.int32)
+    cu_k = torch.tensor([0, 6, 8, 8, 11], dtype=torch.int32)
+    q, k, v, do = rnd((10, 2, 4), 9), rnd((11, 1, 4), 10), rnd((11, 1, 3), 11), rnd((10, 2, 3), 12)
+    kw = dict(mask=2, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
+    dq, dk, dv = grads(q, k, v, do, scale, **kw)
+    f = lambda: loss(q, k, v, do, scale, **kw)  # noqa: E731
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        assert rel_err(g, fd_grad(x, f)) < 1e-6
+    assert (dq[8:10] == 0).all()          # segment with no keys
+    assert (dk[8:11] == 0).all() and (dv[8:11] == 0).all()   # segment with no queries
+
+
 # ------------------------------------------------------------ closed forms
 
 def test_single_key_closed_form():
@@ -233,6 +250,95 @@ def test_block_diagonal_packed_equals_segments():
         g = R.attn_backward(q[r][None], k[r][None], v[r][None], ob, do[r][None], lseb, 0.35, **kw)
         for packed, alone in zip((dq, dk, dv), g):
             assert torch.allclose(packed[r], alone[0], atol=1e-13)
+
+
+def test_block_diagonal_cross_attention_equals_segments():
+    """Packed segments with their own key lengths equal batch-mode attention of
+    each segment alone (Sq = its query length, Sk = its key length); a segment
+    with no keys has LSE = -inf and O = dQ = 0."""
+    lq, lk = [4, 7, 0, 3, 5], [9, 2, 4, 0, 5]
+    cu_q = torch.tensor(np.cumsum([0] + lq), dtype=torch.int32)
+    cu_k = torch.tensor(np.cumsum([0] + lk), dtype=torch.int32)
+    tq, tk = sum(lq), sum(lk)
+    q, k, v, do = rnd((tq, 4, 8), 25), rnd((tk, 2, 8), 26), rnd((tk, 2, 6), 27), rnd((tq, 4, 6), 28)
+    for kw in (dict(mask=2), dict(mask=1), dict(mask=3, left=2, right=1), dict(mask=0)):
+        seg = dict(cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
+        o, lse = R.attn_forward(q, k, v, 0.35, **seg, **kw)
+        dq, dk, dv = R.attn_backward(q, k, v, o, do, lse, 0.35, **seg, **kw)
+        for b in range(len(lq)):
+            rq = slice(int(cu_q[b]), int(cu_q[b + 1]))
+            rk = slice(int(cu_k[b]), int(cu_k[b + 1]))
+            if lk[b] == 0:
+                assert torch.isinf(lse[:, rq]).all() and (lse[:, rq] < 0).all()
+                assert (o[rq] == 0).all() and (dq[rq] == 0).all()
+                continue
+            if lq[b] == 0:
+                assert (dk[rk] == 0).all() and (dv[rk] == 0).all()
+                continue
+            ob, lseb = R.attn_forward(q[rq][None], k[rk][None], v[rk][None], 0.35, **kw)
+            assert torch.allclose(o[rq], ob[0], atol=1e-13)
+            assert torch.equal(torch.isinf(lse[:, rq]), torch.isinf(lseb[0]))
+            fin = torch.isfinite(lseb[0])
+            assert torch.allclose(lse[:, rq][fin], lseb[0][fin], atol=1e-13)
+            g = R.attn_backward(q[rq][None], k[rk][None], v[rk][None], ob, do[rq][None], lseb, 0.35, **kw)
+            for packed, alone, r in zip((dq, dk, dv), g, (rq, rk, rk)):
+                assert torch.allclose(packed[r], alone[0], atol=1e-13)
+
+
+def test_padded_layout_equals_packed():
+    """A padded THD layout (segment starts from the padded offsets, lengths from
+    cu_seqlens) gives, on the segments' rows, exactly the packed result of the
+    same segments; rows of no segment get zero gradients, O = 0, LSE = -inf.
+    Padding rows hold large garbage so that any leak shows."""
+    lq, lk = [4, 7, 0, 3, 5], [9, 2, 4, 0, 5]
+    gq, gk = [1, 2, 0, 3, 1, 2], [0, 3, 1, 2, 0, 4]
+    cu_q = torch.tensor(np.cumsum([0] + lq), dtype=torch.int32)
+    cu_k = torch.tensor(np.cumsum([0] + lk), dtype=torch.int32)
+
+    def starts(lens, gaps):
+        st, r = [], 0
+        for b, n in enumerate(lens):
+            r += gaps[b]
+            st.append(r)
+            r += n
+        return torch.tensor(st + [r + gaps[-1]], dtype=torch.int32)
+
+    st_q, st_k = starts(lq, gq), starts(lk, gk)
+    tq, tk = int(st_q[-1]), int(st_k[-1])
+    q, k, v, do = rnd((sum(lq), 4, 8), 41), rnd((sum(lk), 2, 8), 42), rnd((sum(lk), 2, 6), 43), rnd((sum(lq), 4, 6), 44)
+
+    def spread(x, cu, st, total, seed):
+        out = 1e3 * rnd((total,) + tuple(x.shape[1:]), seed)
+        for b in range(len(cu) - 1):
+            n = int(cu[b + 1] - cu[b])
+            out[int(st[b]):int(st[b]) + n] = x[int(cu[b]):int(cu[b + 1])]
+        return out
+
+    def gather(x, cu, st):
+        return torch.cat([x[int(st[b]):int(st[b]) + int(cu[b + 1] - cu[b])] for b in range(len(cu) - 1)])
+
+    qp, dop = spread(q, cu_q, st_q, tq, 45), spread(do, cu_q, st_q, tq, 46)
+    kp, vp = spread(k, cu_k, st_k, tk, 47), spread(v, cu_k, st_k, tk, 48)
+    pad_q = torch.ones(tq, dtype=torch.bool)
+    pad_q[torch.cat([torch.arange(int(st_q[b]), int(st_q[b]) + lq[b]) for b in range(5)])] = False
+    pad_k = torch.ones(tk, dtype=torch.bool)
+    pad_k[torch.cat([torch.arange(int(st_k[b]), int(st_k[b]) + lk[b]) for b in range(5)])] = False
+    for kw in (dict(mask=2), dict(mask=3, left=2, right=1), dict(mask=0)):
+        packed = dict(cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, **kw)
+        padded = dict(cu_seqlens_q_padded=st_q, cu_seqlens_k_padded=st_k, **packed)
+        o, lse = R.attn_forward(q, k, v, 0.4, **packed)
+        grads_packed = R.attn_backward(q, k, v, o, do, lse, 0.4, **packed)
+        op, lsep = R.attn_forward(qp, kp, vp, 0.4, **padded)
+        assert torch.equal(gather(op, cu_q, st_q), o)
+        assert torch.equal(gather(lsep.T, cu_q, st_q), lse.T)
+        assert (op[pad_q] == 0).all() and torch.isneginf(lsep[:, pad_q]).all()
+        opg = spread(o, cu_q, st_q, tq, 49)          # garbage O and LSE in padding rows
+        lsepg = spread(lse.T, cu_q, st_q, tq, 50).T
+        dq, dk, dv = R.attn_backward(qp, kp, vp, opg, dop, lsepg, 0.4, **padded)
+        assert torch.equal(gather(dq, cu_q, st_q), grads_packed[0])
+        assert torch.equal(gather(dk, cu_k, st_k), grads_packed[1])
+        assert torch.equal(gather(dv, cu_k, st_k), grads_packed[2])
+        assert (dq[pad_q] == 0).all() and (dk[pad_k] == 0).all() and (dv[pad_k] == 0).all()
 
 
 def test_gqa_equals_summed_mha():

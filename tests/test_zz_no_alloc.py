@@ -26,8 +26,10 @@ def _case(B, wl, det):
     x = {k: v.cuda() for k, v in wl.inputs().items()}
     cu = wl.cu_seqlens()
     cu_d = None if cu is None else cu.cuda()
+    cuk = wl.cu_seqlens_k()
+    cuk_d = None if cuk is None else cuk.cuda()
     kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
-              cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+              cu_seqlens_k=cuk_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
     o, lse = B.attn_forward(x["q"], x["k"], x["v"], **kw)
     ref = B.attn_backward(x["q"], x["k"], x["v"], o, x["do"], lse, deterministic=det, **kw)
     outs = (torch.full_like(x["q"], float("nan")), torch.full_like(x["k"], float("nan")),
