@@ -118,24 +118,29 @@ void launch_schedule(const Problem& P, cudaStream_t st) {
 
 // --------------------------------------------------------------- preprocess
 // D and -LSE*log2(e) of every (packed token, query head) row.  16-bit
-// inputs: half a warp per row, 16-byte loads of O and dO.  fp32 inputs: one
-// warp per row.  In atomic mode the single dq_acc slice is zeroed as well.
+// inputs: half a warp per group of four rows, 16-byte loads of O and dO, one
+// resident wave of blocks.  fp32 inputs: one warp per row.  In atomic and
+// ordered-fold modes the single dq_acc slice is zeroed as well.
 
-__device__ __forceinline__ void write_row_stats(const Problem& P, long long r, float acc) {
-  const float LOG2E = 1.4426950408889634f;
+// Index in the LSE layout of row r = token * Hq + head of O / dO.
+__device__ __forceinline__ long long lse_index(const Problem& P, long long r) {
   const long long tok = r / P.hq;
   const int h = (int)(r - tok * P.hq);
-  long long li;
-  if (P.group) {
-    li = (long long)h * P.tq + tok;
-  } else {
-    const long long b = tok / P.sq, q = tok - b * P.sq;
-    li = (b * P.hq + h) * P.sq + q;
-  }
-  if (!ATTN_INDEX_OK(P, li >= 0 && li < P.n_lse, 8)) return;
-  const float l = P.lse[li];
+  if (P.group) return (long long)h * P.tq + tok;
+  const long long b = tok / P.sq, q = tok - b * P.sq;
+  return (b * P.hq + h) * P.sq + q;
+}
+
+__device__ __forceinline__ void store_row_stats(const Problem& P, long long li, float l, float acc) {
+  const float LOG2E = 1.4426950408889634f;
   P.dvec[li] = acc;
   P.nlse2[li] = (l == -INFINITY) ? -INFINITY : -l * LOG2E;
+}
+
+__device__ __forceinline__ void write_row_stats(const Problem& P, long long r, float acc) {
+  const long long li = lse_index(P, r);
+  if (!ATTN_INDEX_OK(P, li >= 0 && li < P.n_lse, 8)) return;
+  store_row_stats(P, li, P.lse[li], acc);
 }
 
 __device__ __forceinline__ float dot8(uint4 a, uint4 b, __nv_bfloat16*) {
@@ -178,27 +183,59 @@ __device__ void zero_padding_rows(const int* st, const int* cu, int nseg, int to
   }
 }
 
+constexpr int PRE_BLOCKS_PER_SM = 3;
+
 template <typename T>
-__global__ void __launch_bounds__(256) preprocess_kernel(Problem P, long long ntok) {
+__global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Problem P, long long ntok) {
   const int lane = threadIdx.x & 31;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long nrows = ntok * P.hq;
   if constexpr (sizeof(T) == 2) {
-    // half warp per row; d_v is a multiple of 8 for the 16-bit kernels
+    // A half warp takes RPH consecutive rows at a time (16-byte loads; d_v is
+    // a multiple of 8 and at most 128 for the 16-bit kernels, so one load per
+    // lane and row).  All loads of a group, LSE included, are issued before
+    // the first reduction so that each half warp keeps RPH rows in flight.
+    constexpr int RPH = 4;
     const int sub = lane & 15;
     const long long hw = tid >> 4, nhw = nthreads >> 4;
     const uint4* O = static_cast<const uint4*>(P.o);
     const uint4* dO = static_cast<const uint4*>(P.dout);
     const int nv = P.dv / 8;
-    for (long long r0 = hw - (hw & 1); r0 < nrows; r0 += nhw) {
-      const long long r = r0 + (hw & 1);
-      float acc = 0.f;
-      if (r < nrows)
-        for (int v = sub; v < nv; v += 16) acc += dot8(O[r * nv + v], dO[r * nv + v], (T*)nullptr);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    // the trip count is warp-uniform (the shuffles below take the full mask)
+    for (long long w0 = (hw >> 1) * 2 * RPH; w0 < nrows; w0 += nhw * RPH) {
+      const long long r0 = w0 + (hw & 1) * RPH;
+      uint4 a[RPH], b[RPH];
+      long long li[RPH];
+      float l[RPH];
+      // (token, head) and, in batch mode, (batch, query) of the first row by
+      // division, of the next rows by stepping
+      long long tok = r0 / P.hq;
+      int h = (int)(r0 - tok * P.hq);
+      long long bq = P.group ? 0 : tok / P.sq;
+      long long q = tok - bq * P.sq;
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (sub == 0 && r < nrows) write_row_stats(P, r, acc);
+      for (int i = 0; i < RPH; ++i) {
+        const long long r = r0 + i;
+        const bool ok = r < nrows && sub < nv;
+        a[i] = ok ? __ldcs(O + r * nv + sub) : z;
+        b[i] = ok ? __ldcs(dO + r * nv + sub) : z;
+        li[i] = P.group ? (long long)h * P.tq + tok : (bq * P.hq + h) * P.sq + q;
+        l[i] = (sub == 0 && r < nrows && ATTN_INDEX_OK(P, li[i] >= 0 && li[i] < P.n_lse, 8)) ? P.lse[li[i]] : 0.f;
+        if (++h == P.hq) {
+          h = 0;
+          ++tok;
+          if (++q == P.sq) { q = 0; ++bq; }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < RPH; ++i) {
+        float acc = dot8(a[i], b[i], (T*)nullptr);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (sub == 0 && r0 + i < nrows && li[i] >= 0 && li[i] < P.n_lse) store_row_stats(P, li[i], l[i], acc);
+      }
     }
   } else {
     const long long warp = tid >> 5, nwarps = nthreads >> 5;
@@ -249,7 +286,7 @@ static int num_sms() {
 
 void launch_preprocess(const Problem& P, cudaStream_t st) {
   const long long ntok = P.group ? (long long)P.tq : (long long)P.nseg * P.sq;
-  const int grid = num_sms() * 8;
+  const int grid = num_sms() * PRE_BLOCKS_PER_SM;   // one resident wave
   switch (P.dtype) {
     case ATTN_BF16: preprocess_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(P, ntok); break;
     case ATTN_FP16: preprocess_kernel<__half><<<grid, 256, 0, st>>>(P, ntok); break;
