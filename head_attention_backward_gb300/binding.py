@@ -28,6 +28,7 @@ STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED_HE
 _DTYPES = {torch.bfloat16: ATTN_BF16, torch.float16: ATTN_FP16, torch.float32: ATTN_FP32}
 
 _i32, _vp, _f32 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+_i64x3 = ctypes.c_int64 * 3
 
 
 class AttnBwdParams(ctypes.Structure):
@@ -37,7 +38,9 @@ class AttnBwdParams(ctypes.Structure):
                 ("cu_seqlens_q_padded", _vp), ("cu_seqlens_k_padded", _vp), ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
                 ("softmax_scale", _f32), ("deterministic", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("dout", _vp), ("lse", _vp),
-                ("dq", _vp), ("dk", _vp), ("dv", _vp)]
+                ("dq", _vp), ("dk", _vp), ("dv", _vp),
+                ("stride_q", _i64x3), ("stride_k", _i64x3), ("stride_v", _i64x3), ("stride_o", _i64x3),
+                ("stride_dout", _i64x3), ("stride_dq", _i64x3), ("stride_dk", _i64x3), ("stride_dv", _i64x3)]
 
 
 class AttnFwdParams(ctypes.Structure):
@@ -45,7 +48,8 @@ class AttnFwdParams(ctypes.Structure):
                 ("seqlen_q", _i32), ("seqlen_k", _i32), ("total_q", _i32), ("total_k", _i32),
                 ("d_qk", _i32), ("d_v", _i32), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
                 ("cu_seqlens_q_padded", _vp), ("cu_seqlens_k_padded", _vp), ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
-                ("softmax_scale", _f32), ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp)]
+                ("softmax_scale", _f32), ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp),
+                ("stride_q", _i64x3), ("stride_k", _i64x3), ("stride_v", _i64x3), ("stride_o", _i64x3)]
 
 
 EXPORTS = ["attn_bwd_workspace_size", "attn_bwd", "attn_bwd_timed", "attn_bwd_read_status",
@@ -158,6 +162,21 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _strides(t, group: bool):
+    """{batch, row, head} element strides of a [B,S,H,D] or [T,H,D] tensor
+    whose last dimension is contiguous."""
+    if t.stride(-1) != 1:
+        raise ValueError("the head dimension must be contiguous (stride 1)")
+    if group:
+        return (0, t.stride(0), t.stride(1))
+    return (t.stride(0), t.stride(1), t.stride(2))
+
+
+def _set_strides(p, group: bool, **tensors):
+    for name, t in tensors.items():
+        getattr(p, "stride_" + name)[:] = _strides(t, group)
+
+
 def _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k):
     if cu_seqlens_q is None:
         b, sq, hq, dqk = q.shape
@@ -184,6 +203,7 @@ def bwd_params(q, k, v, o, do, lse, dq, dk, dv, *, scale, mask=MASK_NONE, left=-
     p.deterministic = int(deterministic)   # False/True or an attn_det_t value (0, 1, 2)
     p.q, p.k, p.v, p.o, p.dout, p.lse = (_ptr(t) for t in (q, k, v, o, do, lse))
     p.dq, p.dk, p.dv = _ptr(dq), _ptr(dk), _ptr(dv)
+    _set_strides(p, cu_seqlens_q is not None, q=q, k=k, v=v, o=o, dout=do, dq=dq, dk=dk, dv=dv)
     return p
 
 
@@ -199,6 +219,7 @@ def fwd_params(q, k, v, o, lse, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_
     p.mask, p.window_left, p.window_right = mask, left, right
     p.softmax_scale = scale
     p.q, p.k, p.v, p.o, p.lse = (_ptr(t) for t in (q, k, v, o, lse))
+    _set_strides(p, cu_seqlens_q is not None, q=q, k=k, v=v, o=o)
     return p
 
 
@@ -213,17 +234,27 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
+def _empty_in_order_of(t, last: int):
+    """An uninitialised tensor shaped like t but with last dimension `last`,
+    its other dimensions laid out in t's memory order (so BHSD or SBHD inputs
+    give a BHSD or SBHD output and the strides fold the same way)."""
+    n = t.dim() - 1
+    order = sorted(range(n), key=lambda i: -t.stride(i))
+    buf = torch.empty([t.shape[i] for i in order] + [last], dtype=t.dtype, device=t.device)
+    return buf.permute([order.index(i) for i in range(n)] + [n])
+
+
 def attn_forward(q, k, v, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlens_q=None,
                  cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, cu_seqlens_q_padded=None,
                  cu_seqlens_k_padded=None, stream=None):
     """O and LSE from the library's forward helper (outputs allocated here; the
     padding rows of a padded layout, which the helper leaves alone, hold O = 0
     and LSE = -inf)."""
+    o = _empty_in_order_of(q, v.shape[-1])
     if cu_seqlens_q is None:
-        o = torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
         lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=q.device)
     else:
-        o = torch.zeros(q.shape[:2] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+        o.zero_()
         lse = torch.full((q.shape[1], q.shape[0]), -math.inf, dtype=torch.float32, device=q.device)
     p = fwd_params(q, k, v, o, lse, scale=scale, mask=mask, left=left, right=right,
                    cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,

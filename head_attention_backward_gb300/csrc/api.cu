@@ -23,6 +23,105 @@ static bool simt_headdims(int dqk, int dv) {
   return dqk >= 4 && dqk <= 64 && dv >= 1 && dv <= 64 && dqk % 4 == 0;
 }
 
+// ------------------------------------------------------------------ strides
+// The kernels address every tensor as [rows, heads, dim] with a row and a
+// head stride.  A batch-mode tensor fits that view when its batch entries
+// follow each other along rows (batch stride = S x row stride: BSHD, packed
+// QKV) -- rows are then b * S + s -- or along heads (batch stride = H x head
+// stride: BHSD, SBHD) -- the problem is then run as one batch entry with
+// B * Hq query and B * Hkv kv heads, which keeps the GQA grouping
+// (h' / G = b * Hkv + h / G) and the [B, Hq, Sq] LSE layout.  All tensors of
+// a call must fit the same way; any other layout is rejected.
+
+struct Stride3 {
+  long long b, r, h;
+};
+
+struct TensorDesc {
+  const int64_t* in;   // the caller's {batch, row, head} strides
+  int seqlen, heads, dim;
+};
+
+// The caller's strides, or the contiguous layout when all three are zero.
+static bool resolve3(const TensorDesc& t, bool group, int batch, bool vec16, Stride3* x) {
+  if (t.in[0] == 0 && t.in[1] == 0 && t.in[2] == 0) {
+    x->h = t.dim;
+    x->r = (long long)t.heads * t.dim;
+    x->b = (long long)t.seqlen * x->r;
+    return true;
+  }
+  x->b = t.in[0];
+  x->r = t.in[1];
+  x->h = t.in[2];
+  const bool need_b = !group && batch > 1;
+  if (x->r <= 0 || x->h <= 0 || (need_b && x->b <= 0)) return false;
+  if (!need_b) x->b = (long long)t.seqlen * x->r;   // never used
+  const long long lim = 1LL << 36;                    // tensor-map strides stay below 2^40 bytes
+  if (x->r >= lim || x->h >= lim || x->b >= lim) return false;
+  if (vec16 && (x->r % 8 || x->h % 8 || x->b % 8)) return false;
+  return true;
+}
+
+// Resolves the n tensors' strides into out[] and returns 0 (rows layout),
+// 1 (heads layout: fold the batch into the heads) or -1 (rejected).  A
+// tensor with one row per batch entry (or one head) never uses its row (or
+// head) stride, so the batch stride stands in for it.
+static int fold_strides(const TensorDesc* t, int n, bool group, int batch, bool vec16, Strides* out) {
+  Stride3 x[8];
+  bool rows = true, heads = true;
+  for (int i = 0; i < n; ++i) {
+    if (!resolve3(t[i], group, batch, vec16, &x[i])) return -1;
+    rows &= t[i].seqlen == 1 || x[i].b == (long long)t[i].seqlen * x[i].r;
+    heads &= t[i].heads == 1 || x[i].b == (long long)t[i].heads * x[i].h;
+  }
+  const int kind = (group || batch == 1 || rows) ? 0 : heads ? 1 : -1;
+  for (int i = 0; i < n && kind >= 0; ++i) {
+    const bool use_b = !group && batch > 1;
+    out[i].r = (kind == 0 && use_b && t[i].seqlen == 1) ? x[i].b : x[i].r;
+    out[i].h = (kind == 1 && t[i].heads == 1) ? x[i].b : x[i].h;
+  }
+  return kind;
+}
+
+// The problem the kernels run: batch folded into the heads when the layout
+// asks for it, and each tensor's {row, head} strides (q, k, v, o, dout, dq,
+// dk, dv).  Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
+static int effective_bwd(const attn_bwd_params& p, attn_bwd_params* e, Strides s[8]) {
+  const bool group = p.cu_seqlens_q != nullptr;
+  const TensorDesc t[8] = {{p.stride_q, p.seqlen_q, p.nhead_q, p.d_qk},   {p.stride_k, p.seqlen_k, p.nhead_kv, p.d_qk},
+                           {p.stride_v, p.seqlen_k, p.nhead_kv, p.d_v},   {p.stride_o, p.seqlen_q, p.nhead_q, p.d_v},
+                           {p.stride_dout, p.seqlen_q, p.nhead_q, p.d_v}, {p.stride_dq, p.seqlen_q, p.nhead_q, p.d_qk},
+                           {p.stride_dk, p.seqlen_k, p.nhead_kv, p.d_qk}, {p.stride_dv, p.seqlen_k, p.nhead_kv, p.d_v}};
+  const int kind = fold_strides(t, 8, group, p.batch, p.dtype != ATTN_FP32, s);
+  if (kind < 0) return ATTN_ERR_INVALID_ARG;
+  *e = p;
+  if (kind == 1) {
+    if ((long long)p.batch * p.nhead_q > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+    e->nhead_q = p.batch * p.nhead_q;
+    e->nhead_kv = p.batch * p.nhead_kv;
+    e->batch = 1;
+  }
+  return ATTN_OK;
+}
+
+static int effective_fwd(const attn_fwd_params& p, attn_fwd_params* e, FwdLayout* L) {
+  const bool group = p.cu_seqlens_q != nullptr;
+  const TensorDesc t[4] = {{p.stride_q, p.seqlen_q, p.nhead_q, p.d_qk}, {p.stride_k, p.seqlen_k, p.nhead_kv, p.d_qk},
+                           {p.stride_v, p.seqlen_k, p.nhead_kv, p.d_v}, {p.stride_o, p.seqlen_q, p.nhead_q, p.d_v}};
+  Strides s[4];
+  const int kind = fold_strides(t, 4, group, p.batch, p.dtype != ATTN_FP32, s);
+  if (kind < 0) return ATTN_ERR_INVALID_ARG;
+  L->q = s[0]; L->k = s[1]; L->v = s[2]; L->o = s[3];
+  *e = p;
+  if (kind == 1) {
+    if ((long long)p.batch * p.nhead_q > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+    e->nhead_q = p.batch * p.nhead_q;
+    e->nhead_kv = p.batch * p.nhead_kv;
+    e->batch = 1;
+  }
+  return ATTN_OK;
+}
+
 template <typename Prm>
 static int validate_common(const Prm* p) {
   if (!p) return ATTN_ERR_INVALID_ARG;
@@ -72,7 +171,8 @@ static int validate_fwd(const attn_fwd_params* p) {
   return ATTN_OK;
 }
 
-static Problem make_problem(const attn_bwd_params& p, void* ws) {
+// p: the effective problem (effective_bwd), s: its strides.
+static Problem make_problem(const attn_bwd_params& p, const Strides s[8], void* ws) {
   const WsLayout L = ws_layout(p);
   Problem P{};
   P.dtype = p.dtype;
@@ -102,6 +202,8 @@ static Problem make_problem(const attn_bwd_params& p, void* ws) {
   P.nsplits = L.nsplits;
   P.q = p.q; P.k = p.k; P.v = p.v; P.o = p.o; P.dout = p.dout; P.lse = p.lse;
   P.dq = p.dq; P.dk = p.dk; P.dv_out = p.dv;
+  P.sq_ = s[0]; P.sk_ = s[1]; P.sv_ = s[2]; P.so_ = s[3];
+  P.sdo_ = s[4]; P.sdq_ = s[5]; P.sdk_ = s[6]; P.sdv_ = s[7];
   char* w = static_cast<char*>(ws);
   P.hdr = reinterpret_cast<int*>(w + L.off_hdr);
   P.nlse2 = reinterpret_cast<float*>(w + L.off_lse2);
@@ -137,11 +239,14 @@ static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t
                cudaEvent_t* ev /* 4 events or null */) {
   int st = validate_bwd(p);
   if (st != ATTN_OK) return st;
+  attn_bwd_params e;
+  Strides sx[8];
+  if ((st = effective_bwd(*p, &e, sx)) != ATTN_OK) return st;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(*p);
+  const WsLayout L = ws_layout(e);
   if (ws_bytes < L.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
-  if (log_enabled()) log_config(*p, L);
-  const Problem P = make_problem(*p, ws);
+  if (log_enabled()) log_config(e, L);
+  const Problem P = make_problem(e, sx, ws);
   if (ev) cudaEventRecord(ev[0], s);
   launch_schedule(P, s);
   launch_preprocess(P, s);
@@ -168,7 +273,11 @@ extern "C" int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes) 
   const int st = validate_common(p);
   if (st != ATTN_OK) return st;
   if (p->deterministic < ATTN_DET_ATOMIC || p->deterministic > ATTN_DET_SPLIT) return ATTN_ERR_INVALID_ARG;
-  *bytes = ws_layout(*p).total;
+  attn_bwd_params e;
+  Strides sx[8];
+  const int s2 = effective_bwd(*p, &e, sx);
+  if (s2 != ATTN_OK) return s2;
+  *bytes = ws_layout(e).total;
   return ATTN_OK;
 }
 
@@ -209,7 +318,11 @@ extern "C" int attn_bwd_read_status(const void* workspace, cudaStream_t stream, 
 extern "C" int attn_fwd(const attn_fwd_params* p, cudaStream_t stream) {
   const int st = validate_fwd(p);
   if (st != ATTN_OK) return st;
-  launch_fwd(*p, stream);
+  attn_fwd_params e;
+  FwdLayout L;
+  const int s2 = effective_fwd(*p, &e, &L);
+  if (s2 != ATTN_OK) return s2;
+  launch_fwd(e, L, stream);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -172,14 +172,22 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, __half*) {
 // Padded group layout: gradient rows that belong to no segment are zero.
 // Gap g in [0, nseg] holds the rows from the end of segment g-1 (row 0 for
 // g = 0) up to the start of segment g (the row total for g = nseg); the
-// schedule kernel has checked that the gaps are well formed.  Row sizes are
-// whole 4-byte words for every supported dtype and head dim.
-__device__ void zero_padding_rows(const int* st, const int* cu, int nseg, int total,
-                                  int row_words, uint32_t* out) {
+// schedule kernel has checked that the gaps are well formed.  A (row, head)
+// vector of `dim` elements is a whole number of 4-byte words at a word
+// boundary for every supported dtype, head dim and stride.
+__device__ void zero_padding_rows(const int* st, const int* cu, int nseg, int total, int heads, int dim,
+                                  const Strides& x, int esize, void* out) {
+  const int wpv = dim * esize / 4;   // words per (row, head)
+  uint32_t* o = static_cast<uint32_t*>(out);
   for (int g = blockIdx.x; g <= nseg; g += gridDim.x) {
     const long long a = g == 0 ? 0 : (long long)st[g - 1] + (cu[g] - cu[g - 1]);
     const long long e = g == nseg ? total : st[g];
-    for (long long i = a * row_words + threadIdx.x; i < e * row_words; i += blockDim.x) out[i] = 0u;
+    const long long n = (e - a) * heads * wpv;
+    for (long long i = threadIdx.x; i < n; i += blockDim.x) {
+      const long long rr = i / ((long long)heads * wpv);
+      const int rem = (int)(i - rr * heads * wpv), hh = rem / wpv, wd = rem - hh * wpv;
+      o[elem_off(x, a + rr, hh) * esize / 4 + wd] = 0u;
+    }
   }
 }
 
@@ -192,9 +200,9 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long nrows = ntok * P.hq;
   if constexpr (sizeof(T) == 2) {
-    // A half warp takes RPH consecutive rows at a time (16-byte loads; d_v is
-    // a multiple of 8 and at most 128 for the 16-bit kernels, so one load per
-    // lane and row).  All loads of a group, LSE included, are issued before
+    // A half warp takes RPH consecutive rows at a time (16-byte loads; d_v and
+    // every stride are multiples of 8 and d_v is at most 128 for the 16-bit
+    // kernels, so one load per lane and row).  All loads of a group, LSE included, are issued before
     // the first reduction so that each half warp keeps RPH rows in flight.
     constexpr int RPH = 4;
     const int sub = lane & 15;
@@ -215,18 +223,25 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
       int h = (int)(r0 - tok * P.hq);
       long long bq = P.group ? 0 : tok / P.sq;
       long long q = tok - bq * P.sq;
+      // element offsets of the row in O and dO (multiples of 8, non-negative)
+      long long oo = elem_off(P.so_, tok, h), od = elem_off(P.sdo_, tok, h);
 #pragma unroll
       for (int i = 0; i < RPH; ++i) {
         const long long r = r0 + i;
         const bool ok = r < nrows && sub < nv;
-        a[i] = ok ? __ldcs(O + r * nv + sub) : z;
-        b[i] = ok ? __ldcs(dO + r * nv + sub) : z;
+        a[i] = ok ? __ldcs(O + (oo >> 3) + sub) : z;
+        b[i] = ok ? __ldcs(dO + (od >> 3) + sub) : z;
         li[i] = P.group ? (long long)h * P.tq + tok : (bq * P.hq + h) * P.sq + q;
         l[i] = (sub == 0 && r < nrows && ATTN_INDEX_OK(P, li[i] >= 0 && li[i] < P.n_lse, 8)) ? P.lse[li[i]] : 0.f;
         if (++h == P.hq) {
           h = 0;
           ++tok;
           if (++q == P.sq) { q = 0; ++bq; }
+          oo = elem_off(P.so_, tok, 0);
+          od = elem_off(P.sdo_, tok, 0);
+        } else {
+          oo += P.so_.h;
+          od += P.sdo_.h;
         }
       }
 #pragma unroll
@@ -242,9 +257,12 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
     const T* O = static_cast<const T*>(P.o);
     const T* dO = static_cast<const T*>(P.dout);
     for (long long r = warp; r < nrows; r += nwarps) {
+      const long long tok = r / P.hq;
+      const int h = (int)(r - tok * P.hq);
+      const T* o = O + elem_off(P.so_, tok, h);
+      const T* d = dO + elem_off(P.sdo_, tok, h);
       float acc = 0.f;
-      for (int c = lane; c < P.dv; c += 32)
-        acc += TypeOps<T>::to_f(O[r * P.dv + c]) * TypeOps<T>::to_f(dO[r * P.dv + c]);
+      for (int c = lane; c < P.dv; c += 32) acc += TypeOps<T>::to_f(o[c]) * TypeOps<T>::to_f(d[c]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (lane == 0) write_row_stats(P, r, acc);
@@ -252,9 +270,9 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
   }
   if (P.padded && *(volatile const int*)(P.hdr + HDR_STATUS) == 0) {
     const int w = (int)sizeof(T);
-    zero_padding_rows(P.st_q, P.cu_q, P.nseg, P.tq, P.hq * P.dqk * w / 4, static_cast<uint32_t*>(P.dq));
-    zero_padding_rows(P.st_k, P.cu_k, P.nseg, P.tk, P.hkv * P.dqk * w / 4, static_cast<uint32_t*>(P.dk));
-    zero_padding_rows(P.st_k, P.cu_k, P.nseg, P.tk, P.hkv * P.dv * w / 4, static_cast<uint32_t*>(P.dv_out));
+    zero_padding_rows(P.st_q, P.cu_q, P.nseg, P.tq, P.hq, P.dqk, P.sdq_, w, P.dq);
+    zero_padding_rows(P.st_k, P.cu_k, P.nseg, P.tk, P.hkv, P.dqk, P.sdk_, w, P.dk);
+    zero_padding_rows(P.st_k, P.cu_k, P.nseg, P.tk, P.hkv, P.dv, P.sdv_, w, P.dv_out);
   }
   if (!P.det || P.fold) {   // the single slice that partials are added into starts at zero
     float4* acc4 = reinterpret_cast<float4*>(P.dq_acc);
@@ -367,13 +385,14 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
   } else if (s.lk > 0) {   // atomic and ordered fold: the single, pre-zeroed slice
     add_tiles(dq_tile(P, 0, h, t), nullptr);
   }
+  T* dQt = dQ + elem_off(P.sdq_, s.q0 + qt * BM, h);   // row 0 of the tile
 #pragma unroll
   for (int i = 0; i < NACC; ++i) {
     const int v = threadIdx.x + i * RC_THREADS;
     const int c = (4 * v) / dqk, e = (4 * v) - c * dqk;   // query row, first d
     if (v < nv4 && c < nvalid &&
         ATTN_INDEX_OK(P, s.q0 + qt * BM + c >= 0 && s.q0 + qt * BM + c < rows_q(P) && h < P.hq, 9)) {
-      T* row = dQ + ((long long)(s.q0 + qt * BM + c) * P.hq + h) * dqk + e;
+      T* row = dQt + c * P.sdq_.r + e;
       T o4[4] = {TypeOps<T>::from_f(acc[i].x * P.scale), TypeOps<T>::from_f(acc[i].y * P.scale),
                  TypeOps<T>::from_f(acc[i].z * P.scale), TypeOps<T>::from_f(acc[i].w * P.scale)};
       if (sizeof(T) == 2) {

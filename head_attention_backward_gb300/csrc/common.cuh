@@ -29,6 +29,13 @@ enum HeaderWord : int {
   HDR_WORDS = 128     // words 16+: optional 64-bit wait counters of instrumented builds
 };
 
+// Element strides of a tensor seen as [rows, heads, dim] (batch entries
+// folded into rows or into heads by the host); the last dimension is
+// contiguous.
+struct Strides {
+  long long r, h;
+};
+
 struct Problem {
   // shapes
   int dtype;
@@ -59,6 +66,7 @@ struct Problem {
   void* dq;
   void* dk;
   void* dv_out;
+  Strides sq_, sk_, sv_, so_, sdo_, sdq_, sdk_, sdv_;
   // workspace
   int* hdr;
   float* nlse2;      // -LSE * log2(e), -inf for rows without a visible key
@@ -132,9 +140,14 @@ inline WsLayout ws_layout(const attn_bwd_params& p) {
 // ------------------------------------------------------------------ segments
 
 struct Seg {
-  int q0, lq;   // first physical row and length of the query segment
+  int q0, lq;   // first row and length of the query segment
   int k0, lk;   // same for keys
 };
+
+// Element offset of (row, head h) of a tensor with strides x.
+__host__ __device__ __forceinline__ long long elem_off(const Strides& x, long long row, int h) {
+  return row * x.r + h * x.h;
+}
 
 __device__ __forceinline__ Seg segment(const Problem& P, int b) {
   Seg s;
@@ -304,7 +317,7 @@ static __device__ __noinline__ bool debug_index_fail(int* hdr, int id) {
 #define ATTN_INDEX_OK(P, cond, id) true
 #endif
 
-// Rows of the q / k tensors (packed tokens in group mode).
+// Rows of the q / k tensors (all batch entries, or the packed tokens).
 __host__ __device__ inline long long rows_q(const Problem& P) { return P.group ? (long long)P.tq : (long long)P.nseg * P.sq; }
 __host__ __device__ inline long long rows_k(const Problem& P) { return P.group ? (long long)P.tk : (long long)P.nseg * P.sk; }
 
@@ -322,6 +335,9 @@ void launch_reduce_convert(const Problem& P, cudaStream_t st);
 void launch_bwd_simt(const Problem& P, cudaStream_t st);
 int launch_bwd_tc(const Problem& P, cudaStream_t st);   // returns ATTN_* status
 int selftest_waits(void* scratch, size_t bytes, cudaStream_t st, int status[3]);
-void launch_fwd(const attn_fwd_params& p, cudaStream_t st);
+struct FwdLayout {
+  Strides q, k, v, o;
+};
+void launch_fwd(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st);
 
 }  // namespace attn

@@ -17,7 +17,7 @@ constexpr int FWD_BK = 64;   // keys per tile
 constexpr int FWD_THREADS = 256;
 
 template <typename T>
-__global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, int group) {
+__global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, FwdLayout L, int group) {
   extern __shared__ float smem[];
   const int dqk = p.d_qk, dv = p.d_v;
   const int sq_stride = dqk + 1, sk_stride = dqk + 1, sv_stride = dv;
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, int
   for (int i = tid; i < FWD_BQ * dqk; i += FWD_THREADS) {
     const int r = i / dqk, c = i % dqk;
     float x = 0.f;
-    if (qs + r < lq) x = TypeOps<T>::to_f(Q[((long long)(q0 + qs + r) * p.nhead_q + h) * dqk + c]);
+    if (qs + r < lq) x = TypeOps<T>::to_f(Q[elem_off(L.q, q0 + qs + r, h) + c]);
     sQ[r * sq_stride + c] = x;
   }
   const MaskArgs m = mask_args(p.mask, p.window_left, p.window_right, lq, lk);
@@ -70,12 +70,12 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, int
     for (int i = tid; i < FWD_BK * dqk; i += FWD_THREADS) {
       const int r = i / dqk, c = i % dqk;
       const long long kk = kb + r;
-      sK[r * sk_stride + c] = kk < lk ? TypeOps<T>::to_f(K[((k0 + kk) * p.nhead_kv + hk) * dqk + c]) : 0.f;
+      sK[r * sk_stride + c] = kk < lk ? TypeOps<T>::to_f(K[elem_off(L.k, k0 + kk, hk) + c]) : 0.f;
     }
     for (int i = tid; i < FWD_BK * dv; i += FWD_THREADS) {
       const int r = i / dv, c = i % dv;
       const long long kk = kb + r;
-      sV[r * sv_stride + c] = kk < lk ? TypeOps<T>::to_f(V[((k0 + kk) * p.nhead_kv + hk) * dv + c]) : 0.f;
+      sV[r * sv_stride + c] = kk < lk ? TypeOps<T>::to_f(V[elem_off(L.v, k0 + kk, hk) + c]) : 0.f;
     }
     __syncthreads();
     float s[FWD_BK / 4];
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, int
   const int qi = qs + row;
   if (qi < lq) {
     const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-    const long long orow = ((long long)(q0 + qi) * p.nhead_q + h) * dv;
+    const long long orow = elem_off(L.o, q0 + qi, h);
     for (int i = 0; i < ncol; ++i) {
       const int c = sub + 4 * i;
       if (c < dv) O[orow + c] = TypeOps<T>::from_f(acc[i] * inv);
@@ -143,22 +143,22 @@ size_t fwd_smem_bytes(int dqk, int dv) {
                           (size_t)FWD_BK * dv + (size_t)FWD_BQ * (FWD_BK + 1));
 }
 
-void launch_fwd(const attn_fwd_params& p, cudaStream_t st) {
+void launch_fwd(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
   const int group = p.cu_seqlens_q != nullptr;
   dim3 grid(cdiv(p.seqlen_q, FWD_BQ), p.nhead_q, p.batch);
   const size_t smem = fwd_smem_bytes(p.d_qk, p.d_v);
   switch (p.dtype) {
     case ATTN_BF16:
       cudaFuncSetAttribute(fwd_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      fwd_kernel<__nv_bfloat16><<<grid, FWD_THREADS, smem, st>>>(p, group);
+      fwd_kernel<__nv_bfloat16><<<grid, FWD_THREADS, smem, st>>>(p, L, group);
       break;
     case ATTN_FP16:
       cudaFuncSetAttribute(fwd_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      fwd_kernel<__half><<<grid, FWD_THREADS, smem, st>>>(p, group);
+      fwd_kernel<__half><<<grid, FWD_THREADS, smem, st>>>(p, L, group);
       break;
     default:
       cudaFuncSetAttribute(fwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      fwd_kernel<float><<<grid, FWD_THREADS, smem, st>>>(p, group);
+      fwd_kernel<float><<<grid, FWD_THREADS, smem, st>>>(p, L, group);
       break;
   }
 }
@@ -199,12 +199,12 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
   const int klen = min(BN, sg.lk - kv0);
   for (int i = r; i < BN * dqk; i += BN) {
     const int rr = i / dqk, c = i % dqk;
-    sK[rr * ks + c] = rr < klen ? TypeOps<T>::to_f(Kg[((long long)(sg.k0 + kv0 + rr) * P.hkv + hk) * dqk + c]) : 0.f;
+    sK[rr * ks + c] = rr < klen ? TypeOps<T>::to_f(Kg[elem_off(P.sk_, sg.k0 + kv0 + rr, hk) + c]) : 0.f;
     sdK[rr * ks + c] = 0.f;
   }
   for (int i = r; i < BN * dv; i += BN) {
     const int rr = i / dv, c = i % dv;
-    sV[rr * vs + c] = rr < klen ? TypeOps<T>::to_f(Vg[((long long)(sg.k0 + kv0 + rr) * P.hkv + hk) * dv + c]) : 0.f;
+    sV[rr * vs + c] = rr < klen ? TypeOps<T>::to_f(Vg[elem_off(P.sv_, sg.k0 + kv0 + rr, hk) + c]) : 0.f;
     sdV[rr * vs + c] = 0.f;
   }
   const MaskArgs m = mask_args(P.mask, P.left, P.right, sg.lq, sg.lk);
@@ -216,11 +216,11 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
       __syncthreads();
       for (int i = r; i < BM * dqk; i += BN) {
         const int c = i / dqk, e = i % dqk;
-        sQ[i] = qs + c < sg.lq ? TypeOps<T>::to_f(Qg[((long long)(sg.q0 + qs + c) * P.hq + h) * dqk + e]) : 0.f;
+        sQ[i] = qs + c < sg.lq ? TypeOps<T>::to_f(Qg[elem_off(P.sq_, sg.q0 + qs + c, h) + e]) : 0.f;
       }
       for (int i = r; i < BM * dv; i += BN) {
         const int c = i / dv, e = i % dv;
-        sdO[i] = qs + c < sg.lq ? TypeOps<T>::to_f(dOg[((long long)(sg.q0 + qs + c) * P.hq + h) * dv + e]) : 0.f;
+        sdO[i] = qs + c < sg.lq ? TypeOps<T>::to_f(dOg[elem_off(P.sdo_, sg.q0 + qs + c, h) + e]) : 0.f;
       }
       if (r < BM) {
         const bool ok = qs + r < sg.lq;
@@ -256,12 +256,12 @@ __global__ void __launch_bounds__(BN) bwd_simt_kernel(Problem P) {
     }
   }
   __syncthreads();
-  const long long krow = (long long)(sg.k0 + kv0 + r) * P.hkv + hk;
-  if (r < klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P) * P.hkv, 12)) {
-    T* dK = static_cast<T*>(P.dk);
-    T* dV = static_cast<T*>(P.dv_out);
-    for (int e = 0; e < dqk; ++e) dK[krow * dqk + e] = TypeOps<T>::from_f(sdK[r * ks + e] * P.scale);
-    for (int e = 0; e < dv; ++e) dV[krow * dv + e] = TypeOps<T>::from_f(sdV[r * vs + e]);
+  const int krow = sg.k0 + kv0 + r;
+  if (r < klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P), 12)) {
+    T* dK = static_cast<T*>(P.dk) + elem_off(P.sdk_, krow, hk);
+    T* dV = static_cast<T*>(P.dv_out) + elem_off(P.sdv_, krow, hk);
+    for (int e = 0; e < dqk; ++e) dK[e] = TypeOps<T>::from_f(sdK[r * ks + e] * P.scale);
+    for (int e = 0; e < dv; ++e) dV[e] = TypeOps<T>::from_f(sdV[r * vs + e]);
   }
 }
 

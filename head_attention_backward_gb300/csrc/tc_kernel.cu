@@ -675,11 +675,17 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       ++n_item;
       if (item.x < 0) break;
       const ItemInfo I = item_info(P, item);
-      const long long krow = (long long)(I.sg.k0 + I.kt * BN + L) * P.hkv + I.hk;
+      const int krow = I.sg.k0 + I.kt * BN + L;   // this lane's key row of dK / dV
+      // element offsets of that row in dK and dV (taken here, before the step
+      // loop: measured faster than at the stores)
+      const long long kofs = elem_off(P.sdk_, krow, I.hk);
+      const long long vofs = elem_off(P.sdv_, krow, I.hk);
       if (I.nsteps == 0) {
-        if (L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P) * P.hkv, 2)) {
-          for (int e = 0; e < DQK; ++e) dKg[krow * DQK + e] = TypeOps<T>::from_f(0.f);
-          for (int e = 0; e < DV; ++e) dVg[krow * DV + e] = TypeOps<T>::from_f(0.f);
+        if (L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P), 2)) {
+          T* dk = dKg + kofs;
+          T* dv = dVg + vofs;
+          for (int e = 0; e < DQK; ++e) dk[e] = TypeOps<T>::from_f(0.f);
+          for (int e = 0; e < DV; ++e) dv[e] = TypeOps<T>::from_f(0.f);
         }
         continue;
       }
@@ -763,14 +769,14 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       g += I.nsteps;
       if (!wait_bar(ctx, B_DKV_FULL, it & 1, 32)) break;
       tc_fence_after();
-      const bool row_ok = L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P) * P.hkv, 2);
+      const bool row_ok = L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P), 2);
 #pragma unroll 1
       for (int ch = 0; ch < DQK / 32; ++ch) {
         uint32_t x[32];
         tmem_ld32(lane_addr + C::T_DK + ch * 32, x);
         tmem_wait_ld();
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dKg + krow * DQK + ch * 32);
+          uint4* dst = reinterpret_cast<uint4*>(dKg + kofs + ch * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint4 w;
@@ -788,7 +794,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         tmem_ld32(lane_addr + C::T_DV + ch * 32, x);
         tmem_wait_ld();
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dVg + krow * DV + ch * 32);
+          uint4* dst = reinterpret_cast<uint4*>(dVg + vofs + ch * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint4 w;
@@ -886,13 +892,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D view (dim, heads, rows) of a contiguous [rows, heads, dim] 16-bit
-// tensor; boxes of 64 x 1 x box_rows with 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* base, bool fp16, int dim, int heads, long long rows, int box_rows) {
+// 3-D view (dim, heads, rows) of a 16-bit tensor with element strides x;
+// boxes of 64 x 1 x box_rows with 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, bool fp16, int dim, int heads, long long rows,
+                     const Strides& x, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)x.h * 2, (cuuint64_t)x.r * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -906,10 +913,11 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
   using C = Cfg<DQK, DV>;
   const bool fp16 = IsHalf<T>::value;
   TmaMaps maps;
-  const long long rq = P.group ? P.tq : (long long)P.nseg * P.sq;
-  const long long rk = P.group ? P.tk : (long long)P.nseg * P.sk;
-  if (!make_map(&maps.q, P.q, fp16, DQK, P.hq, rq, BM) || !make_map(&maps.dout, P.dout, fp16, DV, P.hq, rq, BM) ||
-      !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, BN) || !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, BN))
+  const long long rq = rows_q(P), rk = rows_k(P);
+  if (!make_map(&maps.q, P.q, fp16, DQK, P.hq, rq, P.sq_, BM) ||
+      !make_map(&maps.dout, P.dout, fp16, DV, P.hq, rq, P.sdo_, BM) ||
+      !make_map(&maps.k, P.k, fp16, DQK, P.hkv, rk, P.sk_, BN) ||
+      !make_map(&maps.v, P.v, fp16, DV, P.hkv, rk, P.sv_, BN))
     return ATTN_ERR_CUDA;
   auto kern = bwd_tc_kernel<DQK, DV, T, DQM>;
   // at least 120 KB so that two CTAs never share an SM (each holds all 512 TMEM columns)

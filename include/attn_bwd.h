@@ -125,6 +125,30 @@ typedef struct {
   void* dq;               /* device outputs, same dtype as q; fully overwritten    */
   void* dk;
   void* dv;
+  /* Element strides {batch, row, head} of each tensor (the strided layouts of
+   * the pages' stride_s_q / nhead_stride arguments, TransformerEngine PR #446,
+   * ck_fused_attn_bwd.cpp); the head dimension itself is contiguous.  Batch
+   * mode: element (b, s, h, c) is at b*stride[0] + s*stride[1] + h*stride[2]
+   * + c.  Group mode: (t, h, c) at t*stride[1] + h*stride[2] + c; stride[0]
+   * is ignored.  All three zero = the contiguous layout above, so a
+   * zero-initialised struct keeps the contiguous convention.  Otherwise the
+   * row and head strides must be positive (the batch stride too when
+   * batch > 1) and, for BF16/FP16, multiples of 8 elements (16 bytes: the
+   * tensor-memory-access and vector alignment).  With batch > 1 the batch
+   * entries must follow each other either along rows (batch stride = seqlen
+   * x row stride, as in BSHD or packed QKV) or along heads (batch stride =
+   * nhead x head stride, as in BHSD or SBHD), the same way for every tensor
+   * of the call; any other layout returns ATTN_ERR_INVALID_ARG.  Outputs
+   * must not overlap one another or the inputs.  lse keeps its contiguous
+   * layout. */
+  int64_t stride_q[3];
+  int64_t stride_k[3];
+  int64_t stride_v[3];
+  int64_t stride_o[3];
+  int64_t stride_dout[3];
+  int64_t stride_dq[3];
+  int64_t stride_dk[3];
+  int64_t stride_dv[3];
 } attn_bwd_params;
 
 /* Forward helper that produces O and LSE for benchmark and test inputs
@@ -155,6 +179,10 @@ typedef struct {
   void* o;                /* device output [.., Hq, d_v], dtype; padding rows of a
                              padded group layout are left untouched            */
   float* lse;             /* device output, fp32 natural log (padding rows likewise) */
+  int64_t stride_q[3];    /* element strides, as in attn_bwd_params             */
+  int64_t stride_k[3];
+  int64_t stride_v[3];
+  int64_t stride_o[3];
 } attn_fwd_params;
 
 /* dQ accumulation modes (attn_bwd_params.deterministic).  The per-KV-tile dQ

@@ -69,3 +69,55 @@ def per_segment_report(got, ref, cu, name, tol_rel, min_cos, starts=None):
 def assert_all_ok(reports, what=""):
     bad = [r for r in reports if not r["ok"]]
     assert not bad, f"{what}: {len(bad)} failing comparisons, first: {bad[:3]}"
+
+
+# Strided layouts (per-tensor {batch, row, head} strides).  Each layout turns
+# contiguous device tensors into views with the same values and returns the
+# output views (filled with NaN) that the gradients go to.
+def _heads_outer(t):
+    """The values of a [B,S,H,D] / [T,H,D] tensor in a [B,H,S,D] / [H,T,D] buffer."""
+    if t.dim() == 4:
+        return t.transpose(1, 2).contiguous().transpose(1, 2)
+    return t.transpose(0, 1).contiguous().transpose(0, 1)
+
+
+def layout_heads_outer(x):
+    ins = {n: _heads_outer(t) for n, t in x.items()}
+    outs = tuple(_heads_outer(torch.full_like(x[n], float("nan"))) for n in ("q", "k", "v"))
+    return ins, outs
+
+
+def _sbhd(t):
+    """The values of a [B,S,H,D] tensor in an [S,B,H,D] buffer."""
+    return t.transpose(0, 1).contiguous().transpose(0, 1)
+
+
+def layout_sbhd(x):
+    ins = {n: _sbhd(t) for n, t in x.items()}
+    outs = tuple(_sbhd(torch.full_like(x[n], float("nan"))) for n in ("q", "k", "v"))
+    return ins, outs
+
+
+def layout_packed(x):
+    """q, k, v (and dq, dk, dv) as slices of one [.., Hq + 2 Hkv, D] buffer per
+    row (packed QKV; needs d_qk == d_v); o and dO with rows padded by 8."""
+    hq, hkv = x["q"].shape[-2], x["k"].shape[-2]
+    lead = x["q"].shape[:-2]
+
+    def pack(q, k, v):
+        buf = torch.full(lead + (hq + 2 * hkv, q.shape[-1]), float("nan"), dtype=q.dtype, device=q.device)
+        buf[..., :hq, :], buf[..., hq:hq + hkv, :], buf[..., hq + hkv:, :] = q, k, v
+        return buf[..., :hq, :], buf[..., hq:hq + hkv, :], buf[..., hq + hkv:, :]
+
+    def pad_rows(t):
+        buf = torch.full(lead + (t.shape[-2] + 1, t.shape[-1]), float("nan"), dtype=t.dtype, device=t.device)
+        buf[..., :-1, :] = t
+        return buf[..., :-1, :]
+
+    q, k, v = pack(x["q"], x["k"], x["v"])
+    ins = dict(q=q, k=k, v=v, o=pad_rows(x["o"]), do=pad_rows(x["do"]))
+    nan = torch.full_like(x["q"], float("nan"))
+    return ins, pack(nan, torch.full_like(x["k"], float("nan")), torch.full_like(x["v"], float("nan")))
+
+
+STRIDED_LAYOUTS = (layout_heads_outer, layout_packed, layout_sbhd)

@@ -8,6 +8,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 from head_attention_backward_gb300 import binding as B
 
@@ -41,6 +42,8 @@ int main(void) {
   F(attn_bwd_params, cu_seqlens_q) F(attn_bwd_params, cu_seqlens_q_padded)
   F(attn_bwd_params, cu_seqlens_k_padded) F(attn_bwd_params, mask) F(attn_bwd_params, softmax_scale)
   F(attn_bwd_params, deterministic) F(attn_bwd_params, q) F(attn_bwd_params, lse) F(attn_bwd_params, dv)
+  F(attn_bwd_params, stride_q) F(attn_bwd_params, stride_dout) F(attn_bwd_params, stride_dv)
+  F(attn_fwd_params, stride_q) F(attn_fwd_params, stride_o)
   F(attn_fwd_params, cu_seqlens_k) F(attn_fwd_params, cu_seqlens_k_padded) F(attn_fwd_params, softmax_scale) F(attn_fwd_params, q) F(attn_fwd_params, lse)
   return 0;
 }
@@ -165,6 +168,74 @@ def test_group_mode_needs_both_seqstart_arrays(lib):
     p.cu_seqlens_q = 0x1000           # cu_seqlens_k left NULL
     assert B.attn_bwd_workspace_size(p)[0] == -1
     assert B.attn_bwd(p, 0x100000, 1 << 40, 0) == -1
+
+
+def _with_strides(p, **strides):
+    for name, val in strides.items():
+        getattr(p, "stride_" + name)[:] = val
+    return p
+
+
+def test_strides_validated(lib):
+    S, H, Hk, D = 4096, 32, 8, 128
+    # BHSD ([B,H,S,D] buffers seen as [B,S,H,D]) on every tensor: batch folded into heads
+    bh = dict(q=(H * S * D, D, S * D), k=(Hk * S * D, D, S * D), v=(Hk * S * D, D, S * D),
+              o=(H * S * D, D, S * D), dout=(H * S * D, D, S * D), dq=(H * S * D, D, S * D),
+              dk=(Hk * S * D, D, S * D), dv=(Hk * S * D, D, S * D))
+    ok, n_bhsd = B.attn_bwd_workspace_size(_with_strides(make(), **bh))
+    assert ok == 0 and 0 < n_bhsd <= B.attn_bwd_workspace_size(make())[1]
+    # BHSD on q alone, the rest BSHD: the batch cannot be folded one way for all
+    assert B.attn_bwd_workspace_size(_with_strides(make(), q=bh["q"]))[0] == -1
+    # packed QKV rows (batch stride = S x row stride) mix with contiguous tensors
+    assert B.attn_bwd_workspace_size(_with_strides(make(), q=(S * 3 * H * D, 3 * H * D, D)))[0] == 0
+    bad = [(0, H * D, D),                             # batch stride missing with B = 2
+           (S * H * D, H * D + 4, D),                 # 16-bit row stride not a multiple of 8
+           (S * H * D, H * D, -D),                    # negative head stride
+           (S * H * D, 1 << 37, D)]                   # beyond the tensor-map stride range
+    for st in bad:
+        assert B.attn_bwd_workspace_size(_with_strides(make(), q=st))[0] == -1, st
+        assert B.attn_bwd(_with_strides(make(), dq=st), 0x100000, 1 << 40, 0) == -1, st
+        assert B.attn_bwd(_with_strides(make(), dv=st), 0x100000, 1 << 40, 0) == -1, st
+    # fp32 tensors take any positive stride; group mode ignores the batch stride
+    p = _with_strides(make(dtype=B.ATTN_FP32, d_qk=32, d_v=33), q=(S * (H * 32 + 1), H * 32 + 1, 32))
+    assert B.attn_bwd_workspace_size(p)[0] == 0
+    p = _with_strides(make(total_q=100, total_k=100), q=(0, H * D, D))
+    p.cu_seqlens_q, p.cu_seqlens_k = 0x1000, 0x2000
+    assert B.attn_bwd_workspace_size(p)[0] == 0
+
+
+def test_strided_test_layouts_are_accepted(lib):
+    """Every strided layout the GPU parity tests use passes the sizing call's
+    stride checks (batch folded along rows or heads), and a tensor set that
+    mixes the two foldings is refused."""
+    from head_attention_backward_gb300 import workloads as W
+    from tests.parity import STRIDED_LAYOUTS, layout_heads_outer
+    cases = [W.Workload("b", torch.bfloat16, 2, 4, 2, 300, 300, 128, 128, 1),
+             W.Workload("b1", torch.bfloat16, 3, 4, 1, 200, 333, 64, 64, 0),
+             W.Workload("f", torch.float32, 2, 2, 1, 150, 150, 64, 64, 1),
+             W.thd("t", [100, 0, 37], hq=4, hkv=2, gaps_q=[1, 0, 2, 3], gaps_k=[0, 0, 0, 5])]
+    for wl in cases:
+        x = wl.inputs()
+        x["o"] = torch.zeros_like(x["do"])
+        cu = wl.cu_seqlens()
+        kw = {}
+        if cu is not None:
+            kw = dict(cu_seqlens_q=cu, cu_seqlens_k=wl.cu_seqlens_k(), cu_seqlens_q_padded=wl.cu_seqlens_q_padded(),
+                      cu_seqlens_k_padded=wl.cu_seqlens_k_padded())
+        lse = torch.zeros(wl.shapes()["lse"])
+        for layout in STRIDED_LAYOUTS:
+            if layout.__name__ == "layout_sbhd" and wl.group_mode:
+                continue
+            if layout.__name__ == "layout_packed" and (x["q"].shape[:-2] != x["k"].shape[:-2] or wl.d_qk != wl.d_v):
+                continue   # one packed buffer holds q, k and v rows side by side
+            ins, out = layout(x)
+            p = B.bwd_params(ins["q"], ins["k"], ins["v"], ins["o"], ins["do"], lse, *out, scale=0.1, mask=wl.mask,
+                             max_seqlen_q=wl.sq, max_seqlen_k=wl.sk, **kw)
+            assert B.attn_bwd_workspace_size(p)[0] == 0, (wl.name, layout.__name__)
+        if not wl.group_mode and wl.batch > 1:
+            ins, out = layout_heads_outer(x)
+            p = B.bwd_params(ins["q"], ins["k"], ins["v"], x["o"], x["do"], lse, *out, scale=0.1, mask=wl.mask)
+            assert B.attn_bwd_workspace_size(p)[0] == -1, wl.name
 
 
 def test_padded_starts_only_in_group_mode(lib):

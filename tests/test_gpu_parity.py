@@ -14,7 +14,8 @@ import torch
 
 from head_attention_backward_gb300 import workloads as W
 from oracle import attn_ref as R
-from tests.parity import assert_all_ok, compare, per_segment_report, tolerances
+from tests.parity import (STRIDED_LAYOUTS, assert_all_ok, compare, layout_heads_outer, layout_packed,
+                          layout_sbhd, per_segment_report, tolerances)
 
 pytestmark = pytest.mark.gpu
 
@@ -158,6 +159,90 @@ def test_thd_padded_fp32(B):
     wl = W.thd("thd_padded_fp32", [70, 5, 130], hq=2, hkv=1, d_qk=64, d_v=64, dtype=torch.float32,
                seed=141, gaps_q=[2, 3, 0, 4], gaps_k=[0, 1, 64, 3])
     assert_all_ok(run_backward_vs_oracle(B, wl, 1), "padded THD fp32")
+
+
+def run_strided_vs_oracle(B, wl, det, layout):
+    x = wl.inputs()
+    cu, cuk = wl.cu_seqlens(), wl.cu_seqlens_k()
+    stq, stk = wl.cu_seqlens_q_padded(), wl.cu_seqlens_k_padded()
+    kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cuk)
+    if stq is not None or stk is not None:
+        kw.update(cu_seqlens_q_padded=stq, cu_seqlens_k_padded=stk)
+    o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, **kw)
+    o_in, lse_in = o64.to(wl.dtype), lse64.to(torch.float32)
+    ref = R.attn_backward(x["q"], x["k"], x["v"], o_in, x["do"], lse_in, wl.scale, **kw)
+    dev = {n: t.cuda() for n, t in dict(x, o=o_in).items()}
+    ins, out = layout(dev)
+    assert not ins["q"].is_contiguous() and not out[0].is_contiguous()
+    dkw = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
+    got = B.attn_backward(ins["q"], ins["k"], ins["v"], ins["o"], ins["do"], lse_in.cuda(), scale=wl.scale,
+                          deterministic=det, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk, out=out, **dkw)
+    torch.cuda.synchronize()
+    tol, mcos = tolerances(wl.dtype)
+    reps = []
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        g = g.cpu()
+        rep = compare(g, r, tol, mcos)
+        rep["tensor"] = name
+        reps.append(rep)
+        if cu is not None:
+            offs, st = (cu, stq) if name == "dq" else (cuk, stk)
+            reps.extend(per_segment_report(g, r, offs.tolist(), name, tol, mcos,
+                                           None if st is None else st.tolist()))
+    return reps
+
+
+STRIDED = [
+    (_wl("bf16_gqa_causal_ragged", torch.bfloat16, 2, 4, 2, 300, 300, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=51),
+     layout_heads_outer),
+    (_wl("bf16_mha_window", torch.bfloat16, 2, 2, 2, 257, 257, 128, 128, W.MASK_WINDOW, 40, 0, seed=52),
+     layout_packed),
+    (_wl("bf16_d192_br_long_k", torch.bfloat16, 1, 2, 1, 100, 300, 192, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, seed=53),
+     layout_heads_outer),
+    (_wl("bf16_d64_gqa", torch.bfloat16, 2, 4, 1, 200, 200, 64, 64, W.MASK_CAUSAL_TOP_LEFT, seed=54),
+     layout_packed),
+    (W.thd("thd_gqa", [100, 0, 37, 250, 5], hq=4, hkv=2, seed=55), layout_packed),
+    (W.thd("thd_cross_padded", [100, 0, 37, 250], hq=4, hkv=2, mask=W.MASK_CAUSAL_BOTTOM_RIGHT, seed=56,
+           seqlens_k=[300, 64, 0, 129], gaps_q=[3, 0, 17, 140, 2], gaps_k=[0, 5, 131, 7, 1]), layout_heads_outer),
+    (_wl("fp32_causal", torch.float32, 2, 2, 1, 150, 150, 64, 64, W.MASK_CAUSAL_TOP_LEFT, seed=57),
+     layout_heads_outer),
+    (_wl("bf16_gqa_nomask_sq_ne_sk", torch.bfloat16, 3, 4, 2, 200, 333, 128, 128, W.MASK_NONE, seed=58),
+     layout_sbhd),
+    (_wl("fp16_window_lr", torch.float16, 2, 2, 1, 300, 350, 128, 128, W.MASK_WINDOW, 30, 20, seed=59),
+     layout_sbhd),
+]
+
+
+@pytest.mark.parametrize("det", **DET_MODES)
+@pytest.mark.parametrize("case", STRIDED, ids=lambda c: f"{c[0].name}-{c[1].__name__[7:]}")
+def test_strided_layouts(B, case, det):
+    """Non-contiguous q/k/v/o/dO and dq/dk/dv (heads-outer buffers, packed QKV
+    slices, padded rows) give the oracle's gradients; every output element is
+    written (outputs start as NaN)."""
+    wl, layout = case
+    assert_all_ok(run_strided_vs_oracle(B, wl, det, layout), f"{wl.name} {layout.__name__}")
+
+
+def test_forward_helper_strided(B):
+    for wl, layout in STRIDED[:2] + STRIDED[4:6]:
+        x = wl.inputs()
+        kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=wl.cu_seqlens(),
+                  cu_seqlens_k=wl.cu_seqlens_k())
+        if wl.gaps_q or wl.gaps_k:
+            kw.update(cu_seqlens_q_padded=wl.cu_seqlens_q_padded(), cu_seqlens_k_padded=wl.cu_seqlens_k_padded())
+        o_ref, lse_ref = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, **kw)
+        dev = {n: t.cuda() for n, t in x.items()}
+        dev["o"] = torch.zeros(x["do"].shape, dtype=wl.dtype, device="cuda")
+        ins, _ = layout(dev)
+        dkw = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
+        o, lse = B.attn_forward(ins["q"], ins["k"], ins["v"], scale=wl.scale, max_seqlen_q=wl.sq,
+                                max_seqlen_k=wl.sk, **dkw)
+        torch.cuda.synchronize()
+        tol, mcos = tolerances(wl.dtype)
+        assert compare(o.cpu(), o_ref, tol, mcos)["ok"], wl.name
+        fin = torch.isfinite(lse_ref)
+        assert torch.equal(torch.isfinite(lse.cpu()), fin)
+        assert float((lse.cpu().double()[fin] - lse_ref[fin]).abs().max()) < 1e-3
 
 
 def test_thd_window_and_d192(B):
