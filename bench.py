@@ -75,12 +75,8 @@ def peaks():
 KERNEL_SOURCES = ("tc_kernel.cu", "common.cuh", "sm100_ptx.cuh")
 KERNEL_TRAFFIC = {
     "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:ordered": {
-        "bytes": 621.21e6 + 282.95e6,
-        "src": "90fdca785860b58d",
-        "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
-    "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:split": {
-        "bytes": 551.55e6 + 2.19e9,
-        "src": "523903848972bbd9",
+        "bytes": 624.44e6 + 284.06e6,
+        "src": "59491f421b6c01c1",
         "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
 }
 
@@ -323,26 +319,25 @@ def run_ours(args, wl):
                      "workspace_bytes": nb}
 
     # end to end through the C ABI: pinned host inputs in, results back out
-    e2e_avg, h2d, d2h = float("nan"), 0, 0
+    e2e_avg, h2d, d2h, e2e_chunks = float("nan"), 0, 0, 0
     if not args.no_e2e:
         host = {k: v.to(dev).cpu().pin_memory() for k, v in (("q", d["q"]), ("k", d["k"]), ("v", d["v"]),
                                                                ("o", o), ("do", d["do"]), ("lse", lse))}
         host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs)
-        dev_in = {"q": d["q"], "k": d["k"], "v": d["v"], "o": o, "do": d["do"], "lse": lse}
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in outs)
         e2e_ms = []
+        # attn_bwd_host: chunk c's copies overlap its neighbours' compute
+        h = B.host_tensors(host["q"], host["k"], host["v"], host["o"], host["do"], host["lse"], *host_out)
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        chunks = e2e_chunks = args.e2e_chunks if args.e2e_chunks > 0 else min(wl.batch, 2)
         for i in range(args.warmup + args.steps):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            for k2, t in host.items():
-                dev_in[k2].copy_(t, non_blocking=True)
-            rc = B.attn_bwd(p, ws.data_ptr(), nbytes, stream)
+            rc = B.attn_bwd_host(p, h, ws.data_ptr(), nbytes, stream, s_in.cuda_stream, s_out.cuda_stream, chunks)
             if rc != 0:
-                raise B.AttnError(rc, "attn_bwd")
-            for hb, db in zip(host_out, outs):
-                hb.copy_(db, non_blocking=True)
+                raise B.AttnError(rc, "attn_bwd_host")
             e1.record()
             e1.synchronize()
             if i >= args.warmup:
@@ -366,7 +361,7 @@ def run_ours(args, wl):
                      "step_stage_ms": [sum(s[i] for s in stage) / len(stage) for i in range(4)]},
         "e2e": None if args.no_e2e else {"value": job_throughput(world, fl, e2e_avg), "unit": "TFLOP/s",
                                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                                         "ms_per_step": e2e_avg},
+                                         "ms_per_step": e2e_avg, "api": "attn_bwd_host", "chunks": e2e_chunks},
         "gpu_launches": 4 * args.steps,
         "split_slices": split_leg,
         "clocks": clk,
@@ -394,6 +389,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="batch chunks of the end-to-end leg (0: min(batch, 2))")
     ap.add_argument("--batch", type=int, default=0, help="override the batch of a batch-mode workload")
     ap.add_argument("--atomic", action="store_true", help="same as --dq-mode atomic")
     ap.add_argument("--dq-mode", choices=sorted(DQ_MODES), default=None,

@@ -52,8 +52,13 @@ class AttnFwdParams(ctypes.Structure):
                 ("stride_q", _i64x3), ("stride_k", _i64x3), ("stride_v", _i64x3), ("stride_o", _i64x3)]
 
 
+class AttnHostTensors(ctypes.Structure):
+    _fields_ = [("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("dout", _vp), ("lse", _vp),
+                ("dq", _vp), ("dk", _vp), ("dv", _vp)]
+
+
 EXPORTS = ["attn_bwd_workspace_size", "attn_bwd", "attn_bwd_timed", "attn_bwd_read_status",
-           "attn_fwd", "attn_status_string", "attn_bwd_static_ws", "attn_selftest_waits"]
+           "attn_fwd", "attn_status_string", "attn_bwd_static_ws", "attn_selftest_waits", "attn_bwd_host"]
 
 _lib = None
 
@@ -79,6 +84,9 @@ def load(path: str = LIB_PATH):
     lib.attn_fwd.restype = ctypes.c_int
     lib.attn_status_string.argtypes = [ctypes.c_int]
     lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_bwd_host.argtypes = [P(AttnBwdParams), P(AttnHostTensors), _vp, ctypes.c_size_t, _vp, _vp, _vp,
+                                  ctypes.c_int]
+    lib.attn_bwd_host.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -115,6 +123,22 @@ def attn_bwd_read_status(workspace: int, stream: int = 0):
 
 def attn_fwd(p: AttnFwdParams, stream: int = 0) -> int:
     return load().attn_fwd(ctypes.byref(p), stream)
+
+
+def attn_bwd_host(p: AttnBwdParams, host: AttnHostTensors, workspace: int, workspace_bytes: int, stream: int,
+                  copy_in: int, copy_out: int, chunks: int) -> int:
+    return load().attn_bwd_host(ctypes.byref(p), ctypes.byref(host), workspace, workspace_bytes, stream, copy_in,
+                                copy_out, chunks)
+
+
+def host_tensors(q, k, v, o, do, lse, dq, dk, dv) -> AttnHostTensors:
+    """Pinned host tensors (contiguous) for attn_bwd_host."""
+    h = AttnHostTensors()
+    for name, t in zip(("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv"), (q, k, v, o, do, lse, dq, dk, dv)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"host tensor {name} must be a contiguous CPU tensor (pinned for overlap)")
+        setattr(h, name, t.data_ptr())
+    return h
 
 
 def attn_status_string(st: int) -> str:

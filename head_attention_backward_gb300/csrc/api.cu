@@ -13,8 +13,6 @@
 
 namespace attn {
 
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 static bool tc_headdims(int dqk, int dv) {
   return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
 }
@@ -155,9 +153,13 @@ static int validate_bwd(const attn_bwd_params* p) {
   } else if (!tc_headdims(p->d_qk, p->d_v)) {
     return ATTN_ERR_UNSUPPORTED_HEADDIM;
   }
-  const void* ptrs[] = {p->q, p->k, p->v, p->o, p->dout, p->lse, p->dq, p->dk, p->dv};
+  // 16-bit tensors feed tensor maps and 16-byte vector accesses; fp32 tensors
+  // and lse are read and written one element at a time
+  const uintptr_t amask = p->dtype == ATTN_FP32 ? 3u : 15u;
+  const void* ptrs[] = {p->q, p->k, p->v, p->o, p->dout, p->dq, p->dk, p->dv};
   for (const void* x : ptrs)
-    if (!x || !aligned16(x)) return ATTN_ERR_INVALID_ARG;
+    if (!x || (reinterpret_cast<uintptr_t>(x) & amask) != 0) return ATTN_ERR_INVALID_ARG;
+  if (!p->lse || (reinterpret_cast<uintptr_t>(p->lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -235,8 +237,12 @@ static void log_config(const attn_bwd_params& p, const WsLayout& L) {
                p.softmax_scale, p.deterministic, L.nsplits, L.max_items, L.total);
 }
 
+// Schedule launch for one part of a call split into parts (attn_bwd_host):
+// parts after the first keep the status the earlier parts left.
+void launch_schedule_part(const Problem& P, cudaStream_t st, bool keep_status);
+
 static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t s,
-               cudaEvent_t* ev /* 4 events or null */) {
+               cudaEvent_t* ev /* 4 events or null */, bool keep_status = false) {
   int st = validate_bwd(p);
   if (st != ATTN_OK) return st;
   attn_bwd_params e;
@@ -248,7 +254,7 @@ static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t
   if (log_enabled()) log_config(e, L);
   const Problem P = make_problem(e, sx, ws);
   if (ev) cudaEventRecord(ev[0], s);
-  launch_schedule(P, s);
+  launch_schedule_part(P, s, keep_status);
   launch_preprocess(P, s);
   if (ev) cudaEventRecord(ev[1], s);
   if (P.dtype == ATTN_FP32) {
@@ -263,9 +269,112 @@ static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+static bool all_zero(const int64_t x[3]) { return x[0] == 0 && x[1] == 0 && x[2] == 0; }
+
+static size_t dtype_bytes(int dtype) { return dtype == ATTN_FP32 ? 4 : 2; }
+
+// Chunked host <-> device pipeline of attn_bwd_host: chunk c = batch entries
+// [b0, b1).  Its inputs go up on `in`, its backward runs on `s`, its
+// gradients come down on `out`; events order the three, so the copies of one
+// chunk overlap the compute of its neighbours.
+static int run_host(const attn_bwd_params* p, const attn_host_tensors* h, void* ws, size_t ws_bytes, cudaStream_t s,
+                    cudaStream_t in, cudaStream_t out, int chunks) {
+  int st = validate_bwd(p);
+  if (st != ATTN_OK) return st;
+  if (!h || !h->q || !h->k || !h->v || !h->o || !h->dout || !h->lse || !h->dq || !h->dk || !h->dv)
+    return ATTN_ERR_INVALID_ARG;
+  if (s == in || s == out || in == out) return ATTN_ERR_INVALID_ARG;
+  // the staging buffers are contiguous (zero strides, or the contiguous ones spelt out)
+  const bool group = p->cu_seqlens_q != nullptr;
+  const TensorDesc t[8] = {{p->stride_q, p->seqlen_q, p->nhead_q, p->d_qk},   {p->stride_k, p->seqlen_k, p->nhead_kv, p->d_qk},
+                           {p->stride_v, p->seqlen_k, p->nhead_kv, p->d_v},   {p->stride_o, p->seqlen_q, p->nhead_q, p->d_v},
+                           {p->stride_dout, p->seqlen_q, p->nhead_q, p->d_v}, {p->stride_dq, p->seqlen_q, p->nhead_q, p->d_qk},
+                           {p->stride_dk, p->seqlen_k, p->nhead_kv, p->d_qk}, {p->stride_dv, p->seqlen_k, p->nhead_kv, p->d_v}};
+  for (const TensorDesc& x : t) {
+    if (all_zero(x.in)) continue;
+    const long long h = x.dim, r = (long long)x.heads * x.dim, b = (long long)x.seqlen * r;
+    if (x.in[1] != r || x.in[2] != h || (!group && p->batch > 1 && x.in[0] != b)) return ATTN_ERR_INVALID_ARG;
+  }
+  attn_bwd_params e;
+  Strides sx[8];
+  if ((st = effective_bwd(*p, &e, sx)) != ATTN_OK) return st;
+  if (!ws || ws_bytes < ws_layout(e).total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  const int nb = group ? 1 : p->batch;
+  if (chunks < 1) chunks = 1;
+  if (chunks > nb) chunks = nb;
+  const size_t es = dtype_bytes(p->dtype);
+  // bytes per batch entry of each tensor (group mode: the whole tensor, one chunk)
+  const long long rq = group ? p->total_q : p->seqlen_q, rk = group ? p->total_k : p->seqlen_k;
+  const size_t bq = (size_t)rq * p->nhead_q * p->d_qk * es, bk = (size_t)rk * p->nhead_kv * p->d_qk * es;
+  const size_t bv = (size_t)rk * p->nhead_kv * p->d_v * es, bo = (size_t)rq * p->nhead_q * p->d_v * es;
+  const size_t bl = (size_t)p->nhead_q * rq * sizeof(float);
+  cudaEvent_t ev_in[64], ev_c[64], ev_out;
+  chunks = chunks > 64 ? 64 : chunks;
+  int made = 0;
+  for (; made < chunks; ++made) {
+    if (cudaEventCreateWithFlags(&ev_in[made], cudaEventDisableTiming) != cudaSuccess) break;
+    if (cudaEventCreateWithFlags(&ev_c[made], cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventDestroy(ev_in[made]);
+      break;
+    }
+  }
+  const bool have_out = made == chunks && cudaEventCreateWithFlags(&ev_out, cudaEventDisableTiming) == cudaSuccess;
+  bool ok = have_out;
+  // the caller's earlier work on `s` (which may have produced the inputs' staging
+  // buffers' previous users) comes before the first copy
+  if (ok) ok = cudaEventRecord(ev_c[0], s) == cudaSuccess && cudaStreamWaitEvent(in, ev_c[0], 0) == cudaSuccess &&
+               cudaStreamWaitEvent(out, ev_c[0], 0) == cudaSuccess;
+  for (int c = 0; ok && c < chunks; ++c) {
+    const int b0 = (int)((long long)nb * c / chunks), b1 = (int)((long long)nb * (c + 1) / chunks);
+    const size_t n = (size_t)(b1 - b0);
+    auto dev = [&](const void* base, size_t per) { return static_cast<char*>(const_cast<void*>(base)) + b0 * per; };
+    auto hst = [&](const void* base, size_t per) { return static_cast<const char*>(base) + b0 * per; };
+    const void* srcs[6] = {h->q, h->k, h->v, h->o, h->dout, h->lse};
+    const void* dsts[6] = {p->q, p->k, p->v, p->o, p->dout, p->lse};
+    const size_t per[6] = {bq, bk, bv, bo, bo, bl};
+    for (int i = 0; ok && i < 6; ++i)
+      ok = cudaMemcpyAsync(dev(dsts[i], per[i]), hst(srcs[i], per[i]), n * per[i], cudaMemcpyHostToDevice, in) ==
+           cudaSuccess;
+    ok = ok && cudaEventRecord(ev_in[c], in) == cudaSuccess && cudaStreamWaitEvent(s, ev_in[c], 0) == cudaSuccess;
+    if (!ok) break;
+    attn_bwd_params part = *p;
+    if (!group) {
+      part.batch = (int)n;
+      part.q = dev(p->q, bq); part.k = dev(p->k, bk); part.v = dev(p->v, bv);
+      part.o = dev(p->o, bo); part.dout = dev(p->dout, bo);
+      part.lse = reinterpret_cast<const float*>(dev(p->lse, bl));
+      part.dq = dev(p->dq, bq); part.dk = dev(p->dk, bk); part.dv = dev(p->dv, bv);
+    }
+    if ((st = run(&part, ws, ws_bytes, s, nullptr, c > 0)) != ATTN_OK) break;
+    ok = cudaEventRecord(ev_c[c], s) == cudaSuccess && cudaStreamWaitEvent(out, ev_c[c], 0) == cudaSuccess;
+    void* hd[3] = {h->dq, h->dk, h->dv};
+    const void* dd[3] = {p->dq, p->dk, p->dv};
+    const size_t pg[3] = {bq, bk, bv};
+    for (int i = 0; ok && i < 3; ++i)
+      ok = cudaMemcpyAsync(static_cast<char*>(hd[i]) + b0 * pg[i], dev(dd[i], pg[i]), n * pg[i],
+                           cudaMemcpyDeviceToHost, out) == cudaSuccess;
+  }
+  // `s` completes only after the last gradients are back on the host
+  if (ok && st == ATTN_OK)
+    ok = cudaEventRecord(ev_out, out) == cudaSuccess && cudaStreamWaitEvent(s, ev_out, 0) == cudaSuccess;
+  for (int i = 0; i < made; ++i) {
+    cudaEventDestroy(ev_in[i]);
+    cudaEventDestroy(ev_c[i]);
+  }
+  if (have_out) cudaEventDestroy(ev_out);
+  if (st != ATTN_OK) return st;
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace attn
 
 using namespace attn;
+
+extern "C" int attn_bwd_host(const attn_bwd_params* p, const attn_host_tensors* host, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream, cudaStream_t copy_in,
+                             cudaStream_t copy_out, int chunks) {
+  return run_host(p, host, workspace, workspace_bytes, stream, copy_in, copy_out, chunks);
+}
 
 extern "C" int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes) {
   if (!bytes) return ATTN_ERR_INVALID_ARG;

@@ -18,18 +18,24 @@ namespace attn {
 
 // ----------------------------------------------------------------- schedule
 
-__global__ void __launch_bounds__(256) schedule_kernel(Problem P) {
+// keep_status: a later part of one call split into parts (attn_bwd_host); the
+// status of the earlier parts stays, and a part after a failed one does no work.
+__global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_status) {
   __shared__ int s_bad;
   const int tid = threadIdx.x;
   if (tid == 0) {
     s_bad = 0;
-    P.hdr[HDR_STATUS] = 0;
+    if (keep_status && P.hdr[HDR_STATUS] != 0) {
+      s_bad = 2;
+    } else {
+      P.hdr[HDR_STATUS] = 0;
+      P.hdr[HDR_DIAG] = 0;
+    }
     P.hdr[HDR_NEXT] = 0;
-    P.hdr[HDR_DIAG] = 0;
   }
-  if (tid >= 16 && tid < HDR_WORDS) P.hdr[tid] = 0;   // optional per-site wait counters
   __syncthreads();
-  if (P.group) {
+  if (s_bad == 0 && tid >= 16 && tid < HDR_WORDS) P.hdr[tid] = 0;   // optional per-site wait counters
+  if (P.group && s_bad == 0) {
     // lengths from the logical offsets; each segment's physical rows
     // [start, start + length) lie before the next segment's start and inside
     // the tensor (without padding the starts are the offsets themselves and
@@ -54,7 +60,7 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P) {
     // no work items and no query tiles: nothing later in the call touches dQ
     // rows derived from the rejected cu_seqlens
     if (tid == 0) {
-      P.hdr[HDR_STATUS] = ATTN_ERR_BAD_SEQLENS;
+      if (s_bad == 1) P.hdr[HDR_STATUS] = ATTN_ERR_BAD_SEQLENS;
       P.hdr[HDR_NITEMS] = 0;
     }
     for (int b = tid; b <= P.nseg; b += blockDim.x) P.tile_off[b] = 0;
@@ -113,7 +119,11 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P) {
 }
 
 void launch_schedule(const Problem& P, cudaStream_t st) {
-  schedule_kernel<<<1, 256, 0, st>>>(P);
+  schedule_kernel<<<1, 256, 0, st>>>(P, 0);
+}
+
+void launch_schedule_part(const Problem& P, cudaStream_t st, bool keep_status) {
+  schedule_kernel<<<1, 256, 0, st>>>(P, keep_status ? 1 : 0);
 }
 
 // --------------------------------------------------------------- preprocess

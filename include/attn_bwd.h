@@ -121,8 +121,9 @@ typedef struct {
   const void* v;
   const void* o;
   const void* dout;
-  const float* lse;       /* device, fp32 natural log                              */
-  void* dq;               /* device outputs, same dtype as q; fully overwritten    */
+  const float* lse;       /* device, fp32 natural log, 4-byte aligned              */
+  void* dq;               /* device outputs, same dtype as q; fully overwritten.
+                             q .. dv are 16-byte aligned (4-byte for FP32)     */
   void* dk;
   void* dv;
   /* Element strides {batch, row, head} of each tensor (the strided layouts of
@@ -238,6 +239,42 @@ int attn_fwd(const attn_fwd_params* p, cudaStream_t stream);
 
 /* Static description of a status code. */
 const char* attn_status_string(int status);
+
+/* Host-side tensors of attn_bwd_host: page-locked (pinned) host memory in
+ * the contiguous layouts above.  q, k, v, o, dout, lse are read; dq, dk, dv
+ * are written. */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+} attn_host_tensors;
+
+/* attn_bwd for inputs and outputs in host memory: copies Q, K, V, O, dO and
+ * LSE from `host` into the device buffers of *p, runs the backward pass and
+ * copies dQ, dK, dV back into `host`.  *p is an ordinary attn_bwd problem whose
+ * tensor pointers are the caller's contiguous device staging buffers (all
+ * strides zero).  In batch mode the batch is split into `chunks` runs of
+ * consecutive entries (clamped to [1, batch]; group mode runs one chunk):
+ * chunk c's inputs are copied on `copy_in`, its backward runs on `stream`,
+ * its gradients are copied on `copy_out`, so one chunk's copies overlap
+ * another chunk's compute.  The three streams must be distinct; the copies
+ * start after the work already queued on `stream`, and `stream` completes
+ * only once the last gradients are in host memory (synchronise it before
+ * reading them).  Each chunk runs the same kernels in the same order as
+ * attn_bwd, so the deterministic modes give the same bits as one attn_bwd
+ * call.  The workspace is sized by attn_bwd_workspace_size(p) and reused by
+ * the chunks in turn; a device-side failure in one chunk is kept in it (read
+ * with attn_bwd_read_status) and the later chunks skip their work.  Returns
+ * ATTN_OK when everything was enqueued, an error code otherwise. */
+int attn_bwd_host(const attn_bwd_params* p, const attn_host_tensors* host, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream, cudaStream_t copy_in, cudaStream_t copy_out,
+                  int chunks);
 
 /* Size of the device array attn_bwd_static_ws uses as its workspace. */
 #define ATTN_BWD_STATIC_WS_BYTES (64u << 20)

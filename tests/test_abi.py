@@ -44,6 +44,8 @@ int main(void) {
   F(attn_bwd_params, deterministic) F(attn_bwd_params, q) F(attn_bwd_params, lse) F(attn_bwd_params, dv)
   F(attn_bwd_params, stride_q) F(attn_bwd_params, stride_dout) F(attn_bwd_params, stride_dv)
   F(attn_fwd_params, stride_q) F(attn_fwd_params, stride_o)
+  printf("attn_host_tensors.size %zu\n", sizeof(attn_host_tensors));
+  F(attn_host_tensors, lse) F(attn_host_tensors, dv)
   F(attn_fwd_params, cu_seqlens_k) F(attn_fwd_params, cu_seqlens_k_padded) F(attn_fwd_params, softmax_scale) F(attn_fwd_params, q) F(attn_fwd_params, lse)
   return 0;
 }
@@ -66,11 +68,14 @@ def test_ctypes_structs_match_c_layout():
     lay = _c_layout()
     assert lay["attn_bwd_params.size"] == ctypes.sizeof(B.AttnBwdParams)
     assert lay["attn_fwd_params.size"] == ctypes.sizeof(B.AttnFwdParams)
+    assert lay["attn_host_tensors.size"] == ctypes.sizeof(B.AttnHostTensors)
+    classes = {"attn_bwd_params": B.AttnBwdParams, "attn_fwd_params": B.AttnFwdParams,
+               "attn_host_tensors": B.AttnHostTensors}
     for key, off in lay.items():
         s, m = key.split(".")
         if m == "size":
             continue
-        cls = B.AttnBwdParams if s == "attn_bwd_params" else B.AttnFwdParams
+        cls = classes[s]
         assert getattr(cls, m).offset == off, key
 
 
@@ -236,6 +241,22 @@ def test_strided_test_layouts_are_accepted(lib):
             ins, out = layout_heads_outer(x)
             p = B.bwd_params(ins["q"], ins["k"], ins["v"], x["o"], x["do"], lse, *out, scale=0.1, mask=wl.mask)
             assert B.attn_bwd_workspace_size(p)[0] == -1, wl.name
+
+
+def test_host_entry_validates_before_launch(lib):
+    def host(**kw):
+        h = B.AttnHostTensors()
+        for i, name in enumerate(["q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv"]):
+            setattr(h, name, kw.get(name, 0x20000 * (i + 1)))
+        return h
+    ws, n = 0x100000, 1 << 40
+    assert B.attn_bwd_host(make(), host(lse=0), ws, n, 1, 2, 3, 2) == -1          # missing host tensor
+    assert B.attn_bwd_host(make(), host(), ws, n, 1, 1, 3, 2) == -1               # streams not distinct
+    assert B.attn_bwd_host(make(), host(), ws, n, 1, 2, 2, 2) == -1
+    assert B.attn_bwd_host(_with_strides(make(), q=(4096 * 3 * 32 * 128, 3 * 32 * 128, 128)), host(),
+                           ws, n, 1, 2, 3, 2) == -1                                # staging must be contiguous
+    assert B.attn_bwd_host(make(), host(), ws, 1024, 1, 2, 3, 2) == -3            # workspace too small
+    assert B.attn_bwd_host(make(d_qk=96, d_v=96), host(), ws, n, 1, 2, 3, 2) == -2
 
 
 def test_padded_starts_only_in_group_mode(lib):
