@@ -330,7 +330,7 @@ def run_ours(args, wl):
         # attn_bwd_host: chunk c's copies overlap its neighbours' compute
         h = B.host_tensors(host["q"], host["k"], host["v"], host["o"], host["do"], host["lse"], *host_out)
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        chunks = e2e_chunks = args.e2e_chunks if args.e2e_chunks > 0 else min(wl.batch, 2)
+        chunks = e2e_chunks = args.e2e_chunks if args.e2e_chunks > 0 else max(1, min(wl.batch, 4))
         for i in range(args.warmup + args.steps):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -390,7 +390,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--e2e-chunks", type=int, default=0,
-                    help="batch chunks of the end-to-end leg (0: min(batch, 2))")
+                    help="chunks of the end-to-end leg (0: min(batch, 4) runs of batch entries)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch of a batch-mode workload")
     ap.add_argument("--atomic", action="store_true", help="same as --dq-mode atomic")
     ap.add_argument("--dq-mode", choices=sorted(DQ_MODES), default=None,

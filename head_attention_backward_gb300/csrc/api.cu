@@ -273,10 +273,36 @@ static bool all_zero(const int64_t x[3]) { return x[0] == 0 && x[1] == 0 && x[2]
 
 static size_t dtype_bytes(int dtype) { return dtype == ATTN_FP32 ? 4 : 2; }
 
-// Chunked host <-> device pipeline of attn_bwd_host: chunk c = batch entries
-// [b0, b1).  Its inputs go up on `in`, its backward runs on `s`, its
-// gradients come down on `out`; events order the three, so the copies of one
-// chunk overlap the compute of its neighbours.
+// One tensor of attn_bwd_host: rows per batch entry (all rows in group mode),
+// heads, head dim, element bytes.
+struct HostTensor {
+  long long rows;
+  int heads, dim;
+  size_t es;
+};
+
+// Copies rows [b0 * rows, b1 * rows) x heads [x0, x1) of a contiguous tensor
+// between host and device: one plain copy when the heads are all of them,
+// else a 2-D copy (one row's head slice per line).
+static bool copy_part(const HostTensor& t, void* dst, const void* src, int b0, int b1, int x0, int x1,
+                      cudaMemcpyKind kind, cudaStream_t st) {
+  const size_t row = (size_t)t.heads * t.dim * t.es;
+  const size_t off = (size_t)b0 * t.rows * row + (size_t)x0 * t.dim * t.es;
+  char* d = static_cast<char*>(dst) + off;
+  const char* s = static_cast<const char*>(src) + off;
+  const size_t nrows = (size_t)(b1 - b0) * t.rows;
+  if (nrows == 0) return true;
+  if (x0 == 0 && x1 == t.heads) return cudaMemcpyAsync(d, s, nrows * row, kind, st) == cudaSuccess;
+  return cudaMemcpy2DAsync(d, row, s, row, (size_t)(x1 - x0) * t.dim * t.es, nrows, kind, st) == cudaSuccess;
+}
+
+// Chunked host <-> device pipeline of attn_bwd_host.  A chunk is a run of
+// batch entries or, once there are more chunks than entries, one entry (or
+// the whole packed tensor in group mode) and a run of kv heads with their
+// query heads; either way its LSE rows are one contiguous block.  Its inputs
+// go up on `in`, its backward runs on `s` (on strided views of the staging
+// buffers), its gradients come down on `out`; events order the three, so the
+// copies of one chunk overlap the compute of its neighbours.
 static int run_host(const attn_bwd_params* p, const attn_host_tensors* h, void* ws, size_t ws_bytes, cudaStream_t s,
                     cudaStream_t in, cudaStream_t out, int chunks) {
   int st = validate_bwd(p);
@@ -292,67 +318,94 @@ static int run_host(const attn_bwd_params* p, const attn_host_tensors* h, void* 
                            {p->stride_dk, p->seqlen_k, p->nhead_kv, p->d_qk}, {p->stride_dv, p->seqlen_k, p->nhead_kv, p->d_v}};
   for (const TensorDesc& x : t) {
     if (all_zero(x.in)) continue;
-    const long long h = x.dim, r = (long long)x.heads * x.dim, b = (long long)x.seqlen * r;
-    if (x.in[1] != r || x.in[2] != h || (!group && p->batch > 1 && x.in[0] != b)) return ATTN_ERR_INVALID_ARG;
+    const long long hs = x.dim, r = (long long)x.heads * x.dim, b = (long long)x.seqlen * r;
+    if (x.in[1] != r || x.in[2] != hs || (!group && p->batch > 1 && x.in[0] != b)) return ATTN_ERR_INVALID_ARG;
   }
   attn_bwd_params e;
   Strides sx[8];
   if ((st = effective_bwd(*p, &e, sx)) != ATTN_OK) return st;
   if (!ws || ws_bytes < ws_layout(e).total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
-  const int nb = group ? 1 : p->batch;
+  // chunk grid: nbg runs of batch entries x nhg runs of kv heads
+  const int nb = group ? 1 : p->batch, G = p->nhead_q / p->nhead_kv;
   if (chunks < 1) chunks = 1;
-  if (chunks > nb) chunks = nb;
+  if (chunks > 64) chunks = 64;
+  int nbg = chunks < nb ? chunks : nb, nhg = 1;
+  if (chunks > nb) {
+    nhg = (chunks + nb - 1) / nb;
+    if (nhg > p->nhead_kv) nhg = p->nhead_kv;
+    if ((long long)nbg * nhg > 64) nhg = 64 / nbg > 0 ? 64 / nbg : 1;
+  }
+  const int nchunks = nbg * nhg;
   const size_t es = dtype_bytes(p->dtype);
-  // bytes per batch entry of each tensor (group mode: the whole tensor, one chunk)
   const long long rq = group ? p->total_q : p->seqlen_q, rk = group ? p->total_k : p->seqlen_k;
-  const size_t bq = (size_t)rq * p->nhead_q * p->d_qk * es, bk = (size_t)rk * p->nhead_kv * p->d_qk * es;
-  const size_t bv = (size_t)rk * p->nhead_kv * p->d_v * es, bo = (size_t)rq * p->nhead_q * p->d_v * es;
-  const size_t bl = (size_t)p->nhead_q * rq * sizeof(float);
+  // q, k, v, o, dout, dq, dk, dv; the kv-side tensors take kv-head ranges
+  const HostTensor ht[8] = {{rq, p->nhead_q, p->d_qk, es},  {rk, p->nhead_kv, p->d_qk, es}, {rk, p->nhead_kv, p->d_v, es},
+                            {rq, p->nhead_q, p->d_v, es},   {rq, p->nhead_q, p->d_v, es},   {rq, p->nhead_q, p->d_qk, es},
+                            {rk, p->nhead_kv, p->d_qk, es}, {rk, p->nhead_kv, p->d_v, es}};
+  const bool kv_side[8] = {false, true, true, false, false, false, true, true};
+  const void* hsrc[5] = {h->q, h->k, h->v, h->o, h->dout};
+  void* hdst[3] = {h->dq, h->dk, h->dv};
+  const void* dptr[8] = {p->q, p->k, p->v, p->o, p->dout, p->dq, p->dk, p->dv};
   cudaEvent_t ev_in[64], ev_c[64], ev_out;
-  chunks = chunks > 64 ? 64 : chunks;
   int made = 0;
-  for (; made < chunks; ++made) {
+  for (; made < nchunks; ++made) {
     if (cudaEventCreateWithFlags(&ev_in[made], cudaEventDisableTiming) != cudaSuccess) break;
     if (cudaEventCreateWithFlags(&ev_c[made], cudaEventDisableTiming) != cudaSuccess) {
       cudaEventDestroy(ev_in[made]);
       break;
     }
   }
-  const bool have_out = made == chunks && cudaEventCreateWithFlags(&ev_out, cudaEventDisableTiming) == cudaSuccess;
+  const bool have_out = made == nchunks && cudaEventCreateWithFlags(&ev_out, cudaEventDisableTiming) == cudaSuccess;
   bool ok = have_out;
-  // the caller's earlier work on `s` (which may have produced the inputs' staging
-  // buffers' previous users) comes before the first copy
+  // the caller's earlier work on `s` comes before the first copy
   if (ok) ok = cudaEventRecord(ev_c[0], s) == cudaSuccess && cudaStreamWaitEvent(in, ev_c[0], 0) == cudaSuccess &&
                cudaStreamWaitEvent(out, ev_c[0], 0) == cudaSuccess;
-  for (int c = 0; ok && c < chunks; ++c) {
-    const int b0 = (int)((long long)nb * c / chunks), b1 = (int)((long long)nb * (c + 1) / chunks);
-    const size_t n = (size_t)(b1 - b0);
-    auto dev = [&](const void* base, size_t per) { return static_cast<char*>(const_cast<void*>(base)) + b0 * per; };
-    auto hst = [&](const void* base, size_t per) { return static_cast<const char*>(base) + b0 * per; };
-    const void* srcs[6] = {h->q, h->k, h->v, h->o, h->dout, h->lse};
-    const void* dsts[6] = {p->q, p->k, p->v, p->o, p->dout, p->lse};
-    const size_t per[6] = {bq, bk, bv, bo, bo, bl};
-    for (int i = 0; ok && i < 6; ++i)
-      ok = cudaMemcpyAsync(dev(dsts[i], per[i]), hst(srcs[i], per[i]), n * per[i], cudaMemcpyHostToDevice, in) ==
-           cudaSuccess;
+  for (int c = 0; ok && c < nchunks; ++c) {
+    const int bg = c / nhg, hg = c % nhg;
+    const int b0 = (int)((long long)nb * bg / nbg), b1 = (int)((long long)nb * (bg + 1) / nbg);
+    const int k0 = (int)((long long)p->nhead_kv * hg / nhg), k1 = (int)((long long)p->nhead_kv * (hg + 1) / nhg);
+    const int q0 = k0 * G, q1 = k1 * G;
+    auto heads = [&](int i, int& x0, int& x1) { x0 = kv_side[i] ? k0 : q0; x1 = kv_side[i] ? k1 : q1; };
+    for (int i = 0; ok && i < 5; ++i) {
+      int x0, x1;
+      heads(i, x0, x1);
+      ok = copy_part(ht[i], const_cast<void*>(dptr[i]), hsrc[i], b0, b1, x0, x1, cudaMemcpyHostToDevice, in);
+    }
+    // LSE rows of the chunk: [b0, b1) x [q0, q1) x rows, one block (either the
+    // heads are all of them or the chunk has one batch entry)
+    const size_t lse_off = ((size_t)b0 * p->nhead_q + q0) * rq;
+    const size_t lse_n = (size_t)(b1 - b0) * (q1 - q0) * rq;
+    ok = ok && cudaMemcpyAsync(const_cast<float*>(p->lse) + lse_off, h->lse + lse_off, lse_n * sizeof(float),
+                               cudaMemcpyHostToDevice, in) == cudaSuccess;
     ok = ok && cudaEventRecord(ev_in[c], in) == cudaSuccess && cudaStreamWaitEvent(s, ev_in[c], 0) == cudaSuccess;
     if (!ok) break;
     attn_bwd_params part = *p;
-    if (!group) {
-      part.batch = (int)n;
-      part.q = dev(p->q, bq); part.k = dev(p->k, bk); part.v = dev(p->v, bv);
-      part.o = dev(p->o, bo); part.dout = dev(p->dout, bo);
-      part.lse = reinterpret_cast<const float*>(dev(p->lse, bl));
-      part.dq = dev(p->dq, bq); part.dk = dev(p->dk, bk); part.dv = dev(p->dv, bv);
+    if (!group) part.batch = b1 - b0;
+    part.nhead_q = q1 - q0;
+    part.nhead_kv = k1 - k0;
+    void* views[8];
+    for (int i = 0; i < 8; ++i) {
+      int x0, x1;
+      heads(i, x0, x1);
+      const HostTensor& x = ht[i];
+      views[i] = static_cast<char*>(const_cast<void*>(dptr[i])) +
+                 ((size_t)b0 * x.rows * x.heads + x0) * x.dim * x.es;
+      int64_t* sd[8] = {part.stride_q, part.stride_k, part.stride_v, part.stride_o,
+                        part.stride_dout, part.stride_dq, part.stride_dk, part.stride_dv};
+      sd[i][0] = (int64_t)x.rows * x.heads * x.dim;
+      sd[i][1] = (int64_t)x.heads * x.dim;
+      sd[i][2] = x.dim;
     }
+    part.q = views[0]; part.k = views[1]; part.v = views[2]; part.o = views[3]; part.dout = views[4];
+    part.dq = views[5]; part.dk = views[6]; part.dv = views[7];
+    part.lse = p->lse + lse_off;
     if ((st = run(&part, ws, ws_bytes, s, nullptr, c > 0)) != ATTN_OK) break;
     ok = cudaEventRecord(ev_c[c], s) == cudaSuccess && cudaStreamWaitEvent(out, ev_c[c], 0) == cudaSuccess;
-    void* hd[3] = {h->dq, h->dk, h->dv};
-    const void* dd[3] = {p->dq, p->dk, p->dv};
-    const size_t pg[3] = {bq, bk, bv};
-    for (int i = 0; ok && i < 3; ++i)
-      ok = cudaMemcpyAsync(static_cast<char*>(hd[i]) + b0 * pg[i], dev(dd[i], pg[i]), n * pg[i],
-                           cudaMemcpyDeviceToHost, out) == cudaSuccess;
+    for (int i = 0; ok && i < 3; ++i) {
+      int x0, x1;
+      heads(5 + i, x0, x1);
+      ok = copy_part(ht[5 + i], hdst[i], dptr[5 + i], b0, b1, x0, x1, cudaMemcpyDeviceToHost, out);
+    }
   }
   // `s` completes only after the last gradients are back on the host
   if (ok && st == ATTN_OK)

@@ -259,11 +259,14 @@ typedef struct {
  * LSE from `host` into the device buffers of *p, runs the backward pass and
  * copies dQ, dK, dV back into `host`.  *p is an ordinary attn_bwd problem whose
  * tensor pointers are the caller's contiguous device staging buffers (all
- * strides zero).  In batch mode the batch is split into `chunks` runs of
- * consecutive entries (clamped to [1, batch]; group mode runs one chunk):
- * chunk c's inputs are copied on `copy_in`, its backward runs on `stream`,
- * its gradients are copied on `copy_out`, so one chunk's copies overlap
- * another chunk's compute.  The three streams must be distinct; the copies
+ * strides zero).  The problem is split into at most `chunks` (1..64) parts:
+ * runs of consecutive batch entries while chunks <= batch, else single
+ * entries (group mode: the whole packed tensor) times runs of kv heads with
+ * their query heads, whose head slices travel as 2-D copies (one line per
+ * row; on a GB300 these run far below the plain copies' ~200 GB/s, so
+ * chunks <= batch is the fast choice).  Chunk c's inputs are copied on
+ * `copy_in`, its backward runs on `stream`, its gradients are copied on
+ * `copy_out`, so one chunk's copies overlap another chunk's compute.  The three streams must be distinct; the copies
  * start after the work already queued on `stream`, and `stream` completes
  * only once the last gradients are in host memory (synchronise it before
  * reading them).  Each chunk runs the same kernels in the same order as

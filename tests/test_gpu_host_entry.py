@@ -26,6 +26,8 @@ def _case(wl):
     x = wl.inputs()
     cu, cuk = wl.cu_seqlens(), wl.cu_seqlens_k()
     kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cuk)
+    if wl.gaps_q or wl.gaps_k:
+        kw.update(cu_seqlens_q_padded=wl.cu_seqlens_q_padded(), cu_seqlens_k_padded=wl.cu_seqlens_k_padded())
     o, lse = R.attn_forward(x["q"], x["k"], x["v"], wl.scale, **kw)
     x["o"], x["lse"] = o.to(wl.dtype), lse.to(torch.float32)
     return x, kw
@@ -65,6 +67,8 @@ CASES = [
     W.Workload("gqa_b3_causal", torch.bfloat16, 3, 4, 2, 300, 300, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=71),
     W.Workload("mha_b4_window_d64", torch.bfloat16, 4, 2, 2, 257, 257, 64, 64, W.MASK_WINDOW, 40, 0, seed=72),
     W.thd("thd", [100, 0, 37, 250, 5], hq=4, hkv=2, seed=73),
+    W.thd("thd_cross_padded", [100, 0, 37], hq=6, hkv=3, mask=W.MASK_CAUSAL_BOTTOM_RIGHT, seed=74,
+          seqlens_k=[300, 64, 0], gaps_q=[3, 0, 17, 5], gaps_k=[0, 5, 131, 2]),
 ]
 
 
@@ -73,6 +77,7 @@ CASES = [
 def test_host_entry_bitwise_equal_to_device_call(B, wl, det):
     x, kw = _case(wl)
     ref = _device_run(B, wl, x, kw, det)
+    # chunks beyond the batch split the kv heads too (2-D copies of head slices)
     for chunks in (1, 2, 3, 8):
         got = _host_run(B, wl, x, kw, det, chunks)
         for name, g, r in zip(("dq", "dk", "dv"), got, ref):
