@@ -237,6 +237,10 @@ static void log_config(const attn_bwd_params& p, const WsLayout& L) {
                p.softmax_scale, p.deterministic, L.nsplits, L.max_items, L.total);
 }
 
+// Tensor-core forward (fwd_tc.cu); ATTN_ERR_UNSUPPORTED_HEADDIM for the
+// dtypes and head dims it is not built for.
+int launch_fwd_tc(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st);
+
 // Schedule launch for one part of a call split into parts (attn_bwd_host):
 // parts after the first keep the status the earlier parts left.
 void launch_schedule_part(const Problem& P, cudaStream_t st, bool keep_status);
@@ -484,7 +488,9 @@ extern "C" int attn_fwd(const attn_fwd_params* p, cudaStream_t stream) {
   FwdLayout L;
   const int s2 = effective_fwd(*p, &e, &L);
   if (s2 != ATTN_OK) return s2;
-  launch_fwd(e, L, stream);
+  const int s3 = launch_fwd_tc(e, L, stream);
+  if (s3 == ATTN_ERR_UNSUPPORTED_HEADDIM) launch_fwd(e, L, stream);   // fp32, other head dims
+  else if (s3 != ATTN_OK) return s3;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -1,0 +1,473 @@
+// Forward FMHA on tcgen05 tensor cores (sm_103a): O = softmax(s Q K^T) V and
+// the natural-log LSE, for 16-bit inputs with (d_qk, d_v) in {(64, 64),
+// (128, 128), (192, 128)}.  It produces the O and LSE the backward pass takes
+// (the forward implied by ck_attn_fwd in TransformerEngine PR #446); fp32
+// inputs and other head dims keep the CUDA-core forward in simt_kernels.cu.
+//
+// One CTA per (128-row query tile, query head, batch entry / segment); the
+// query rows sit on the 128 TMEM lanes.  Per KV tile of 128 keys:
+//
+//   S  = Q K^T                 (M = queries, N = keys, K = d_qk)   SMEM x SMEM
+//   P  = exp2(s log2(e) S - m) (CUDA cores, online row max m and sum l)
+//   O += P V                   (M = queries, N = d_v,  K = keys)   TMEM x SMEM
+//
+// S is double-buffered in TMEM, so S of the next tile is computed while the
+// softmax warps work on this one; K and V come in by TMA, two stages deep.
+// The running max is only moved (and O rescaled in TMEM) when a row's max
+// grows by more than 2^8, so that P = exp2(x - m) <= 256 stays exact enough
+// in 16 bits and most tiles skip the rescale.  At the end O / l goes to
+// global memory and LSE = (m + log2 l) ln 2.
+//
+// Warp roles (192 threads): warp 0 lane 0 loads (TMA), warp 1 allocates TMEM
+// and its lane 0 issues the MMAs, warps 2-5 run the softmax and the epilogue
+// (one query row per thread).  Every wait is bounded by %globaltimer; a CTA
+// whose wait expires writes NaN into its rows' LSE instead of a result.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace fwdtc {
+
+using namespace ptx;
+
+constexpr int FM = 128;                  // query rows per CTA
+constexpr int FN = 128;                  // keys per KV tile
+constexpr int NUM_SM_WARPS = 4;          // softmax / epilogue warps
+constexpr int FIRST_SM_WARP = 2;
+constexpr int NTHREADS = 32 * (FIRST_SM_WARP + NUM_SM_WARPS);
+constexpr int STAGES = 2;                // K/V pipeline depth
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint32_t SLEEP_HINT_NS = 20000;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.f;      // move the running max only past this growth
+
+template <int DQK, int DV>
+struct FCfg {
+  static constexpr int NCK = DQK / 64;
+  static constexpr int NCV = DV / 64;
+  static constexpr int CH = 128 * 128;                    // one 64-wide chunk of 128 rows
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + NCK * CH;
+  static constexpr int STAGE = (NCK + NCV) * CH;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * STAGE;
+  static constexpr int NBAR = 16;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
+  static constexpr uint32_t Q_BYTES = NCK * CH;
+  static constexpr uint32_t KV_BYTES = (NCK + NCV) * CH;
+  // TMEM columns: two S buffers, O, P (bf16/fp16 pairs, the A operand of P V)
+  static constexpr int T_S = 0;
+  static constexpr int T_O = 2 * FN;
+  static constexpr int T_P = T_O + 128;
+  static_assert(T_P + FN / 2 <= (int)TMEM_COLS, "TMEM overflow");
+  static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+};
+
+enum {
+  B_Q_FULL = 0, B_KV_FULL = 1, B_KV_EMPTY = B_KV_FULL + STAGES, B_S_FULL = B_KV_EMPTY + STAGES,
+  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2, B_PV_DONE, B_DRAIN
+};
+
+struct Maps {
+  CUtensorMap q, k, v;
+};
+
+struct Args {
+  int group, hq, g, sq, sk;
+  const int* cu_q;
+  const int* cu_k;
+  const int* st_q;
+  const int* st_k;
+  int mask, left, right;
+  float scale_log2;
+  void* o;
+  Strides so;
+  float* lse;
+  int tq;                  // group mode: LSE row stride (rows of q)
+};
+
+struct Ctx {
+  uint64_t* bar;
+  int* abort_flag;
+};
+
+__device__ __noinline__ bool wait_expired(const Ctx& c, uint64_t t0) {
+  if (*(volatile int*)c.abort_flag) return true;
+  if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+    *(volatile int*)c.abort_flag = 1;
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
+  const uint32_t a = smem_u32(c.bar + idx);
+  if (mbar_test_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait_sleep(a, parity, SLEEP_HINT_NS))
+    if (wait_expired(c, t0)) return false;
+  return true;
+}
+
+// The same wait for all lanes of a warp, with one outcome for all of them
+// (the tensor-memory loads and stores that follow are warp-collective).
+__device__ __forceinline__ bool wait_bar_warp(const Ctx& c, int idx, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_bar(c, idx, parity));
+}
+
+template <typename T> struct IsHalf { static constexpr bool value = false; };
+template <> struct IsHalf<__half> { static constexpr bool value = true; };
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16*) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int DQK, int DV, typename T>
+__global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_constant__ Maps maps, const Args A) {
+  using C = FCfg<DQK, DV>;
+  const int qt = gridDim.x - 1 - blockIdx.x;   // the longest causal tiles first
+  const int h = blockIdx.y, b = blockIdx.z, hk = h / A.g;
+  int q0, lq, k0, lk;
+  if (A.group) {
+    lq = __ldg(A.cu_q + b + 1) - __ldg(A.cu_q + b);
+    lk = __ldg(A.cu_k + b + 1) - __ldg(A.cu_k + b);
+    q0 = __ldg(A.st_q + b);
+    k0 = __ldg(A.st_k + b);
+  } else {
+    q0 = b * A.sq; lq = A.sq; k0 = b * A.sk; lk = A.sk;
+  }
+  const int qs = qt * FM;
+  if (qs >= lq) return;
+  // KV tiles any row of this query tile can see
+  const MaskArgs m = mask_args(A.mask, A.left, A.right, lq, lk);
+  const int qe = min(qs + FM, lq) - 1;
+  int klo = 0, khi = lk - 1;
+  if (m.left >= 0) klo = max(klo, qs + m.off - m.left);
+  if (m.right >= 0) khi = min(khi, qe + m.off + m.right);
+  const int kt0 = klo / FN;
+  const int nkv = (lk > 0 && khi >= klo) ? khi / FN - kt0 + 1 : 0;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Ctx ctx{bar, abort_flag};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar + B_Q_FULL, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar + B_KV_FULL + s, 1);
+      mbar_init(bar + B_KV_EMPTY + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar + B_S_FULL + s, 1);
+      mbar_init(bar + B_S_EMPTY + s, NUM_SM_WARPS);
+    }
+    mbar_init(bar + B_P_FULL, NUM_SM_WARPS);
+    mbar_init(bar + B_PV_DONE, 1);
+    mbar_init(bar + B_DRAIN, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      mbar_arrive_expect_tx(bar + B_Q_FULL, C::Q_BYTES);
+      for (int c = 0; c < C::NCK; ++c)
+        tma_load_3d(smem + C::OFF_Q + c * C::CH, &maps.q, bar + B_Q_FULL, c * 64, h, q0 + qs);
+      int j = 0;
+      for (; j < nkv; ++j) {
+        const int s = j % STAGES;
+        if (!wait_bar(ctx, B_KV_EMPTY + s, ((j / STAGES) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(bar + B_KV_FULL + s, C::KV_BYTES);
+        const int krow = k0 + (kt0 + j) * FN;
+        uint8_t* kv = smem + C::OFF_KV + s * C::STAGE;
+        for (int c = 0; c < C::NCK; ++c) tma_load_3d(kv + c * C::CH, &maps.k, bar + B_KV_FULL + s, c * 64, hk, krow);
+        for (int c = 0; c < C::NCV; ++c)
+          tma_load_3d(kv + (C::NCK + c) * C::CH, &maps.v, bar + B_KV_FULL + s, c * 64, hk, krow);
+      }
+      // no copy may still be writing this CTA's shared memory when it exits
+      wait_bar(ctx, B_Q_FULL, 0);
+      for (int i = j - 1; i >= 0 && i >= j - STAGES; --i) wait_bar(ctx, B_KV_FULL + i % STAGES, (i / STAGES) & 1);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr bool F16 = IsHalf<T>::value;
+      constexpr uint32_t ID_S = idesc_f16(FM, FN, false, false, F16);
+      constexpr uint32_t ID_PV = idesc_f16(FM, DV, false, true, F16);
+      const uint64_t dQ = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);        // K-major
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);       // K-major, stage 0
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + C::OFF_KV + C::NCK * C::CH), C::CH, 1024);   // MN-major
+      bool ok = wait_bar(ctx, B_Q_FULL, 0);
+      auto issue_pv = [&](int j) -> bool {
+        if (!wait_bar(ctx, B_P_FULL, j & 1)) return false;
+        tc_fence_after();
+        const uint64_t v = dV + (((j % STAGES) * C::STAGE) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < FN / 16; ++ks)
+          umma_ts(tmem + C::T_O, tmem + C::T_P + ks * 8, v + ((ks * 2048) >> 4), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(bar + B_PV_DONE);
+        umma_commit(bar + B_KV_EMPTY + j % STAGES);
+        return true;
+      };
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int s = j % STAGES, sb = j & 1;
+        if (!(ok = wait_bar(ctx, B_KV_FULL + s, (j / STAGES) & 1))) break;
+        if (!(ok = wait_bar(ctx, B_S_EMPTY + sb, ((j >> 1) & 1) ^ 1))) break;
+        tc_fence_after();
+        const uint64_t k = dK + ((s * C::STAGE) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < DQK / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::CH + (ks & 3) * 32;
+          umma_ss(tmem + C::T_S + sb * FN, dQ + (off >> 4), k + (off >> 4), ID_S, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(bar + B_S_FULL + sb);
+        // O += P V of the previous tile runs behind this tile's S
+        if (j > 0 && !(ok = issue_pv(j - 1))) break;
+      }
+      if (ok && nkv > 0) issue_pv(nkv - 1);
+      // no MMA of this CTA may be in flight when TMEM is released
+      umma_commit(bar + B_DRAIN);
+      wait_bar(ctx, B_DRAIN, 0);
+    }
+  } else {
+    // ----------------------------------------------- softmax and epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                 // query row = TMEM lane
+    const int qi = qs + r;
+    const bool row_ok = qi < lq;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    float mx = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      if (!(ok = wait_bar_warp(ctx, B_S_FULL + sb, (j >> 1) & 1))) break;
+      tc_fence_after();
+      uint32_t sv[FN];
+#pragma unroll
+      for (int c = 0; c < FN / 32; ++c)
+        tmem_ld32(lane_addr + C::T_S + sb * FN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + B_S_EMPTY + sb);
+      // scaled scores in log2 units; masked keys -inf
+      const int kb = (kt0 + j) * FN;
+      const bool full = kb + FN <= lk && (m.right < 0 || kb + FN - 1 <= qs + m.off + m.right) &&
+                        (m.left < 0 || kb >= qe + m.off - m.left);
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < FN; ++c) {
+        float x = __uint_as_float(sv[c]) * A.scale_log2;
+        if (!full) x = (kb + c < lk && visible(m, qi, kb + c)) ? x : -INFINITY;
+        sv[c] = __float_as_uint(x);
+        tmax = fmaxf(tmax, x);
+      }
+      // move the running max only when it grows past the threshold
+      float alpha = 1.f;
+      bool rescale = false;
+      if (tmax > mx + RESCALE_LOG2) {
+        alpha = fast_exp2(mx - tmax);      // 0 when mx = -inf
+        rescale = j > 0;
+        mx = tmax;
+      }
+      const float mref = mx == -INFINITY ? 0.f : mx;
+      float sum = 0.f;
+      uint32_t pk[FN / 2];
+#pragma unroll
+      for (int c = 0; c < FN; c += 2) {
+        const float p0 = fast_exp2(__uint_as_float(sv[c]) - mref), p1 = fast_exp2(__uint_as_float(sv[c + 1]) - mref);
+        sum += p0 + p1;
+        pk[c >> 1] = pack2(p0, p1, (T*)nullptr);
+      }
+      l = l * alpha + sum;
+      // O and the P buffer are free once the previous tile's O += P V is done
+      if (j > 0) {
+        if (!(ok = wait_bar_warp(ctx, B_PV_DONE, (j - 1) & 1))) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + C::T_O + c * 32, o);
+          tmem_wait_ld();
+          uint32_t lo[16], hi[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            lo[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            hi[i] = __float_as_uint(__uint_as_float(o[16 + i]) * alpha);
+          }
+          tmem_st16(lane_addr + C::T_O + c * 32, lo);
+          tmem_st16(lane_addr + C::T_O + c * 32 + 16, hi);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < FN / 32; ++c)
+        tmem_st16(lane_addr + C::T_P + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + c * 16));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + B_P_FULL);
+    }
+    // epilogue: O / l and the LSE of this thread's row
+    if (ok && nkv > 0) {
+      ok = wait_bar_warp(ctx, B_PV_DONE, (nkv - 1) & 1);
+      tc_fence_after();
+    }
+    const long long li = A.group ? (long long)h * A.tq + q0 + qi : ((long long)b * A.hq + h) * A.sq + qi;
+    T* orow = static_cast<T*>(A.o) + elem_off(A.so, (long long)q0 + qi, h);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < DV / 32; ++c) {
+      uint32_t o[32];
+      if (ok && nkv > 0) {
+        tmem_ld32(lane_addr + C::T_O + c * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      if (row_ok && ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv, (T*)nullptr);
+          w.y = pack2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv, (T*)nullptr);
+          w.z = pack2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv, (T*)nullptr);
+          w.w = pack2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv, (T*)nullptr);
+          dst[v] = w;
+        }
+      }
+    }
+    if (row_ok) A.lse[li] = !ok ? __int_as_float(0x7fc00000) : l > 0.f ? (mx + log2f(l)) * 0.6931471805599453f
+                                                                        : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D view (dim, heads, rows) of a 16-bit tensor with element strides x;
+// boxes of 64 x 1 x 128 rows with 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, bool fp16, int dim, int heads, long long rows,
+                     const Strides& x) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)x.h * 2, (cuuint64_t)x.r * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int DQK, int DV, typename T>
+static int launch_typed(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
+  using C = FCfg<DQK, DV>;
+  const bool group = p.cu_seqlens_q != nullptr;
+  const bool fp16 = IsHalf<T>::value;
+  const long long rq = group ? p.total_q : (long long)p.batch * p.seqlen_q;
+  const long long rk = group ? p.total_k : (long long)p.batch * p.seqlen_k;
+  Maps maps;
+  if (!make_map(&maps.q, p.q, fp16, DQK, p.nhead_q, rq, L.q) || !make_map(&maps.k, p.k, fp16, DQK, p.nhead_kv, rk, L.k) ||
+      !make_map(&maps.v, p.v, fp16, DV, p.nhead_kv, rk, L.v))
+    return ATTN_ERR_CUDA;
+  Args a;
+  a.group = group ? 1 : 0;
+  a.hq = p.nhead_q;
+  a.g = p.nhead_q / p.nhead_kv;
+  a.sq = p.seqlen_q;
+  a.sk = p.seqlen_k;
+  a.cu_q = p.cu_seqlens_q;
+  a.cu_k = p.cu_seqlens_k;
+  a.st_q = p.cu_seqlens_q_padded ? p.cu_seqlens_q_padded : p.cu_seqlens_q;
+  a.st_k = p.cu_seqlens_k_padded ? p.cu_seqlens_k_padded : p.cu_seqlens_k;
+  a.mask = p.mask;
+  a.left = p.mask == ATTN_MASK_WINDOW ? p.window_left : -1;
+  a.right = p.mask == ATTN_MASK_WINDOW ? p.window_right : -1;
+  a.scale_log2 = p.softmax_scale * 1.4426950408889634f;
+  a.o = p.o;
+  a.so = L.o;
+  a.lse = p.lse;
+  a.tq = group ? p.total_q : 0;
+  const int ntq = cdiv(p.seqlen_q > 0 ? p.seqlen_q : 1, FM);
+  auto kern = fwd_tc_kernel<DQK, DV, T>;
+  // more than half the shared memory, so that two CTAs (each holding all
+  // TMEM columns) never share an SM
+  const int smem = C::SMEM_BYTES > 120 * 1024 ? C::SMEM_BYTES : 120 * 1024;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  kern<<<dim3(ntq, p.nhead_q, p.batch), NTHREADS, smem, st>>>(maps, a);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <typename T>
+static int launch_dims(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
+  if (p.d_qk == 128 && p.d_v == 128) return launch_typed<128, 128, T>(p, L, st);
+  if (p.d_qk == 64 && p.d_v == 64) return launch_typed<64, 64, T>(p, L, st);
+  if (p.d_qk == 192 && p.d_v == 128) return launch_typed<192, 128, T>(p, L, st);
+  return ATTN_ERR_UNSUPPORTED_HEADDIM;
+}
+
+}  // namespace fwdtc
+
+// Tensor-core forward for the 16-bit head-dim pairs it is built for;
+// ATTN_ERR_UNSUPPORTED_HEADDIM otherwise (the caller then runs the CUDA-core
+// forward).
+int launch_fwd_tc(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
+  if (p.dtype == ATTN_BF16) return fwdtc::launch_dims<__nv_bfloat16>(p, L, st);
+  if (p.dtype == ATTN_FP16) return fwdtc::launch_dims<__half>(p, L, st);
+  return ATTN_ERR_UNSUPPORTED_HEADDIM;
+}
+
+}  // namespace attn

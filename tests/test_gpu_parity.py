@@ -254,8 +254,9 @@ def test_thd_window_and_d192(B):
 def test_forward_helper_matches_oracle(B):
     cross = W.thd("t_cross_padded", PAD_Q, hq=4, hkv=2, mask=W.MASK_CAUSAL_BOTTOM_RIGHT, seed=4,
                   seqlens_k=PAD_K, gaps_q=PADDED[0]["gaps_q"], gaps_k=PADDED[0]["gaps_k"])
-    for wl in (SMALL[0], SMALL[2], SMALL[3], SMALL[8], SMALL[11], W.thd("t", [100, 80, 76], hq=4, hkv=2, seed=3),
-               cross):
+    # SMALL[0] (fp32) runs the CUDA-core forward, the 16-bit cases the tensor-core one
+    for wl in (SMALL[0], SMALL[2], SMALL[3], SMALL[4], SMALL[6], SMALL[8], SMALL[9], SMALL[10], SMALL[11], SMALL[12],
+               W.thd("t", [100, 80, 76], hq=4, hkv=2, seed=3), cross):
         x = wl.inputs()
         kw = dict(mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=wl.cu_seqlens(),
                   cu_seqlens_k=wl.cu_seqlens_k())
