@@ -18,9 +18,9 @@
 // in 16 bits and most tiles skip the rescale.  At the end O / l goes to
 // global memory and LSE = (m + log2 l) ln 2.
 //
-// Warp roles (192 threads): warp 0 lane 0 loads (TMA), warp 1 allocates TMEM
-// and its lane 0 issues the MMAs, warps 2-5 run the softmax and the epilogue
-// (one query row per thread).  Every wait is bounded by %globaltimer; a CTA
+// Warp roles (320 threads): warp 0 lane 0 loads (TMA), warp 1 allocates TMEM
+// and its lane 0 issues the MMAs, warps 2-9 run the softmax and the epilogue
+// (two warps per query row block, 64 key columns each).  Every wait is bounded by %globaltimer; a CTA
 // whose wait expires writes NaN into its rows' LSE instead of a result.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -37,7 +37,8 @@ using namespace ptx;
 
 constexpr int FM = 128;                  // query rows per CTA
 constexpr int FN = 128;                  // keys per KV tile
-constexpr int NUM_SM_WARPS = 4;          // softmax / epilogue warps
+constexpr int NUM_SM_WARPS = 8;          // softmax / epilogue warps: two per TMEM lane quarter
+constexpr int SM_COLS = FN / 2;          // key columns of one softmax warp
 constexpr int FIRST_SM_WARP = 2;
 constexpr int NTHREADS = 32 * (FIRST_SM_WARP + NUM_SM_WARPS);
 constexpr int STAGES = 2;                // K/V pipeline depth
@@ -55,9 +56,10 @@ struct FCfg {
   static constexpr int OFF_KV = OFF_Q + NCK * CH;
   static constexpr int STAGE = (NCK + NCV) * CH;
   static constexpr int OFF_BAR = OFF_KV + STAGES * STAGE;
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
+  static constexpr int OFF_RED = OFF_MISC + 64;            // [3 slots][2 halves][128 rows] fp32
+  static constexpr int SMEM_BYTES = OFF_RED + 3 * 2 * 128 * 4 + 1024;   // + alignment slack
   static constexpr uint32_t Q_BYTES = NCK * CH;
   static constexpr uint32_t KV_BYTES = (NCK + NCV) * CH;
   // TMEM columns: two S buffers, O, P (bf16/fp16 pairs, the A operand of P V)
@@ -70,7 +72,10 @@ struct FCfg {
 
 enum {
   B_Q_FULL = 0, B_KV_FULL = 1, B_KV_EMPTY = B_KV_FULL + STAGES, B_S_FULL = B_KV_EMPTY + STAGES,
-  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2, B_PV_DONE, B_DRAIN
+  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2, B_PV_DONE, B_DRAIN,
+  // the two warps of a row block exchange row maxima per tile ([quarter][tile parity])
+  // and row sums at the end ([quarter]); two lane-0 arrivals each
+  B_RED, B_EPI = B_RED + 8, B_END = B_EPI + 4
 };
 
 struct Maps {
@@ -179,6 +184,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     mbar_init(bar + B_P_FULL, NUM_SM_WARPS);
     mbar_init(bar + B_PV_DONE, 1);
     mbar_init(bar + B_DRAIN, 1);
+    for (int i = B_RED; i < B_END; ++i) mbar_init(bar + i, 2);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -257,38 +263,63 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     }
   } else {
     // ----------------------------------------------- softmax and epilogue
+    // Warps w and w + 4 share the TMEM lanes of quarter w & 3 (query rows)
+    // and take key columns [0, 64) and [64, 128) of each tile; they agree on
+    // each row's max through shared memory, handing it over with an mbarrier
+    // (a bounded wait, like every other wait of the kernel).
     const int quarter = warp & 3;
+    const int half = (warp - FIRST_SM_WARP) >> 2;
     const int r = quarter * 32 + lane;                 // query row = TMEM lane
     const int qi = qs + r;
     const bool row_ok = qi < lq;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    float* red = reinterpret_cast<float*>(smem + C::OFF_RED);   // [slot][half][row]
+    // this warp's value of row r for the partner warp: write, arrive, wait
+    auto exchange = [&](float v, int slot, int b_idx, uint32_t parity, float& other) -> bool {
+      red[(slot * 2 + half) * 128 + r] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + b_idx);
+      if (!wait_bar_warp(ctx, b_idx, parity)) return false;
+      other = red[(slot * 2 + (half ^ 1)) * 128 + r];
+      return true;
+    };
+    constexpr int OC = DV / 2;                         // O columns of this warp
     float mx = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int sb = j & 1;
       if (!(ok = wait_bar_warp(ctx, B_S_FULL + sb, (j >> 1) & 1))) break;
       tc_fence_after();
-      uint32_t sv[FN];
+      uint32_t sv[SM_COLS];
 #pragma unroll
-      for (int c = 0; c < FN / 32; ++c)
-        tmem_ld32(lane_addr + C::T_S + sb * FN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+      for (int c = 0; c < SM_COLS / 32; ++c)
+        tmem_ld32(lane_addr + C::T_S + sb * FN + half * SM_COLS + c * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar + B_S_EMPTY + sb);
-      // scaled scores in log2 units; masked keys -inf
-      const int kb = (kt0 + j) * FN;
-      const bool full = kb + FN <= lk && (m.right < 0 || kb + FN - 1 <= qs + m.off + m.right) &&
+      // scaled scores in log2 units (masked keys -inf) and their max, with
+      // independent partial maxima to keep the dependency chains short
+      const int kb = (kt0 + j) * FN + half * SM_COLS;
+      const bool full = kb + SM_COLS <= lk && (m.right < 0 || kb + SM_COLS - 1 <= qs + m.off + m.right) &&
                         (m.left < 0 || kb >= qe + m.off - m.left);
-      float tmax = -INFINITY;
+      float pm[8];
 #pragma unroll
-      for (int c = 0; c < FN; ++c) {
+      for (int i = 0; i < 8; ++i) pm[i] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < SM_COLS; ++c) {
         float x = __uint_as_float(sv[c]) * A.scale_log2;
         if (!full) x = (kb + c < lk && visible(m, qi, kb + c)) ? x : -INFINITY;
         sv[c] = __float_as_uint(x);
-        tmax = fmaxf(tmax, x);
+        pm[c & 7] = fmaxf(pm[c & 7], x);
       }
-      // move the running max only when it grows past the threshold
+      float tmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      float omax;
+      if (!(ok = exchange(tmax, sb, B_RED + quarter * 2 + sb, (j >> 1) & 1, omax))) break;
+      tmax = fmaxf(tmax, omax);
+      // move the running max only when it grows past the threshold (both
+      // warps of the pair see the same values and decide the same way)
       float alpha = 1.f;
       bool rescale = false;
       if (tmax > mx + RESCALE_LOG2) {
@@ -297,15 +328,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         mx = tmax;
       }
       const float mref = mx == -INFINITY ? 0.f : mx;
-      float sum = 0.f;
-      uint32_t pk[FN / 2];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[SM_COLS / 2];
 #pragma unroll
-      for (int c = 0; c < FN; c += 2) {
+      for (int c = 0; c < SM_COLS; c += 2) {
         const float p0 = fast_exp2(__uint_as_float(sv[c]) - mref), p1 = fast_exp2(__uint_as_float(sv[c + 1]) - mref);
-        sum += p0 + p1;
+        ps[(c >> 1) & 3] += p0 + p1;
         pk[c >> 1] = pack2(p0, p1, (T*)nullptr);
       }
-      l = l * alpha + sum;
+      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       // O and the P buffer are free once the previous tile's O += P V is done
       if (j > 0) {
         if (!(ok = wait_bar_warp(ctx, B_PV_DONE, (j - 1) & 1))) break;
@@ -313,9 +344,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       }
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
+        for (int c = 0; c < OC / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + C::T_O + c * 32, o);
+          const uint32_t col = lane_addr + C::T_O + half * OC + c * 32;
+          tmem_ld32(col, o);
           tmem_wait_ld();
           uint32_t lo[16], hi[16];
 #pragma unroll
@@ -323,31 +355,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             lo[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             hi[i] = __float_as_uint(__uint_as_float(o[16 + i]) * alpha);
           }
-          tmem_st16(lane_addr + C::T_O + c * 32, lo);
-          tmem_st16(lane_addr + C::T_O + c * 32 + 16, hi);
+          tmem_st16(col, lo);
+          tmem_st16(col + 16, hi);
         }
       }
 #pragma unroll
-      for (int c = 0; c < FN / 32; ++c)
-        tmem_st16(lane_addr + C::T_P + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + c * 16));
+      for (int c = 0; c < SM_COLS / 32; ++c)
+        tmem_st16(lane_addr + C::T_P + half * (SM_COLS / 2) + c * 16,
+                  *reinterpret_cast<const uint32_t(*)[16]>(pk + c * 16));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar + B_P_FULL);
     }
-    // epilogue: O / l and the LSE of this thread's row
+    // epilogue: the row's sum over both halves, O / l (each warp its half of
+    // the columns) and the LSE
+    ok = __all_sync(0xffffffffu, ok);
     if (ok && nkv > 0) {
       ok = wait_bar_warp(ctx, B_PV_DONE, (nkv - 1) & 1);
       tc_fence_after();
     }
+    float lo_other = 0.f;
+    if (ok) ok = exchange(l, 2, B_EPI + quarter, 0, lo_other);
+    l += lo_other;
     const long long li = A.group ? (long long)h * A.tq + q0 + qi : ((long long)b * A.hq + h) * A.sq + qi;
-    T* orow = static_cast<T*>(A.o) + elem_off(A.so, (long long)q0 + qi, h);
+    T* orow = static_cast<T*>(A.o) + elem_off(A.so, (long long)q0 + qi, h) + half * OC;
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-    for (int c = 0; c < DV / 32; ++c) {
+    for (int c = 0; c < OC / 32; ++c) {
       uint32_t o[32];
       if (ok && nkv > 0) {
-        tmem_ld32(lane_addr + C::T_O + c * 32, o);
+        tmem_ld32(lane_addr + C::T_O + half * OC + c * 32, o);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -366,8 +404,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         }
       }
     }
-    if (row_ok) A.lse[li] = !ok ? __int_as_float(0x7fc00000) : l > 0.f ? (mx + log2f(l)) * 0.6931471805599453f
-                                                                        : -INFINITY;
+    if (row_ok && half == 0)
+      A.lse[li] = !ok ? __int_as_float(0x7fc00000) : l > 0.f ? (mx + log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
 
   tc_fence_before();
