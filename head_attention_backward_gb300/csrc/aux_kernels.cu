@@ -18,10 +18,21 @@ namespace attn {
 
 // ----------------------------------------------------------------- schedule
 
+// Grouped work order (group mode only): used when the dq_acc slice exceeds
+// SCHED_GROUP_ABOVE bytes, with groups of about SCHED_GROUP_BYTES of query
+// tiles (L2 is 129 MB on GB300).  Measured on the packed THD workload (a
+// 268 MB slice): main kernel 0.817 -> 0.668 ms in ordered mode; on batch
+// workloads whose slice about fits L2, groups of one entry lengthened the
+// fold's waits, so they keep the plain order.
+constexpr long long SCHED_GROUP_ABOVE = 160LL << 20;
+constexpr long long SCHED_GROUP_BYTES = 96LL << 20;
+constexpr int SCHED_MAX_SEGS = 2048;   // segments cached in shared memory
+
 // keep_status: a later part of one call split into parts (attn_bwd_host); the
 // status of the earlier parts stays, and a part after a failed one does no work.
 __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_status) {
   __shared__ int s_bad;
+  __shared__ int s_lk[SCHED_MAX_SEGS], s_grp[SCHED_MAX_SEGS];
   const int tid = threadIdx.x;
   if (tid == 0) {
     s_bad = 0;
@@ -66,27 +77,70 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_statu
     for (int b = tid; b <= P.nseg; b += blockDim.x) P.tile_off[b] = 0;
     return;
   }
-  // KV-tile-major enumeration by warp 0: for kt, for segment, for kv head.
+  // Enumeration by warp 0, KV-tile-major: for kt, for segment, for kv head.
+  // When the dq_acc slice is much larger than L2, consecutive segments are
+  // first taken in groups of about SCHED_GROUP_BYTES of query tiles each (and
+  // KV-tile-major inside a group), so that in ordered-fold mode the partial
+  // sums a group adds into stay in L2 while its KV tiles pass over them.
+  // Either way each segment's KV tiles stay in ascending order, which the
+  // ordered fold's waits rely on.
   if (tid < 32) {
     const int lane = tid;
-    const int nkv_max = cdiv(P.sk > 0 ? P.sk : 1, BN);
+    const long long tile_bytes = (long long)P.hq * P.dqk * BM * 4;   // one query tile's partial sums, all heads
+    const bool grouped = P.group && P.nseg <= SCHED_MAX_SEGS && (long long)P.ntiles * tile_bytes > SCHED_GROUP_ABOVE;
     int n = 0;
-    for (int kt = 0; kt < nkv_max; ++kt) {
+    auto emit = [&](int g0, int g1, int nkv, const int* lks) {
+      for (int kt = 0; kt < nkv; ++kt) {
+        for (int b0 = g0; b0 < g1; b0 += 32) {
+          const int b = b0 + lane;
+          bool has = false;
+          if (b < g1) {
+            const int lk = lks ? lks[b] : (P.group ? P.cu_k[b + 1] - P.cu_k[b] : P.sk);
+            has = kt * BN < lk;
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, has);
+          const int before = __popc(m & ((1u << lane) - 1u));
+          if (has) {
+            const int base = n + before * P.hkv;
+            for (int h = 0; h < P.hkv; ++h)
+              if (base + h < P.max_items) P.items[base + h] = make_int4(b, h, kt, 0);
+          }
+          n += __popc(m) * P.hkv;
+        }
+      }
+    };
+    if (!grouped) {
+      emit(0, P.nseg, cdiv(P.sk > 0 ? P.sk : 1, BN), nullptr);
+    } else {
+      // segment lengths and group ids (query-tile bytes before the segment /
+      // SCHED_GROUP_BYTES) into shared memory, 32 segments at a time
+      long long carry = 0;
       for (int b0 = 0; b0 < P.nseg; b0 += 32) {
         const int b = b0 + lane;
-        bool has = false;
+        int lq = 0, lk = 0;
         if (b < P.nseg) {
-          const int lk = P.group ? P.cu_k[b + 1] - P.cu_k[b] : P.sk;
-          has = kt * BN < lk;
+          lq = P.cu_q[b + 1] - P.cu_q[b];
+          lk = P.cu_k[b + 1] - P.cu_k[b];
         }
-        const unsigned m = __ballot_sync(0xffffffffu, has);
-        const int before = __popc(m & ((1u << lane) - 1u));
-        if (has) {
-          const int base = n + before * P.hkv;
-          for (int h = 0; h < P.hkv; ++h)
-            if (base + h < P.max_items) P.items[base + h] = make_int4(b, h, kt, 0);
+        const long long bytes = (long long)cdiv(max(lq, 0), BM) * tile_bytes;
+        long long incl = bytes;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        n += __popc(m) * P.hkv;
+        if (b < P.nseg) {
+          s_lk[b] = max(lk, 0);
+          s_grp[b] = (int)((carry + incl - bytes) / SCHED_GROUP_BYTES);
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncwarp();
+      for (int g0 = 0; g0 < P.nseg;) {
+        int g1 = g0 + 1, nkv = cdiv(s_lk[g0], BN);
+        while (g1 < P.nseg && s_grp[g1] == s_grp[g0]) nkv = max(nkv, cdiv(s_lk[g1++], BN));
+        emit(g0, g1, nkv, s_lk);
+        g0 = g1;
       }
     }
     if (lane == 0) {

@@ -87,8 +87,10 @@ def test_window_dqk192_dv128_S8192(B, det):
     assert_all_ok(_check_batch(wl, x, got, [(0, 0), (0, 15)], [(0, 5)], 5), f"window det={det}")
 
 
-@pytest.mark.parametrize("det", [False, True], ids=["atomic", "det"])
+@pytest.mark.parametrize("det", [0, 1, 2], ids=["atomic", "ordered", "split"])
 def test_thd_packed_T16384_every_segment(B, det):
+    """The packed THD workload's dq_acc slice (about 270 MB) is over the
+    grouping threshold, so this also runs the grouped work order."""
     wl = W.thd_packed(deterministic=det)
     x, cu, (dq, dk, dv) = _run(B, wl, det)
     cu = cu.tolist()
@@ -108,3 +110,13 @@ def test_thd_packed_T16384_every_segment(B, det):
             rep.update(tensor=name, segment=b, length=n)
             reps.append(rep)
     assert_all_ok(reps, f"thd det={det}")
+
+
+def test_thd_grouped_order_ordered_fold_equals_split_bits(B):
+    """Under the grouped work order the ordered fold still adds each query
+    tile's partials in ascending KV-tile order: same bits as the split slices."""
+    wl = W.thd_packed(deterministic=True)
+    _, _, a = _run(B, wl, 1)
+    _, _, b = _run(B, wl, 2)
+    for name, x, y in zip(("dq", "dk", "dv"), a, b):
+        assert torch.equal(x, y), name
