@@ -304,17 +304,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       const int kb = (kt0 + j) * FN + half * SM_COLS;
       const bool full = kb + SM_COLS <= lk && (m.right < 0 || kb + SM_COLS - 1 <= qs + m.off + m.right) &&
                         (m.left < 0 || kb >= qe + m.off - m.left);
+      // row max of the raw scores (the scale is positive), masked keys -inf
       float pm[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) pm[i] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < SM_COLS; ++c) {
-        float x = __uint_as_float(sv[c]) * A.scale_log2;
-        if (!full) x = (kb + c < lk && visible(m, qi, kb + c)) ? x : -INFINITY;
-        sv[c] = __float_as_uint(x);
+        float x = __uint_as_float(sv[c]);
+        if (!full) {
+          x = (kb + c < lk && visible(m, qi, kb + c)) ? x : -INFINITY;
+          sv[c] = __float_as_uint(x);
+        }
         pm[c & 7] = fmaxf(pm[c & 7], x);
       }
-      float tmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      float tmax = A.scale_log2 *
+                   fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       float omax;
       if (!(ok = exchange(tmax, sb, B_RED + quarter * 2 + sb, (j >> 1) & 1, omax))) break;
       tmax = fmaxf(tmax, omax);
@@ -328,15 +332,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         mx = tmax;
       }
       const float mref = mx == -INFINITY ? 0.f : mx;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = exp2(s * scale log2(e) - m), two scores per packed fma
+      const float2 sc2 = make_float2(A.scale_log2, A.scale_log2), nm2 = make_float2(-mref, -mref);
+      const float2 one2 = make_float2(1.f, 1.f);
+      float2 ps[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ps[i] = make_float2(0.f, 0.f);
       uint32_t pk[SM_COLS / 2];
 #pragma unroll
       for (int c = 0; c < SM_COLS; c += 2) {
-        const float p0 = fast_exp2(__uint_as_float(sv[c]) - mref), p1 = fast_exp2(__uint_as_float(sv[c + 1]) - mref);
-        ps[(c >> 1) & 3] += p0 + p1;
-        pk[c >> 1] = pack2(p0, p1, (T*)nullptr);
+        const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nm2);
+        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        ps[(c >> 1) & 3] = fma2(p, one2, ps[(c >> 1) & 3]);
+        pk[c >> 1] = pack2(p.x, p.y, (T*)nullptr);
       }
-      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      l = l * alpha + (((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y)));
       // O and the P buffer are free once the previous tile's O += P V is done
       if (j > 0) {
         if (!(ok = wait_bar_warp(ctx, B_PV_DONE, (j - 1) & 1))) break;
@@ -499,10 +509,12 @@ static int launch_dims(const attn_fwd_params& p, const FwdLayout& L, cudaStream_
 
 }  // namespace fwdtc
 
-// Tensor-core forward for the 16-bit head-dim pairs it is built for;
-// ATTN_ERR_UNSUPPORTED_HEADDIM otherwise (the caller then runs the CUDA-core
-// forward).
+// Tensor-core forward for the 16-bit head-dim pairs it is built for and a
+// positive softmax scale; ATTN_ERR_UNSUPPORTED_HEADDIM otherwise (the caller
+// then runs the CUDA-core forward).
 int launch_fwd_tc(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
+  // the row max is taken on the raw scores, which needs a positive scale
+  if (!(p.softmax_scale > 0.f)) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   if (p.dtype == ATTN_BF16) return fwdtc::launch_dims<__nv_bfloat16>(p, L, st);
   if (p.dtype == ATTN_FP16) return fwdtc::launch_dims<__half>(p, L, st);
   return ATTN_ERR_UNSUPPORTED_HEADDIM;

@@ -223,6 +223,20 @@ def test_strided_layouts(B, case, det):
     assert_all_ok(run_strided_vs_oracle(B, wl, det, layout), f"{wl.name} {layout.__name__}")
 
 
+def test_forward_negative_scale_takes_cuda_core_path(B):
+    """The tensor-core forward takes the row max on raw scores and needs a
+    positive scale; a negative one runs the CUDA-core forward, still exact."""
+    wl = SMALL[2]
+    x = wl.inputs()
+    o_ref, lse_ref = R.attn_forward(x["q"], x["k"], x["v"], -0.05, mask=wl.mask)
+    o, lse = B.attn_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), scale=-0.05, mask=wl.mask)
+    torch.cuda.synchronize()
+    tol, mcos = tolerances(wl.dtype)
+    assert compare(o.cpu(), o_ref, tol, mcos)["ok"]
+    fin = torch.isfinite(lse_ref)
+    assert float((lse.cpu().double()[fin] - lse_ref[fin]).abs().max()) < 1e-3
+
+
 def test_forward_helper_strided(B):
     for wl, layout in STRIDED[:2] + STRIDED[4:6]:
         x = wl.inputs()
