@@ -120,3 +120,24 @@ def test_thd_grouped_order_ordered_fold_equals_split_bits(B):
     _, _, b = _run(B, wl, 2)
     for name, x, y in zip(("dq", "dk", "dv"), a, b):
         assert torch.equal(x, y), name
+
+
+def test_bench_workload_deterministic_10_runs_bitwise(B):
+    """The bench workload in both deterministic modes: 10 runs give the same
+    bits, and the ordered fold gives the split slices' bits (compared on the
+    device)."""
+    wl = W.gqa_causal_det()
+    x = {k: v.cuda() for k, v in wl.inputs().items()}
+    kw = dict(scale=wl.scale, mask=wl.mask)
+    o, lse = B.attn_forward(x["q"], x["k"], x["v"], **kw)
+    first = {}
+    for mode in (B.DET_ORDERED, B.DET_SPLIT):
+        for i in range(10):
+            got = B.attn_backward(x["q"], x["k"], x["v"], o, x["do"], lse, deterministic=mode, **kw)
+            if i == 0:
+                first[mode] = got
+            else:
+                for name, a, b in zip(("dq", "dk", "dv"), first[mode], got):
+                    assert torch.equal(a, b), f"mode {mode} run {i}: {name} differs"
+    for name, a, b in zip(("dq", "dk", "dv"), first[B.DET_ORDERED], first[B.DET_SPLIT]):
+        assert torch.equal(a, b), f"ordered fold and split slices differ in {name}"
