@@ -20,7 +20,7 @@ score matrices and library matmuls as the only primitives.  Sources:
   ``ck_to_aiter_mask_type``: mask kinds are "no mask", causal aligned top-left
   (1), causal aligned bottom-right (2) and a generic left/right window (3).
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
 
 1. Visibility of key j to query i, with off = 0 (top-left) or Lk - Lq
    (bottom-right):  causal  <=>  j <= i + off;  window(left, right)  <=>
