@@ -308,14 +308,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       float pm[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) pm[i] = -INFINITY;
+      if (full) {   // one uniform branch per tile, not per score
 #pragma unroll
-      for (int c = 0; c < SM_COLS; ++c) {
-        float x = __uint_as_float(sv[c]);
-        if (!full) {
-          x = (kb + c < lk && visible(m, qi, kb + c)) ? x : -INFINITY;
+        for (int c = 0; c < SM_COLS; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(sv[c]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < SM_COLS; ++c) {
+          const float x = (kb + c < lk && visible(m, qi, kb + c)) ? __uint_as_float(sv[c]) : -INFINITY;
           sv[c] = __float_as_uint(x);
+          pm[c & 7] = fmaxf(pm[c & 7], x);
         }
-        pm[c & 7] = fmaxf(pm[c & 7], x);
       }
       float tmax = A.scale_log2 *
                    fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
