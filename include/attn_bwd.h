@@ -25,7 +25,8 @@
  *   (aiter PR #2216 follow-up: "LOG_ERROR + return -1" on missing group
  *   pointers; TransformerEngine PR #671: a hard head-dim check instead of a
  *   silent hard-coded size).
- * - Tensors are contiguous.  Batch mode (cu_seqlens_q == cu_seqlens_k ==
+ * - Tensors are contiguous by default (per-tensor strides: see the stride_*
+ *   fields of attn_bwd_params).  Batch mode (cu_seqlens_q == cu_seqlens_k ==
  *   NULL): q [B,Sq,Hq,d_qk], k [B,Sk,Hkv,d_qk], v [B,Sk,Hkv,d_v],
  *   o/dout/dq [B,Sq,Hq,·], dk/dv like k/v, lse [B,Hq,Sq].  Group mode:
  *   q [Tq,Hq,d_qk], k [Tk,Hkv,d_qk], v [Tk,Hkv,d_v], lse [Hq,Tq]; segment b
