@@ -206,11 +206,15 @@ typedef enum { ATTN_DET_ATOMIC = 0, ATTN_DET_ORDERED = 1, ATTN_DET_SPLIT = 2 } a
  * fields (no device access, no GPU probe), using the same layout function as
  * attn_bwd, so the sizing and the launch cannot disagree (the sizing-pass
  * lesson of TransformerEngine PR #671, review reply on is_v3_api_check).
- * In ATTN_DET_SPLIT mode (and ATTN_DET_ORDERED with FP32 inputs) the
- * workspace holds nsplits = ceil(seqlen_k / 128) fp32 dq_acc slices of
- * [B][Hq][Sq][d_qk] (group mode: [Hq][Tq][d_qk], row = packed token, the
- * fp32-packed layout of PR #671, Root cause), otherwise one slice (plus one
- * turn counter per query tile and head in ATTN_DET_ORDERED mode).
+ * The workspace is dominated by fp32 dq_acc slices, each Hq x ntiles query
+ * tiles of 64 rows x d_qk, with ntiles = batch * ceil(seqlen_q / 64) in batch
+ * mode and min(floor(total_q / 64) + batch, batch * ceil(seqlen_q / 64)) in
+ * group mode (each segment's rows start a new tile: a per-segment padded
+ * layout, the kind TransformerEngine PR #671's Fix switches dq_acc to, with
+ * one layout shared by the sizing call and the kernels).  ATTN_DET_SPLIT (and
+ * ATTN_DET_ORDERED with FP32 inputs) uses nsplits = ceil(seqlen_k / 128)
+ * slices, the other modes one; ATTN_DET_ORDERED adds a turn counter per
+ * query tile and head.  Small per-row and per-tile tables come on top.
  * Writes the size to *bytes.  Returns ATTN_OK or an error code. */
 int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes);
 
@@ -285,8 +289,8 @@ int attn_bwd_host(const attn_bwd_params* p, const attn_host_tensors* host, void*
 
 /* attn_bwd for callers that cannot allocate device memory (for example code
  * that runs where cudaMalloc is forbidden or whose allocator is not reachable
- * from the call site).  The paper has no counterpart: it is an addition of
- * this library.  The caller still passes every input and output through *p;
+ * from the call site).  The cited PRs have no counterpart: it is an addition
+ * of this library.  The caller still passes every input and output through *p;
  * the workspace is a fixed ATTN_BWD_STATIC_WS_BYTES device array inside the
  * library (held on every GPU that loads the library until the process
  * exits), so no memory is allocated by this call.
