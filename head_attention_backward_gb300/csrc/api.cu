@@ -167,9 +167,14 @@ static int validate_fwd(const attn_fwd_params* p) {
   int st = validate_common(p);
   if (st != ATTN_OK) return st;
   if (p->d_qk > 192 || p->d_v > 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
-  const void* ptrs[] = {p->q, p->k, p->v, p->o, p->lse};
+  // 16-bit tensors feed tensor maps and 16-byte vector stores of O (the same
+  // rule as the backward's); fp32 tensors and lse are accessed one element
+  // at a time
+  const uintptr_t amask = p->dtype == ATTN_FP32 ? 3u : 15u;
+  const void* ptrs[] = {p->q, p->k, p->v, p->o};
   for (const void* x : ptrs)
-    if (!x) return ATTN_ERR_INVALID_ARG;
+    if (!x || (reinterpret_cast<uintptr_t>(x) & amask) != 0) return ATTN_ERR_INVALID_ARG;
+  if (!p->lse || (reinterpret_cast<uintptr_t>(p->lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 

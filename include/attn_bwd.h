@@ -155,7 +155,9 @@ typedef struct {
 
 /* Forward helper that produces O and LSE for benchmark and test inputs
  * (the forward pass implied by TransformerEngine PR #446's ck_attn_fwd).
- * Same field meanings as attn_bwd_params; o and lse are outputs. */
+ * Same field meanings and alignment rules as attn_bwd_params (q, k, v, o
+ * 16-byte aligned, 4-byte for FP32; lse 4-byte aligned); o and lse are
+ * outputs. */
 typedef struct {
   int32_t dtype;
   int32_t batch;

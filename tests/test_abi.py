@@ -297,3 +297,13 @@ def test_fwd_rejects_bad_args(lib):
     p.q, p.k, p.v, p.o, p.lse = 0x1000, 0x2000, 0x3000, 0x4000, 0x5000
     p.d_qk = 256
     assert B.attn_fwd(p, 0) == -2
+    p.d_qk = 64
+    p.o = 0x4002                           # O is written with 16-byte vector stores
+    assert B.attn_fwd(p, 0) == -1
+    p.o, p.q = 0x4000, 0x1008              # q feeds a tensor map
+    assert B.attn_fwd(p, 0) == -1
+    p.q, p.lse = 0x1000, 0x5002            # lse: 4-byte alignment
+    assert B.attn_fwd(p, 0) == -1
+    p.dtype, p.lse, p.o = 2, 0x5000, 0x4004   # fp32: 4-byte alignment is enough, 2 is not
+    p.q = 0x1002
+    assert B.attn_fwd(p, 0) == -1
