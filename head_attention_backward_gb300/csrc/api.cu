@@ -131,6 +131,10 @@ static int validate_common(const Prm* p) {
   if (gq != gk) return ATTN_ERR_INVALID_ARG;   // group mode needs both seqstart arrays
   // padded starts only refine group mode
   if (!gq && (p->cu_seqlens_q_padded || p->cu_seqlens_k_padded)) return ATTN_ERR_INVALID_ARG;
+  // the seqstart arrays are read as int32 on the device
+  const void* seq[] = {p->cu_seqlens_q, p->cu_seqlens_k, p->cu_seqlens_q_padded, p->cu_seqlens_k_padded};
+  for (const void* x : seq)
+    if ((reinterpret_cast<uintptr_t>(x) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   if (gq && (p->total_q < 0 || p->total_k < 0)) return ATTN_ERR_INVALID_ARG;
   if (p->mask < ATTN_MASK_NONE || p->mask > ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;
   if (p->mask == ATTN_MASK_WINDOW && (p->window_left < -1 || p->window_right < -1))

@@ -78,7 +78,8 @@ typedef enum {
  * BOTTOM_RIGHT and WINDOW (per segment), key j is visible to query i iff
  *   CAUSAL_*: j <= i + off
  *   WINDOW:   i + off - window_left <= j <= i + off + window_right
- * (inclusive; a negative bound means unbounded on that side). */
+ * (inclusive; -1 means unbounded on that side, other negative bounds are
+ * rejected). */
 typedef enum {
   ATTN_MASK_NONE = 0,
   ATTN_MASK_CAUSAL_TOP_LEFT = 1,
@@ -104,8 +105,9 @@ typedef struct {
   int32_t total_k;        /* group mode: Tk = cu_seqlens_k[batch]; ignored in batch */
   int32_t d_qk;           /* head dim of q and k                                   */
   int32_t d_v;            /* head dim of v and o                                   */
-  const int32_t* cu_seqlens_q; /* device, [batch+1], or NULL (batch mode)          */
-  const int32_t* cu_seqlens_k; /* device, [batch+1], or NULL (batch mode)          */
+  const int32_t* cu_seqlens_q; /* device, [batch+1], 4-byte aligned, or NULL
+                                  (batch mode)                                  */
+  const int32_t* cu_seqlens_k; /* device, [batch+1], 4-byte aligned, or NULL      */
   const int32_t* cu_seqlens_q_padded; /* device, [batch+1]: physical start row of
                              each query segment, or NULL (start = cu_seqlens_q);
                              group mode only.  Must satisfy padded[b] + Lq_b <=

@@ -175,6 +175,18 @@ def test_group_mode_needs_both_seqstart_arrays(lib):
     assert B.attn_bwd(p, 0x100000, 1 << 40, 0) == -1
 
 
+def test_seqstart_arrays_must_be_int32_aligned(lib):
+    p = make(total_q=100, total_k=100)
+    p.cu_seqlens_q, p.cu_seqlens_k = 0x1000, 0x2000
+    assert B.attn_bwd_workspace_size(p)[0] == 0
+    for field in ("cu_seqlens_q", "cu_seqlens_k", "cu_seqlens_q_padded", "cu_seqlens_k_padded"):
+        q = make(total_q=100, total_k=100)
+        q.cu_seqlens_q, q.cu_seqlens_k = 0x1000, 0x2000
+        setattr(q, field, 0x3002)
+        assert B.attn_bwd_workspace_size(q)[0] == -1, field
+        assert B.attn_bwd(q, 0x100000, 1 << 40, 0) == -1, field
+
+
 def _with_strides(p, **strides):
     for name, val in strides.items():
         getattr(p, "stride_" + name)[:] = val
