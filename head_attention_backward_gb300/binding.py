@@ -24,6 +24,8 @@ DET_ATOMIC, DET_ORDERED, DET_SPLIT = 0, 1, 2   # attn_det_t
 STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED_HEADDIM",
           -3: "ATTN_ERR_WORKSPACE_TOO_SMALL", -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_DEVICE_FLAG",
           -6: "ATTN_ERR_TIMEOUT", -7: "ATTN_ERR_BAD_SEQLENS"}
+# attn_status_t codes by name (ATTN_OK, ATTN_ERR_INVALID_ARG, ...)
+globals().update({name: code for code, name in STATUS.items()})
 
 _DTYPES = {torch.bfloat16: ATTN_BF16, torch.float16: ATTN_FP16, torch.float32: ATTN_FP32}
 

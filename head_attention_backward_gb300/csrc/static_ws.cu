@@ -15,7 +15,10 @@
 // process exits.  Host code cannot use the array's name as a device address
 // (on the host it is only a stand-in symbol), so the device address is
 // looked up once per device with cudaGetSymbolAddress, with that device
-// current, on the first call made while it is the current device.
+// current, on the first call made while it is the current device.  The
+// address is cached per device ordinal and belongs to the primary context of
+// that device: a cudaDeviceReset (which unloads the module) or a non-primary
+// context would need a new lookup, and the header declares both unsupported.
 #include <mutex>
 
 #include "common.cuh"

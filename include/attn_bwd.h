@@ -303,6 +303,10 @@ int attn_bwd_host(const attn_bwd_params* p, const attn_host_tensors* host, void*
  * - The first call while a given device is current looks up the array's
  *   device address (cudaGetSymbolAddress); make that first call before any
  *   stream capture on that device.
+ * - That address is kept per device ordinal for the life of the process and
+ *   belongs to the device's primary context.  After cudaDeviceReset, or with
+ *   a non-primary context current, it no longer names the library's array:
+ *   neither case is supported by this entry point (use attn_bwd there).
  * - All calls on a device share the one array: calls that overlap on the GPU
  *   (other streams, other host threads) race and corrupt each other.  Calls
  *   ordered on one stream are safe; each call initialises what it reads.

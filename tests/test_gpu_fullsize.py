@@ -100,15 +100,21 @@ def test_thd_packed_T16384_every_segment(B, det):
     for b in range(len(cu) - 1):
         n = cu[b + 1] - cu[b]
         rows = _rows(n, rng, k=4)
-        h = int(rng.integers(0, wl.hq))
-        hk = int(rng.integers(0, wl.hkv))
-        rq = R.dq_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, h, rows, **okw)
-        ek, ev = R.dkv_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, hk, rows, **okw)
         idx = torch.tensor(rows) + cu[b]
-        for name, g, r in (("dq", dq[idx, h], rq), ("dk", dk[idx, hk], ek), ("dv", dv[idx, hk], ev)):
-            rep = compare(g, r, 2e-2, 0.9999)
-            rep.update(tensor=name, segment=b, length=n)
+        # two query heads (one random, one from the other half of the heads)
+        # and both ends of the kv-head range, every segment
+        h0 = int(rng.integers(0, wl.hq // 2))
+        for h in (h0, h0 + wl.hq // 2):
+            rq = R.dq_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, h, rows, **okw)
+            rep = compare(dq[idx, h], rq, 2e-2, 0.9999)
+            rep.update(tensor="dq", segment=b, length=n, head=h)
             reps.append(rep)
+        for hk in (0, wl.hkv - 1):
+            ek, ev = R.dkv_rows(x["q"], x["k"], x["v"], x["do"], wl.scale, b, hk, rows, **okw)
+            for name, g, r in (("dk", dk[idx, hk], ek), ("dv", dv[idx, hk], ev)):
+                rep = compare(g, r, 2e-2, 0.9999)
+                rep.update(tensor=name, segment=b, length=n, head=hk)
+                reps.append(rep)
     assert_all_ok(reps, f"thd det={det}")
 
 

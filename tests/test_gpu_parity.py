@@ -100,11 +100,15 @@ def test_small_backward(B, wl, det):
 
 
 @pytest.mark.parametrize("det", **DET_MODES)
+@pytest.mark.parametrize("heads", [(8, 2), (32, 8)], ids=["hq8_hkv2", "hq32_hkv8"])
 @pytest.mark.parametrize("segs", W.PAGE_SPLITS + [[1, 1, 130, 1], [5, 0, 7], [2048]], ids=str)
-def test_thd_splits_per_segment(B, segs, det):
-    """Packed THD, padding-causal within segments, llama3-shaped GQA heads
+def test_thd_splits_per_segment(B, segs, heads, det):
+    """Packed THD, padding-causal within segments, GQA heads: a small group and
+    the Llama-3-8B shape of the packed benchmark workload (32 query, 8 kv
+    heads); every segment of every tensor is compared on its own
     (TransformerEngine PR #671, Tests / Verification)."""
-    wl = W.thd("thd", segs, hq=8, hkv=2, seed=sum(segs))
+    hq, hkv = heads
+    wl = W.thd("thd", segs, hq=hq, hkv=hkv, seed=sum(segs) + hq)
     reps = run_backward_vs_oracle(B, wl, det)
     assert_all_ok(reps, f"segments {segs}")
 
