@@ -250,9 +250,10 @@ static void log_config(const attn_bwd_params& p, const WsLayout& L) {
 // dtypes and head dims it is not built for.
 int launch_fwd_tc(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st);
 
-// Schedule launch for one part of a call split into parts (attn_bwd_host):
-// parts after the first keep the status the earlier parts left.
-void launch_schedule_part(const Problem& P, cudaStream_t st, bool keep_status);
+// Schedule and preprocess launches of one call, or of one part of a call
+// split into parts (attn_bwd_host: parts after the first keep the status the
+// earlier parts left).
+void launch_schedule_preprocess(const Problem& P, cudaStream_t st, bool keep_status);
 
 static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t s,
                cudaEvent_t* ev /* 4 events or null */, bool keep_status = false) {
@@ -267,8 +268,7 @@ static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t
   if (log_enabled()) log_config(e, L);
   const Problem P = make_problem(e, sx, ws);
   if (ev) cudaEventRecord(ev[0], s);
-  launch_schedule_part(P, s, keep_status);
-  launch_preprocess(P, s);
+  launch_schedule_preprocess(P, s, keep_status);
   if (ev) cudaEventRecord(ev[1], s);
   if (P.dtype == ATTN_FP32) {
     launch_bwd_simt(P, s);

@@ -33,7 +33,20 @@ constexpr int SCHED_MAX_SEGS = 2048;   // segments cached in shared memory
 __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_status) {
   __shared__ int s_bad;
   __shared__ int s_lk[SCHED_MAX_SEGS], s_grp[SCHED_MAX_SEGS];
+  __shared__ int s_cq[SCHED_MAX_SEGS + 1], s_ck[SCHED_MAX_SEGS + 1];
   const int tid = threadIdx.x;
+  // the logical offsets are read many times below: one parallel pass copies
+  // them into shared memory (up to SCHED_MAX_SEGS segments; beyond that they
+  // are read from global memory)
+  const bool cached = P.group && P.nseg <= SCHED_MAX_SEGS;
+  if (cached) {
+    for (int b = tid; b <= P.nseg; b += blockDim.x) {
+      s_cq[b] = P.cu_q[b];
+      s_ck[b] = P.cu_k[b];
+    }
+  }
+  const int* cq = cached ? s_cq : P.cu_q;
+  const int* ck = cached ? s_ck : P.cu_k;
   if (tid == 0) {
     s_bad = 0;
     if (keep_status && P.hdr[HDR_STATUS] != 0) {
@@ -52,12 +65,12 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_statu
     // the tensor (without padding the starts are the offsets themselves and
     // the last one must equal the row total)
     for (int b = tid; b < P.nseg; b += blockDim.x) {
-      const int lq = P.cu_q[b + 1] - P.cu_q[b], lk = P.cu_k[b + 1] - P.cu_k[b];
+      const int lq = cq[b + 1] - cq[b], lk = ck[b + 1] - ck[b];
       bool bad = lq < 0 || lk < 0 || lq > P.sq || lk > P.sk;
       const long long sq0 = P.st_q[b], sq1 = P.st_q[b + 1];
       const long long sk0 = P.st_k[b], sk1 = P.st_k[b + 1];
       bad |= sq0 + lq > sq1 || sk0 + lk > sk1;
-      if (b == 0) bad |= P.cu_q[0] != 0 || P.cu_k[0] != 0 || sq0 < 0 || sk0 < 0;
+      if (b == 0) bad |= cq[0] != 0 || ck[0] != 0 || sq0 < 0 || sk0 < 0;
       if (b == P.nseg - 1) {
         bad |= sq1 > P.tq || sk1 > P.tk;
         if (P.st_q == P.cu_q) bad |= sq1 != P.tq;
@@ -95,7 +108,7 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_statu
           const int b = b0 + lane;
           bool has = false;
           if (b < g1) {
-            const int lk = lks ? lks[b] : (P.group ? P.cu_k[b + 1] - P.cu_k[b] : P.sk);
+            const int lk = lks ? lks[b] : (P.group ? ck[b + 1] - ck[b] : P.sk);
             has = kt * BN < lk;
           }
           const unsigned m = __ballot_sync(0xffffffffu, has);
@@ -119,8 +132,8 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_statu
         const int b = b0 + lane;
         int lq = 0, lk = 0;
         if (b < P.nseg) {
-          lq = P.cu_q[b + 1] - P.cu_q[b];
-          lk = P.cu_k[b + 1] - P.cu_k[b];
+          lq = cq[b + 1] - cq[b];
+          lk = ck[b + 1] - ck[b];
         }
         const long long bytes = (long long)cdiv(max(lq, 0), BM) * tile_bytes;
         long long incl = bytes;
@@ -158,7 +171,7 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_statu
     for (int b0 = 0; b0 <= P.nseg; b0 += 32) {
       const int b = b0 + lane;
       int v = 0;
-      if (b < P.nseg) v = cdiv(P.cu_q[b + 1] - P.cu_q[b], BM);
+      if (b < P.nseg) v = cdiv(cq[b + 1] - cq[b], BM);
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -172,13 +185,6 @@ __global__ void __launch_bounds__(256) schedule_kernel(Problem P, int keep_statu
   }
 }
 
-void launch_schedule(const Problem& P, cudaStream_t st) {
-  schedule_kernel<<<1, 256, 0, st>>>(P, 0);
-}
-
-void launch_schedule_part(const Problem& P, cudaStream_t st, bool keep_status) {
-  schedule_kernel<<<1, 256, 0, st>>>(P, keep_status ? 1 : 0);
-}
 
 // --------------------------------------------------------------- preprocess
 // D and -LSE*log2(e) of every (packed token, query head) row.  16-bit
@@ -257,11 +263,42 @@ __device__ void zero_padding_rows(const int* st, const int* cu, int nseg, int to
 
 constexpr int PRE_BLOCKS_PER_SM = 3;
 
+// Batch mode needs no cu_seqlens validation, so the preprocess kernel also
+// does the scheduler's part (sched != 0): block 0 resets the workspace header
+// (keeping an earlier part's failure when sched == 2, as schedule_kernel
+// does) and the grid writes the work list in the same KV-tile-major order,
+// item (kt, b, h) at index (kt * B + b) * Hkv + h.  This saves the one-block
+// scheduler launch.  The main kernel starts after this kernel has finished,
+// so it sees the header and the list complete.
+__device__ __forceinline__ void batch_schedule(const Problem& P, int sched, long long tid, long long nthreads) {
+  if (blockIdx.x == 0) {
+    __shared__ int s_skip;
+    if (threadIdx.x == 0) {
+      s_skip = sched == 2 && P.hdr[HDR_STATUS] != 0;
+      if (!s_skip) {
+        P.hdr[HDR_STATUS] = 0;
+        P.hdr[HDR_DIAG] = 0;
+      }
+      P.hdr[HDR_NEXT] = 0;
+      P.hdr[HDR_NITEMS] = s_skip ? 0 : P.max_items;
+    }
+    __syncthreads();
+    if (!s_skip && threadIdx.x >= 16 && threadIdx.x < HDR_WORDS) P.hdr[threadIdx.x] = 0;
+  }
+  const int per_kt = P.nseg * P.hkv;
+  for (long long i = tid; i < P.max_items; i += nthreads) {
+    const int kt = (int)(i / per_kt), r = (int)(i - (long long)kt * per_kt);
+    const int b = r / P.hkv;
+    P.items[i] = make_int4(b, r - b * P.hkv, kt, 0);
+  }
+}
+
 template <typename T>
-__global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Problem P, long long ntok) {
+__global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Problem P, long long ntok, int sched) {
   const int lane = threadIdx.x & 31;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
+  if (sched) batch_schedule(P, sched, tid, nthreads);
   const long long nrows = ntok * P.hq;
   if constexpr (sizeof(T) == 2) {
     // A half warp takes RPH consecutive rows at a time (16-byte loads; d_v and
@@ -366,18 +403,39 @@ static int num_sms() {
   return n > 0 ? n : 1;
 }
 
-void launch_preprocess(const Problem& P, cudaStream_t st) {
+// sched: 0 = the scheduler kernel ran before; 1 / 2 = batch mode, this
+// kernel schedules (2: keep an earlier part's status).
+static void launch_preprocess_sched(const Problem& P, cudaStream_t st, int sched) {
   const long long ntok = P.group ? (long long)P.tq : (long long)P.nseg * P.sq;
   const int grid = num_sms() * PRE_BLOCKS_PER_SM;   // one resident wave
   switch (P.dtype) {
-    case ATTN_BF16: preprocess_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(P, ntok); break;
-    case ATTN_FP16: preprocess_kernel<__half><<<grid, 256, 0, st>>>(P, ntok); break;
-    default: preprocess_kernel<float><<<grid, 256, 0, st>>>(P, ntok); break;
+    case ATTN_BF16: preprocess_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(P, ntok, sched); break;
+    case ATTN_FP16: preprocess_kernel<__half><<<grid, 256, 0, st>>>(P, ntok, sched); break;
+    default: preprocess_kernel<float><<<grid, 256, 0, st>>>(P, ntok, sched); break;
   }
 }
 
+void launch_preprocess(const Problem& P, cudaStream_t st) { launch_preprocess_sched(P, st, 0); }
+
+// Schedule + preprocess of one call (or one part of a call split into parts,
+// keep_status: the earlier parts' status stays).  Group mode validates
+// cu_seqlens in the scheduler kernel first; batch mode folds the schedule into
+// the preprocess kernel (debug builds keep the separate scheduler, whose
+// header reset then precedes every index check of the preprocess).
+void launch_schedule_preprocess(const Problem& P, cudaStream_t st, bool keep_status) {
+#ifndef ATTN_DEBUG
+  if (!P.group) {
+    launch_preprocess_sched(P, st, keep_status ? 2 : 1);
+    return;
+  }
+#endif
+  schedule_kernel<<<1, 256, 0, st>>>(P, keep_status ? 1 : 0);
+  launch_preprocess_sched(P, st, 0);
+}
+
 // ----------------------------------------------------------- reduce/convert
-// One block per (query head, query tile).  Split mode: the query-major dQ
+// One block per (query head, query tile) at a time; one resident wave of
+// blocks loops over the pairs.  Split mode: the query-major dQ
 // tiles of the slices whose KV tile reaches this query tile (the others were
 // never written) are summed in ascending slice order; atomic and ordered-fold
 // modes read the single slice.  Each thread owns four consecutive d of one
@@ -386,16 +444,12 @@ void launch_preprocess(const Problem& P, cudaStream_t st) {
 constexpr int RC_THREADS = 256;
 
 // NACC = float4 accumulators per thread = ceil(d_qk * BM / 4 / RC_THREADS).
-template <typename T, int NACC>
-__global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
-  // a rejected problem (bad cu_seqlens, expired wait) leaves dQ untouched
-  if (*(volatile const int*)(P.hdr + HDR_STATUS) != 0) return;
+// One (head, query tile) of the dQ output: w = head * ntiles + tile.
+template <typename T, int NACC, bool SPLIT>
+__device__ __forceinline__ void reduce_convert_tile(const Problem& P, long long w) {
   const int dqk = P.dqk;
   const int nv4 = dqk * BM / 4;      // float4 per dQ tile
   T* dQ = static_cast<T*>(P.dq);
-  // block -> (head, tile), head-major (measured a few percent faster than
-  // interleaving heads or putting the most-loaded causal tiles first)
-  const long long w = blockIdx.x;
   const int h = (int)(w / P.ntiles);
   const int t = (int)(w % P.ntiles);
   int b, qt;
@@ -427,7 +481,7 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
       }
     }
   };
-  if (P.det && !P.fold) {
+  if constexpr (SPLIT) {
     const MaskArgs m = mask_args(P.mask, P.left, P.right, s.lq, s.lk);
     int nkv = cdiv(s.lk, BN);
     if (nkv > P.nsplits) nkv = P.nsplits;   // guards cu_seqlens that broke their bound
@@ -447,7 +501,11 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
       k0 = k1 < nkv ? next(k1 + 1) : nkv;
     }
   } else if (s.lk > 0) {   // atomic and ordered fold: the single, pre-zeroed slice
-    add_tiles(dq_tile(P, 0, h, t), nullptr);
+#pragma unroll
+    for (int i = 0; i < NACC; ++i) {
+      const int v = threadIdx.x + i * RC_THREADS;
+      if (v < nv4) acc[i] = __ldcs(reinterpret_cast<const float4*>(dq_tile(P, 0, h, t)) + v);
+    }
   }
   T* dQt = dQ + elem_off(P.sdq_, s.q0 + qt * BM, h);   // row 0 of the tile
 #pragma unroll
@@ -469,21 +527,56 @@ __global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
   }
 }
 
-template <typename T>
-static void launch_rc(const Problem& P, unsigned grid, cudaStream_t st) {
+// SPLIT: sum the split slices (deterministic split mode); otherwise convert
+// the single slice (atomic, ordered fold), an instantiation of its own so that
+// its lower register count allows a full SM of blocks.
+template <typename T, int NACC, bool SPLIT>
+__global__ void __launch_bounds__(RC_THREADS) reduce_convert_kernel(Problem P) {
+  // a rejected problem (bad cu_seqlens, expired wait) leaves dQ untouched
+  if (*(volatile const int*)(P.hdr + HDR_STATUS) != 0) return;
+  const long long work = (long long)P.hq * P.ntiles;
+  // one resident wave of blocks walks the (head, tile) pairs head-major
+  for (long long w = blockIdx.x; w < work; w += gridDim.x) reduce_convert_tile<T, NACC, SPLIT>(P, w);
+}
+
+// Single slice: one resident wave of blocks (as many as the occupancy of the
+// instantiation allows on every SM), or fewer when there are fewer (head,
+// tile) pairs.  Split slices: one block per pair (a block sums a variable
+// number of slices, so many independent blocks overlap better than a loop).
+template <typename K>
+static void launch_rc_kernel(K kern, const Problem& P, long long work, bool wave_grid, cudaStream_t st) {
+  long long grid = work;
+  if (wave_grid) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RC_THREADS, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    const long long wave = (long long)num_sms() * per_sm;
+    if (wave < grid) grid = wave;
+  }
+  kern<<<(unsigned)grid, RC_THREADS, 0, st>>>(P);
+}
+
+template <typename T, bool SPLIT>
+static void launch_rc(const Problem& P, long long work, cudaStream_t st) {
   const int nacc = cdiv(P.dqk * BM / 4, RC_THREADS);
-  if (nacc <= 4) reduce_convert_kernel<T, 4><<<grid, RC_THREADS, 0, st>>>(P);
-  else if (nacc <= 8) reduce_convert_kernel<T, 8><<<grid, RC_THREADS, 0, st>>>(P);
-  else reduce_convert_kernel<T, 12><<<grid, RC_THREADS, 0, st>>>(P);
+  if (nacc <= 4) launch_rc_kernel(reduce_convert_kernel<T, 4, SPLIT>, P, work, !SPLIT, st);
+  else if (nacc <= 8) launch_rc_kernel(reduce_convert_kernel<T, 8, SPLIT>, P, work, !SPLIT, st);
+  else launch_rc_kernel(reduce_convert_kernel<T, 12, SPLIT>, P, work, !SPLIT, st);
+}
+
+template <typename T>
+static void launch_rc(const Problem& P, long long work, cudaStream_t st) {
+  if (P.det && !P.fold) launch_rc<T, true>(P, work, st);
+  else launch_rc<T, false>(P, work, st);
 }
 
 void launch_reduce_convert(const Problem& P, cudaStream_t st) {
-  const long long work = (long long)P.hq * P.ntiles;   // one block per (head, query tile)
+  const long long work = (long long)P.hq * P.ntiles;   // (head, query tile) pairs
   if (work <= 0) return;
   switch (P.dtype) {
-    case ATTN_BF16: launch_rc<__nv_bfloat16>(P, (unsigned)work, st); break;
-    case ATTN_FP16: launch_rc<__half>(P, (unsigned)work, st); break;
-    default: launch_rc<float>(P, (unsigned)work, st); break;
+    case ATTN_BF16: launch_rc<__nv_bfloat16>(P, work, st); break;
+    case ATTN_FP16: launch_rc<__half>(P, work, st); break;
+    default: launch_rc<float>(P, work, st); break;
   }
 }
 

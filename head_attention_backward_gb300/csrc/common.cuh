@@ -329,7 +329,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // ------------------------------------------------------- kernel entry points
 
-void launch_schedule(const Problem& P, cudaStream_t st);
 void launch_preprocess(const Problem& P, cudaStream_t st);
 void launch_reduce_convert(const Problem& P, cudaStream_t st);
 void launch_bwd_simt(const Problem& P, cudaStream_t st);
