@@ -373,7 +373,9 @@ def run_ours(args, wl):
         "e2e": None if args.no_e2e else {"value": job_throughput(world, fl, e2e_avg), "unit": "TFLOP/s",
                                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                          "ms_per_step": e2e_avg, "api": "attn_bwd_host", "chunks": e2e_chunks},
-        "gpu_launches": 4 * args.steps,
+        # the library's own kernels per step: preprocess, main, reduce/convert,
+        # plus the scheduler in group mode (batch mode schedules in the preprocess)
+        "gpu_launches": (4 if wl.group_mode else 3) * args.steps,
         "forward": {"kernel": "fwd_tc_kernel" if wl.dtype != torch.float32 else "fwd_kernel",
                     "ms": fwd_ms, "TFLOP/s": fl * (wl.d_qk + wl.d_v) / (3 * wl.d_qk + 2 * wl.d_v) / fwd_ms / 1e9,
                     "note": "median of 10 attn_fwd calls on the same inputs; not part of the timed step"},
