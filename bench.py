@@ -36,7 +36,7 @@ from head_attention_backward_gb300 import workloads as W  # noqa: E402
 
 METRIC = "attn-bwd TFLOP/s (mask-adjusted, bf16) and % of GB300 dense BF16 peak"
 WORKLOADS = {"gqa_causal_det": W.gqa_causal_det, "mha_causal": W.mha_causal,
-             "thd_packed": W.thd_packed, "window_192": W.window_192}
+             "thd_packed": W.thd_packed, "window_192": W.window_192, "gqa_d256": W.gqa_d256}
 
 
 def dist_env():
@@ -107,11 +107,20 @@ def dq_mode(wl):
     return int(wl.deterministic)
 
 
+def dq_mode_run(wl):
+    """The dQ accumulation the library runs for the workload: the ordered fold
+    is served by the split slices for fp32 inputs and head dim 256."""
+    m = dq_mode(wl)
+    if m == DQ_MODES["ordered"] and (wl.dtype == torch.float32 or wl.d_qk > 192):
+        return DQ_MODES["split"]
+    return m
+
+
 def config_of(wl):
     c = {"workload": wl.name, "batch": wl.batch, "nhead_q": wl.hq, "nhead_kv": wl.hkv,
          "seqlen": wl.sq, "d_qk": wl.d_qk, "d_v": wl.d_v, "mask": wl.mask,
          "window": [wl.left, wl.right], "deterministic": bool(wl.deterministic),
-         "dq_mode": DQ_MODE_NAMES[dq_mode(wl)],
+         "dq_mode": DQ_MODE_NAMES[dq_mode_run(wl)],
          "l2": "flushed (256 MB write) before every timed step"}
     if wl.group_mode:
         c["segments"] = len(wl.seqlens)
@@ -310,7 +319,7 @@ def run_ours(args, wl):
     # the pages' split-slice workspace on the same workload (same bits as the
     # ordered fold), timed beside it for reference
     split_leg = None
-    if dq_mode(wl) == DQ_MODES["ordered"] and not args.no_split_leg:
+    if dq_mode_run(wl) == DQ_MODES["ordered"] and not args.no_split_leg:
         ps = B.bwd_params(d["q"], d["k"], d["v"], o, d["do"], lse, *outs, deterministic=DQ_MODES["split"], **kw)
         nb = B.workspace_bytes(ps)
         wss = B.alloc_workspace(nb, dev)

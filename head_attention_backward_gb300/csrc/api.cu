@@ -14,7 +14,8 @@
 namespace attn {
 
 static bool tc_headdims(int dqk, int dv) {
-  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128) ||
+         (dqk == 256 && dv == 256);
 }
 
 static bool simt_headdims(int dqk, int dv) {
@@ -170,7 +171,7 @@ static int validate_bwd(const attn_bwd_params* p) {
 static int validate_fwd(const attn_fwd_params* p) {
   int st = validate_common(p);
   if (st != ATTN_OK) return st;
-  if (p->d_qk > 192 || p->d_v > 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  if (p->d_qk > 256 || p->d_v > 256) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   // 16-bit tensors feed tensor maps and 16-byte vector stores of O (the same
   // rule as the backward's); fp32 tensors and lse are accessed one element
   // at a time

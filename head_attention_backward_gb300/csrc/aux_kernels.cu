@@ -293,7 +293,8 @@ __device__ __forceinline__ void batch_schedule(const Problem& P, int sched, long
   }
 }
 
-template <typename T>
+// VW: 16-byte vectors per lane and row (1 for d_v <= 128, 2 for d_v = 256).
+template <typename T, int VW>
 __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Problem P, long long ntok, int sched) {
   const int lane = threadIdx.x & 31;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -302,10 +303,10 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
   const long long nrows = ntok * P.hq;
   if constexpr (sizeof(T) == 2) {
     // A half warp takes RPH consecutive rows at a time (16-byte loads; d_v and
-    // every stride are multiples of 8 and d_v is at most 128 for the 16-bit
-    // kernels, so one load per lane and row).  All loads of a group, LSE included, are issued before
-    // the first reduction so that each half warp keeps RPH rows in flight.
-    constexpr int RPH = 4;
+    // every stride are multiples of 8; d_v is at most 128, one load per lane
+    // and row, or 256, two).  All loads of a group, LSE included, are issued
+    // before the first reduction so that each half warp keeps RPH rows in flight.
+    constexpr int RPH = 4 / VW;
     const int sub = lane & 15;
     const long long hw = tid >> 4, nhw = nthreads >> 4;
     const uint4* O = static_cast<const uint4*>(P.o);
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
     // the trip count is warp-uniform (the shuffles below take the full mask)
     for (long long w0 = (hw >> 1) * 2 * RPH; w0 < nrows; w0 += nhw * RPH) {
       const long long r0 = w0 + (hw & 1) * RPH;
-      uint4 a[RPH], b[RPH];
+      uint4 a[RPH], b[RPH], a2[VW == 2 ? RPH : 1], b2[VW == 2 ? RPH : 1];
       long long li[RPH];
       float l[RPH];
       // (token, head) and, in batch mode, (batch, query) of the first row by
@@ -332,6 +333,11 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
         const bool ok = r < nrows && sub < nv;
         a[i] = ok ? __ldcs(O + (oo >> 3) + sub) : z;
         b[i] = ok ? __ldcs(dO + (od >> 3) + sub) : z;
+        if constexpr (VW == 2) {   // d_v = 256: the second half of the row
+          const bool ok2 = r < nrows && sub + 16 < nv;
+          a2[i] = ok2 ? __ldcs(O + (oo >> 3) + sub + 16) : z;
+          b2[i] = ok2 ? __ldcs(dO + (od >> 3) + sub + 16) : z;
+        }
         li[i] = P.group ? (long long)h * P.tq + tok : (bq * P.hq + h) * P.sq + q;
         l[i] = (sub == 0 && r < nrows && ATTN_INDEX_OK(P, li[i] >= 0 && li[i] < P.n_lse, 8)) ? P.lse[li[i]] : 0.f;
         if (++h == P.hq) {
@@ -348,6 +354,7 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
 #pragma unroll
       for (int i = 0; i < RPH; ++i) {
         float acc = dot8(a[i], b[i], (T*)nullptr);
+        if constexpr (VW == 2) acc += dot8(a2[i], b2[i], (T*)nullptr);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         if (sub == 0 && r0 + i < nrows && li[i] >= 0 && li[i] < P.n_lse) store_row_stats(P, li[i], l[i], acc);
@@ -408,10 +415,17 @@ static int num_sms() {
 static void launch_preprocess_sched(const Problem& P, cudaStream_t st, int sched) {
   const long long ntok = P.group ? (long long)P.tq : (long long)P.nseg * P.sq;
   const int grid = num_sms() * PRE_BLOCKS_PER_SM;   // one resident wave
+  const bool wide = P.dv > 128;
   switch (P.dtype) {
-    case ATTN_BF16: preprocess_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(P, ntok, sched); break;
-    case ATTN_FP16: preprocess_kernel<__half><<<grid, 256, 0, st>>>(P, ntok, sched); break;
-    default: preprocess_kernel<float><<<grid, 256, 0, st>>>(P, ntok, sched); break;
+    case ATTN_BF16:
+      if (wide) preprocess_kernel<__nv_bfloat16, 2><<<grid, 256, 0, st>>>(P, ntok, sched);
+      else preprocess_kernel<__nv_bfloat16, 1><<<grid, 256, 0, st>>>(P, ntok, sched);
+      break;
+    case ATTN_FP16:
+      if (wide) preprocess_kernel<__half, 2><<<grid, 256, 0, st>>>(P, ntok, sched);
+      else preprocess_kernel<__half, 1><<<grid, 256, 0, st>>>(P, ntok, sched);
+      break;
+    default: preprocess_kernel<float, 1><<<grid, 256, 0, st>>>(P, ntok, sched); break;
   }
 }
 
@@ -495,10 +509,16 @@ __device__ __forceinline__ void reduce_convert_tile(const Problem& P, long long 
       return kt;
     };
     for (int k0 = next(0); k0 < nkv;) {
-      const int k1 = next(k0 + 1);
-      if (ATTN_INDEX_OK(P, k0 < P.nsplits && t < P.ntiles, 10))
-        add_tiles(dq_tile(P, k0, h, t), k1 < nkv ? dq_tile(P, k1, h, t) : nullptr);
-      k0 = k1 < nkv ? next(k1 + 1) : nkv;
+      if constexpr (NACC > 8) {
+        // d_qk = 256: one slice in flight at a time (register budget)
+        if (ATTN_INDEX_OK(P, k0 < P.nsplits && t < P.ntiles, 10)) add_tiles(dq_tile(P, k0, h, t), nullptr);
+        k0 = next(k0 + 1);
+      } else {
+        const int k1 = next(k0 + 1);
+        if (ATTN_INDEX_OK(P, k0 < P.nsplits && t < P.ntiles, 10))
+          add_tiles(dq_tile(P, k0, h, t), k1 < nkv ? dq_tile(P, k1, h, t) : nullptr);
+        k0 = k1 < nkv ? next(k1 + 1) : nkv;
+      }
     }
   } else if (s.lk > 0) {   // atomic and ordered fold: the single, pre-zeroed slice
 #pragma unroll
@@ -561,7 +581,8 @@ static void launch_rc(const Problem& P, long long work, cudaStream_t st) {
   const int nacc = cdiv(P.dqk * BM / 4, RC_THREADS);
   if (nacc <= 4) launch_rc_kernel(reduce_convert_kernel<T, 4, SPLIT>, P, work, !SPLIT, st);
   else if (nacc <= 8) launch_rc_kernel(reduce_convert_kernel<T, 8, SPLIT>, P, work, !SPLIT, st);
-  else launch_rc_kernel(reduce_convert_kernel<T, 12, SPLIT>, P, work, !SPLIT, st);
+  else if (nacc <= 12) launch_rc_kernel(reduce_convert_kernel<T, 12, SPLIT>, P, work, !SPLIT, st);
+  else launch_rc_kernel(reduce_convert_kernel<T, 16, SPLIT>, P, work, !SPLIT, st);
 }
 
 template <typename T>

@@ -94,9 +94,10 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Workspace layout: pure function of the scalar problem fields, used by both
 // attn_bwd_workspace_size and attn_bwd.
 // Deterministic dQ by the ordered fold: the tensor-core kernel in
-// ATTN_DET_ORDERED mode (the fp32 kernel always uses split slices).
+// ATTN_DET_ORDERED mode with one pass per KV tile (the fp32 kernel and the
+// two-pass head dim 256 use split slices).
 inline bool det_fold(const attn_bwd_params& p) {
-  return p.deterministic == ATTN_DET_ORDERED && p.dtype != ATTN_FP32;
+  return p.deterministic == ATTN_DET_ORDERED && p.dtype != ATTN_FP32 && p.d_qk <= 192;
 }
 
 inline WsLayout ws_layout(const attn_bwd_params& p) {

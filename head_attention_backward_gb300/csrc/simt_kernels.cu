@@ -16,7 +16,8 @@ constexpr int FWD_BQ = 64;   // query rows per block
 constexpr int FWD_BK = 64;   // keys per tile
 constexpr int FWD_THREADS = 256;
 
-template <typename T>
+// NC: output columns per thread (d_v <= 4 NC).
+template <typename T, int NC>
 __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, FwdLayout L, int group) {
   extern __shared__ float smem[];
   const int dqk = p.d_qk, dv = p.d_v;
@@ -59,9 +60,9 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, Fwd
 
   const int row = tid >> 2, sub = tid & 3;
   const int ncol = (dv + 3) / 4;   // output columns of this thread: sub, sub+4, ...
-  float acc[32];
+  float acc[NC];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  for (int i = 0; i < NC; ++i) acc[i] = 0.f;
   float mrow = -INFINITY, lrow = 0.f;
   const float sl2 = p.softmax_scale * 1.4426950408889634f;
 
@@ -143,23 +144,28 @@ size_t fwd_smem_bytes(int dqk, int dv) {
                           (size_t)FWD_BK * dv + (size_t)FWD_BQ * (FWD_BK + 1));
 }
 
+template <typename T, int NC>
+static void launch_fwd_typed(const attn_fwd_params& p, const FwdLayout& L, dim3 grid, size_t smem, int group,
+                             cudaStream_t st) {
+  cudaFuncSetAttribute(fwd_kernel<T, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  fwd_kernel<T, NC><<<grid, FWD_THREADS, smem, st>>>(p, L, group);
+}
+
+template <typename T>
+static void launch_fwd_dtype(const attn_fwd_params& p, const FwdLayout& L, dim3 grid, size_t smem, int group,
+                             cudaStream_t st) {
+  if (p.d_v > 128) launch_fwd_typed<T, 64>(p, L, grid, smem, group, st);
+  else launch_fwd_typed<T, 32>(p, L, grid, smem, group, st);
+}
+
 void launch_fwd(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
   const int group = p.cu_seqlens_q != nullptr;
   dim3 grid(cdiv(p.seqlen_q, FWD_BQ), p.nhead_q, p.batch);
   const size_t smem = fwd_smem_bytes(p.d_qk, p.d_v);
   switch (p.dtype) {
-    case ATTN_BF16:
-      cudaFuncSetAttribute(fwd_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      fwd_kernel<__nv_bfloat16><<<grid, FWD_THREADS, smem, st>>>(p, L, group);
-      break;
-    case ATTN_FP16:
-      cudaFuncSetAttribute(fwd_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      fwd_kernel<__half><<<grid, FWD_THREADS, smem, st>>>(p, L, group);
-      break;
-    default:
-      cudaFuncSetAttribute(fwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      fwd_kernel<float><<<grid, FWD_THREADS, smem, st>>>(p, L, group);
-      break;
+    case ATTN_BF16: launch_fwd_dtype<__nv_bfloat16>(p, L, grid, smem, group, st); break;
+    case ATTN_FP16: launch_fwd_dtype<__half>(p, L, grid, smem, group, st); break;
+    default: launch_fwd_dtype<float>(p, L, grid, smem, group, st); break;
   }
 }
 

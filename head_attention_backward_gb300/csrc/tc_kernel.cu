@@ -71,12 +71,21 @@ struct TmaMaps {
 
 template <int DQK, int DV>
 struct Cfg {
+  // Head dims above 192 (256): dK, dV and dQ^T of a 128-key tile do not fit
+  // TMEM at full width, so each item runs NPASS passes over its query tiles,
+  // pass p accumulating the 128 columns [128 p, 128 p + 128) of dK, dV and
+  // dQ (S^T and dP^T are recomputed at full depth in every pass).
+  static constexpr int DA = DQK > 192 ? 128 : DQK;      // dK / dQ columns per pass
+  static constexpr int DVA = DQK > 192 ? 128 : DV;      // dV columns per pass
+  static constexpr int NPASS = DQK / DA;
+  static_assert(NPASS == 1 || (DQK == DV && DQK == NPASS * DA), "multi-pass needs d_qk == d_v");
   static constexpr int NCK = DQK / 64;                  // 64-wide chunks of q/k rows
   static constexpr int NCV = DV / 64;                   // chunks of v/o rows
+  static constexpr int NCA = DA / 64;                   // chunks of one pass's columns
   static constexpr int DQK_PAD = (DQK + 127) / 128 * 128;
   static constexpr int NCK_PAD = DQK_PAD / 64;          // k chunks incl. zero padding
-  static constexpr int NMB = DQK_PAD / 128;             // M blocks of dQ^T
-  static constexpr int ST = DQK <= 128 ? 3 : 2;         // Q/dO pipeline stages
+  static constexpr int NMB = (DA + 127) / 128;          // M blocks of dQ^T per pass
+  static constexpr int ST = DQK <= 128 ? 3 : DQK <= 192 ? 2 : 1;   // Q/dO pipeline stages
   static constexpr int KCH = BN * 128;                  // bytes of one 64-wide k/v chunk
   static constexpr int QCH = BM * 128;                  // bytes of one 64-wide q/dO chunk
   // shared memory map (1024-byte aligned regions)
@@ -95,8 +104,8 @@ struct Cfg {
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + NR * 8 + 1024;  // + alignment slack
   // TMEM column map; the two P^T buffers (bf16, two per column) are MMA A operands
   static constexpr int T_DK = 0;
-  static constexpr int T_DV = DQK;
-  static constexpr int T_S = DQK + DV;
+  static constexpr int T_DV = DA;
+  static constexpr int T_S = DA + DVA;
   static constexpr int T_DP = T_S + BM;
   static constexpr bool ALIAS = T_DP + BM + NMB * BM + BM > (int)TMEM_COLS;
   static constexpr int T_DQ = ALIAS ? T_S : T_DP + BM;
@@ -249,6 +258,7 @@ template <int DQK, int DV, typename T, int DQM>
 __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const __grid_constant__ TmaMaps maps, const Problem P) {
   using C = Cfg<DQK, DV>;
   constexpr bool FOLD = DQM == DQ_FOLD;
+  static_assert(!FOLD || C::NPASS == 1, "the ordered fold keeps one turn per query tile: single pass only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -355,10 +365,11 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           tma_load_3d(smem + C::OFF_V + c * C::KCH, &maps.v, bar + B_KV_FULL, c * 64, I.hk, krow);
       }
       bool ok = true;
-      for (int s = 0; s < I.nsteps; ++s) {
+      const int nrun = I.nsteps * C::NPASS;   // every pass reloads the query tiles
+      for (int s = 0; s < nrun; ++s) {
         const uint32_t gs = g + s, st = gs % C::ST;
         int h, qt;
-        step_coords(P, I, s, h, qt);
+        step_coords(P, I, C::NPASS == 1 ? s : s % I.nsteps, h, qt);
         if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
         // -LSE*log2(e) and D of the tile's 64 query rows, copied asynchronously;
         // rows past the segment end read as zeros (their columns are masked)
@@ -384,7 +395,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         }
       }
       if (!ok) break;
-      g += I.nsteps;
+      g += nrun;
       ++it;
     }
   } else if (warp == 1 || warp == SDP_ISSUER_WARP) {
@@ -399,8 +410,8 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       constexpr bool F16 = IsHalf<T>::value;
       constexpr uint32_t ID_SDP = idesc_f16(128, BM, false, false, F16);
       constexpr uint32_t ID_DQ = idesc_f16(128, BM, true, true, F16);
-      constexpr uint32_t ID_DV = idesc_f16(128, DV, false, true, F16);
-      constexpr uint32_t ID_DK = idesc_f16(128, DQK, false, true, F16);
+      constexpr uint32_t ID_DV = idesc_f16(128, C::DVA, false, true, F16);
+      constexpr uint32_t ID_DK = idesc_f16(128, C::DA, false, true, F16);
       // Descriptors of each operand's first 16-element K step; later steps add
       // (byte offset >> 4) to the start-address field (no carry: smem < 256 KB).
       const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);          // K-major
@@ -412,7 +423,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       const uint64_t ddO_k = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
       const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::QCH, 1024);
       const uint64_t ddO_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::QCH, 1024);
-      uint32_t g = 0, it = 0, n_item = 0;
+      uint32_t g = 0, it = 0, n_item = 0, kvp = 0;   // kvp: dK/dV accumulations handed to the drain
       bool ok = true;
       // The MMA groups are issued from straight-line code: a tcgen05.mma
       // sequence chosen per iteration by an if/else measured about twice as
@@ -454,13 +465,15 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         return wait_bar(ctx, B_PDS_FULL + (gs & 1), (gs >> 1) & 1, 15);
       };
       // dV += P^T dO (P^T from TMEM) and dK += dS^T Q (dS^T from shared
-      // memory, K-major) of step gs; their commit frees the Q/dO stage.
-      auto mma_dvdk = [&](uint32_t gs, uint32_t acc_first) {
+      // memory, K-major) of step gs, for the columns of pass `pass`; their
+      // commit frees the Q/dO stage.
+      auto mma_dvdk = [&](uint32_t gs, uint32_t acc_first, int pass) {
 #ifdef ATTN_WAIT_STATS
         const long long t0 = clock64();
 #endif
         const uint32_t st = gs % C::ST, pb = gs & 1;
-        const uint64_t q = dQ_mn + ((st * C::NCK * C::QCH) >> 4), d = ddO_mn + ((st * C::NCV * C::QCH) >> 4);
+        const uint64_t q = dQ_mn + (((st * C::NCK + pass * C::NCA) * C::QCH) >> 4),
+                       d = ddO_mn + (((st * C::NCV + pass * C::NCA) * C::QCH) >> 4);
         const uint64_t a_ds = ddS_k + ((pb * C::DS_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
@@ -478,15 +491,16 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       auto wait_dq = [&](uint32_t gs) -> bool {
         return C::ALIAS || wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16);
       };
-      // dQ^T = K^T dS^T of step gs; its commit also frees the P/dS buffer.
-      auto mma_dq = [&](uint32_t gs) {
+      // dQ^T = K^T dS^T of step gs (the rows of pass `pass`); its commit
+      // also frees the P/dS buffer.
+      auto mma_dq = [&](uint32_t gs, int pass) {
         const uint32_t pb = gs & 1;
         const uint64_t b_ds = ddS_mn + ((pb * C::DS_BYTES) >> 4);
 #pragma unroll
         for (int mb = 0; mb < C::NMB; ++mb) {
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks) {
-            umma_ss(tmem + C::T_DQ + mb * BM, dK_mn + ((mb * 2 * C::KCH + ks * 2048) >> 4),
+            umma_ss(tmem + C::T_DQ + mb * BM, dK_mn + (((pass * C::NCA + mb * 2) * C::KCH + ks * 2048) >> 4),
                     b_ds + ((ks * 2048) >> 4), ID_DQ, ks > 0);
           }
         }
@@ -502,7 +516,8 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         if (item.x < 0) break;
         const ItemInfo I = item_info(P, item);
         if (I.nsteps == 0) continue;
-        const uint32_t last = g + I.nsteps - 1;
+        const int nrun = I.nsteps * C::NPASS;
+        const uint32_t last = g + nrun - 1;
         if (is_sdp) {
           if (!(ok = wait_bar(ctx, B_KV_FULL, it & 1, 14))) break;
           for (uint32_t gs = g; gs <= last; ++gs) {
@@ -511,23 +526,33 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
             mma_sdp(gs);
           }
         } else {
-          if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (it & 1) ^ 1, 17))) break;
+          if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (kvp & 1) ^ 1, 17))) break;
           for (uint32_t gs = g; gs <= last; ++gs) {
+            const int pass = C::NPASS == 1 ? 0 : (int)(gs - g) / I.nsteps;
+            const bool pass_first = C::NPASS == 1 ? gs == g : (int)(gs - g) == pass * I.nsteps;
+            if (C::NPASS > 1 && pass_first && pass > 0) {
+              // the previous pass's dK/dV columns are complete: to the drain,
+              // and wait until it has read them before accumulating the next
+              umma_commit(bar + B_DKV_FULL);
+              ++kvp;
+              if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (kvp & 1) ^ 1, 17))) break;
+            }
             if (!(ok = wait_pds(gs))) break;
             tc_fence_after();
-            mma_dvdk(gs, gs != g);
+            mma_dvdk(gs, pass_first ? 0u : 1u, pass);
             if (!(ok = wait_dq(gs))) break;
             tc_fence_after();
-            mma_dq(gs);
+            mma_dq(gs, pass);
           }
           if (!ok) break;
           // the item's last dQ/dV/dK followed its last P/dS, which followed
           // every S/dP of the item: K/V and the dK/dV accumulators are done
           umma_commit(bar + B_KV_EMPTY);
           umma_commit(bar + B_DKV_FULL);
+          ++kvp;
         }
         if (!ok) break;
-        g += I.nsteps;
+        g += nrun;
         ++it;
       }
       // make sure no MMA of this issuer is in flight before TMEM is released
@@ -558,10 +583,11 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       const int kk = I.kt * BN + r;                    // segment-local key index
       const bool key_ok = r < I.klen;
       bool ok = true;
-      for (int s = 0; s < I.nsteps; ++s) {
+      const int nrun = I.nsteps * C::NPASS;   // every pass recomputes P and dS
+      for (int s = 0; s < nrun; ++s) {
         const uint32_t gs = g + s, st = gs % C::ST;
         int h, qt;
-        step_coords(P, I, s, h, qt);
+        step_coords(P, I, C::NPASS == 1 ? s : s % I.nsteps, h, qt);
         if (!(ok = wait_bar(ctx, B_SDP_FULL, gs & 1, 21))) break;
         tc_fence_after();
         uint32_t sv[CW], dpv[CW];
@@ -621,7 +647,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         if (lane == 0) mbar_arrive(bar + B_PDS_FULL + pb);
       }
       if (!ok) break;
-      g += I.nsteps;
+      g += nrun;
     }
   } else if (FOLD && warp == TURN_WARP) {
     // ------------------------------------------- ordered fold: turn thread
@@ -665,7 +691,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     T* dKg = static_cast<T*>(P.dk);
     T* dVg = static_cast<T*>(P.dv_out);
-    uint32_t g = 0, it = 0, n_item = 0;
+    uint32_t g = 0, kvp = 0, n_item = 0;   // kvp: dK/dV accumulations written out
     while (true) {
       const int slot = n_item % NI;
       if (!wait_bar(ctx, B_IT_FULL + slot, (n_item / NI) & 1, 30)) break;
@@ -689,11 +715,62 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         }
         continue;
       }
+      // dK (scaled) and dV of this lane's key row, the columns of pass `pass`,
+      // once the issuer has committed them; then the accumulators are free
+      auto write_dkdv = [&](int pass) -> bool {
+        if (!wait_bar(ctx, B_DKV_FULL, kvp & 1, 32)) return false;
+        tc_fence_after();
+        const bool row_ok = L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P), 2);
+#pragma unroll 1
+        for (int ch = 0; ch < C::DA / 32; ++ch) {
+          uint32_t x[32];
+          tmem_ld32(lane_addr + C::T_DK + ch * 32, x);
+          tmem_wait_ld();
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dKg + kofs + pass * C::DA + ch * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 w;
+              w.x = pack2(__uint_as_float(x[8 * j + 0]) * P.scale, __uint_as_float(x[8 * j + 1]) * P.scale, (T*)nullptr);
+              w.y = pack2(__uint_as_float(x[8 * j + 2]) * P.scale, __uint_as_float(x[8 * j + 3]) * P.scale, (T*)nullptr);
+              w.z = pack2(__uint_as_float(x[8 * j + 4]) * P.scale, __uint_as_float(x[8 * j + 5]) * P.scale, (T*)nullptr);
+              w.w = pack2(__uint_as_float(x[8 * j + 6]) * P.scale, __uint_as_float(x[8 * j + 7]) * P.scale, (T*)nullptr);
+              dst[j] = w;
+            }
+          }
+        }
+#pragma unroll 1
+        for (int ch = 0; ch < C::DVA / 32; ++ch) {
+          uint32_t x[32];
+          tmem_ld32(lane_addr + C::T_DV + ch * 32, x);
+          tmem_wait_ld();
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dVg + vofs + pass * C::DVA + ch * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 w;
+              w.x = pack2(__uint_as_float(x[8 * j + 0]), __uint_as_float(x[8 * j + 1]), (T*)nullptr);
+              w.y = pack2(__uint_as_float(x[8 * j + 2]), __uint_as_float(x[8 * j + 3]), (T*)nullptr);
+              w.z = pack2(__uint_as_float(x[8 * j + 4]), __uint_as_float(x[8 * j + 5]), (T*)nullptr);
+              w.w = pack2(__uint_as_float(x[8 * j + 6]), __uint_as_float(x[8 * j + 7]), (T*)nullptr);
+              dst[j] = w;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar + B_DKV_EMPTY);
+        ++kvp;
+        return true;
+      };
       bool ok = true;
-      for (int s = 0; s < I.nsteps; ++s) {
+      const int nrun = I.nsteps * C::NPASS;
+      for (int s = 0; s < nrun; ++s) {
         const uint32_t gs = g + s;
+        const int pass = C::NPASS == 1 ? 0 : s / I.nsteps;
+        const int sl = C::NPASS == 1 ? s : s - pass * I.nsteps;
         int h, qt;
-        step_coords(P, I, s, h, qt);
+        step_coords(P, I, sl, h, qt);
         const int tile = qtile_index(P, I.b, qt);
         // ordered fold: this partial is number `rank` of the tile's sum; lane 0
         // of each warp reads the tile's counter before the dQ tile is ready
@@ -711,7 +788,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
                                                 (DQM != DQ_SPLIT || (I.kt >= 0 && I.kt < P.nsplits)), 1);
 #pragma unroll 1
         for (int mb = 0; mb < C::NMB && ok; ++mb) {
-          const int rows = min(128, DQK - mb * 128);
+          const int rows = min(128, C::DA - mb * 128);
 #pragma unroll 1
           for (int hx = 0; hx < 2; ++hx) {     // query columns 0-31, then 32-63
             uint32_t v[32];
@@ -738,7 +815,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
               // store measured ~20% slower on the whole kernel, 16-byte
               // row-segment stores slower still, d-major vector reductions
               // slower again.)
-              float* dst = dst_tile + mb * 128 + L + hx * 32 * DQK;
+              float* dst = dst_tile + pass * C::DA + mb * 128 + L + hx * 32 * DQK;
               if constexpr (DQM == DQ_SPLIT) {   // plain store into this KV tile's slice
 #pragma unroll
                 for (int c = 0; c < 32; ++c) __stcg(dst + c * DQK, __uint_as_float(v[c]));
@@ -764,52 +841,12 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
+        // multi-pass: the dK/dV columns of a pass are complete after its last step
+        if (C::NPASS > 1 && sl == I.nsteps - 1 && pass < C::NPASS - 1 && !(ok = write_dkdv(pass))) break;
       }
       if (!ok) break;
-      g += I.nsteps;
-      if (!wait_bar(ctx, B_DKV_FULL, it & 1, 32)) break;
-      tc_fence_after();
-      const bool row_ok = L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P), 2);
-#pragma unroll 1
-      for (int ch = 0; ch < DQK / 32; ++ch) {
-        uint32_t x[32];
-        tmem_ld32(lane_addr + C::T_DK + ch * 32, x);
-        tmem_wait_ld();
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dKg + kofs + ch * 32);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 w;
-            w.x = pack2(__uint_as_float(x[8 * j + 0]) * P.scale, __uint_as_float(x[8 * j + 1]) * P.scale, (T*)nullptr);
-            w.y = pack2(__uint_as_float(x[8 * j + 2]) * P.scale, __uint_as_float(x[8 * j + 3]) * P.scale, (T*)nullptr);
-            w.z = pack2(__uint_as_float(x[8 * j + 4]) * P.scale, __uint_as_float(x[8 * j + 5]) * P.scale, (T*)nullptr);
-            w.w = pack2(__uint_as_float(x[8 * j + 6]) * P.scale, __uint_as_float(x[8 * j + 7]) * P.scale, (T*)nullptr);
-            dst[j] = w;
-          }
-        }
-      }
-#pragma unroll 1
-      for (int ch = 0; ch < DV / 32; ++ch) {
-        uint32_t x[32];
-        tmem_ld32(lane_addr + C::T_DV + ch * 32, x);
-        tmem_wait_ld();
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dVg + vofs + ch * 32);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 w;
-            w.x = pack2(__uint_as_float(x[8 * j + 0]), __uint_as_float(x[8 * j + 1]), (T*)nullptr);
-            w.y = pack2(__uint_as_float(x[8 * j + 2]), __uint_as_float(x[8 * j + 3]), (T*)nullptr);
-            w.z = pack2(__uint_as_float(x[8 * j + 4]), __uint_as_float(x[8 * j + 5]), (T*)nullptr);
-            w.w = pack2(__uint_as_float(x[8 * j + 6]), __uint_as_float(x[8 * j + 7]), (T*)nullptr);
-            dst[j] = w;
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar + B_DKV_EMPTY);
-      ++it;
+      g += nrun;
+      if (!write_dkdv(C::NPASS - 1)) break;
     }
   }
 
@@ -952,6 +989,9 @@ static int launch_dims(const Problem& P, cudaStream_t st) {
   if (P.dqk == 128 && P.dv == 128) return launch_typed<128, 128, T, DQM>(P, st);
   if (P.dqk == 64 && P.dv == 64) return launch_typed<64, 64, T, DQM>(P, st);
   if (P.dqk == 192 && P.dv == 128) return launch_typed<192, 128, T, DQM>(P, st);
+  if constexpr (DQM != DQ_FOLD) {
+    if (P.dqk == 256 && P.dv == 256) return launch_typed<256, 256, T, DQM>(P, st);
+  }
   return ATTN_ERR_UNSUPPORTED_HEADDIM;
 }
 

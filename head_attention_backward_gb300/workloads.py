@@ -198,6 +198,12 @@ def window_192(deterministic=True) -> Workload:
                     deterministic=deterministic, seed=5)
 
 
+def gqa_d256(deterministic=True) -> Workload:
+    """Head dim 256 (the widest pair the library takes): GQA, causal."""
+    return Workload("gqa_B1_Hq16_Hkv4_S4096_d256_causal", torch.bfloat16, 1, 16, 4, 4096, 4096, 256, 256,
+                    MASK_CAUSAL_TOP_LEFT, deterministic=deterministic, seed=6)
+
+
 # Fixed splits the THD fix was verified on (PR #671, Verification and the
 # review reply on non-16-multiple lengths).
 PAGE_SPLITS = [[256], [100, 80, 76], [128, 128], [64, 64, 64, 64], [200, 56], [103, 77, 61]]

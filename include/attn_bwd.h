@@ -89,9 +89,12 @@ typedef enum {
 
 /* Element type of q, k, v, o, dout, dq, dk, dv (lse is always fp32).
  * Supported head dims: BF16/FP16 (d_qk, d_v) in {(64,64), (128,128),
- * (192,128)} on the tensor-core kernel; FP32 d_qk in [4, 64] with
- * d_qk % 4 == 0 and d_v in [1, 64] on the fp32 SIMT kernel.  Any other pair
- * returns ATTN_ERR_UNSUPPORTED_HEADDIM before a launch. */
+ * (192,128), (256,256)} on the tensor-core kernel (at (256,256) each KV tile
+ * is processed in two passes over its query tiles, one per 128-column half of
+ * dK, dV and dQ); FP32 d_qk in [4, 64] with d_qk % 4 == 0 and d_v in [1, 64]
+ * on the fp32 SIMT kernel.  Any other pair returns
+ * ATTN_ERR_UNSUPPORTED_HEADDIM before a launch (the loud head-dim check asked
+ * for in the review of TE PR #671). */
 typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1, ATTN_FP32 = 2 } attn_dtype_t;
 
 typedef struct {
@@ -197,7 +200,8 @@ typedef struct {
  *   ATTN_DET_ORDERED: in ascending KV-tile order, each partial added into one
  *     fp32 dq_acc tile in turn (a per-tile turn counter serialises the adds,
  *     so the sum is bitwise repeatable; partials never leave the L2 cache
- *     as separate slices).  FP32 inputs use the split slices instead;
+ *     as separate slices).  FP32 inputs and head dim 256 (whose two passes add
+ *     each partial in two column halves) use the split slices instead;
  *   ATTN_DET_SPLIT: each partial stored to its own dq_acc slice, nsplits =
  *     ceil(seqlen_k / 128), then summed in ascending slice order by a
  *     reduction kernel -- the split workspace of aiter PR #2216 (Motivation).
@@ -216,7 +220,7 @@ typedef enum { ATTN_DET_ATOMIC = 0, ATTN_DET_ORDERED = 1, ATTN_DET_SPLIT = 2 } a
  * group mode (each segment's rows start a new tile: a per-segment padded
  * layout, the kind TransformerEngine PR #671's Fix switches dq_acc to, with
  * one layout shared by the sizing call and the kernels).  ATTN_DET_SPLIT (and
- * ATTN_DET_ORDERED with FP32 inputs) uses nsplits = ceil(seqlen_k / 128)
+ * ATTN_DET_ORDERED with FP32 inputs or d_qk = 256) uses nsplits = ceil(seqlen_k / 128)
  * slices, the other modes one; ATTN_DET_ORDERED adds a turn counter per
  * query tile and head.  Small per-row and per-tile tables come on top.
  * Writes the size to *bytes.  Returns ATTN_OK or an error code. */

@@ -116,6 +116,14 @@ def test_workspace_size_fp32_ordered_uses_split_slices(lib):
     assert n >= (4096 // 128) * 2 * 32 * 4096 * 64 * 4
 
 
+def test_workspace_size_head_dim_256_ordered_uses_split_slices(lib):
+    """d_qk = 256 runs two passes per KV tile (one per column half), so the
+    deterministic request is served by the split slices."""
+    st, n = B.attn_bwd_workspace_size(make(d_qk=256, d_v=256, deterministic=B.DET_ORDERED))
+    assert st == 0
+    assert n >= (4096 // 128) * 2 * 32 * 4096 * 256 * 4
+
+
 def test_workspace_size_atomic_one_slice(lib):
     st, n = B.attn_bwd_workspace_size(make(deterministic=0))
     assert st == 0
@@ -159,6 +167,9 @@ ERR = dict(inv=-1, hd=-2, ws=-3)
     (dict(d_qk=96, d_v=96), "hd"),
     (dict(d_qk=128, d_v=64), "hd"),
     (dict(dtype=B.ATTN_FP32, d_qk=128, d_v=128), "hd"),
+    (dict(d_qk=256, d_v=128), "hd"),
+    (dict(d_qk=320, d_v=320), "hd"),
+    (dict(dtype=B.ATTN_FP32, d_qk=256, d_v=256), "hd"),
     (dict(q=None), "inv"),
     (dict(dq=0x10008), "inv"),          # not 16-byte aligned
 ])
@@ -307,7 +318,7 @@ def test_fwd_rejects_bad_args(lib):
     p.nhead_kv = 2
     assert B.attn_fwd(p, 0) == -1          # null pointers
     p.q, p.k, p.v, p.o, p.lse = 0x1000, 0x2000, 0x3000, 0x4000, 0x5000
-    p.d_qk = 256
+    p.d_qk = 320
     assert B.attn_fwd(p, 0) == -2
     p.d_qk = 64
     p.o = 0x4002                           # O is written with 16-byte vector stores

@@ -87,6 +87,15 @@ def test_window_dqk192_dv128_S8192(B, det):
     assert_all_ok(_check_batch(wl, x, got, [(0, 0), (0, 15)], [(0, 5)], 5), f"window det={det}")
 
 
+@pytest.mark.parametrize("det", [0, 1], ids=["atomic", "det"])
+def test_head_dim_256_B1_Hq16_Hkv4_S4096(B, det):
+    """Head dim 256: two passes per KV tile, one per column half of dK, dV, dQ
+    (the deterministic request runs on the split slices)."""
+    wl = W.gqa_d256(deterministic=det)
+    x, _, got = _run(B, wl, det)
+    assert_all_ok(_check_batch(wl, x, got, [(0, 0), (0, 15), (0, 6)], [(0, 0), (0, 3)], 6), f"d256 det={det}")
+
+
 @pytest.mark.parametrize("det", [0, 1, 2], ids=["atomic", "ordered", "split"])
 def test_thd_packed_T16384_every_segment(B, det):
     """The packed THD workload's dq_acc slice (about 270 MB) is over the

@@ -16,7 +16,7 @@ from tests.parity import assert_all_ok
 
 pytestmark = pytest.mark.gpu
 
-DIMS = [(64, 64), (128, 128), (192, 128)]
+DIMS = [(64, 64), (128, 128), (192, 128), (256, 256)]
 
 
 def _case(i):
@@ -48,7 +48,7 @@ def _case(i):
     return wl, det
 
 
-@pytest.mark.parametrize("i", range(24))
+@pytest.mark.parametrize("i", range(32))
 def test_random_problem(B, i):
     wl, det = _case(i)
     assert_all_ok(run_backward_vs_oracle(B, wl, det), f"case {i}: {wl} det={det}")

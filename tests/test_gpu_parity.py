@@ -87,6 +87,9 @@ SMALL = [
     _wl("bf16_d64_causal", torch.bfloat16, 2, 2, 1, 200, 200, 64, 64, W.MASK_CAUSAL_TOP_LEFT, seed=10),
     _wl("bf16_d192_window", torch.bfloat16, 1, 2, 2, 400, 400, 192, 128, W.MASK_WINDOW, 150, 0, seed=11),
     _wl("fp16_causal", torch.float16, 1, 2, 2, 200, 200, 128, 128, W.MASK_CAUSAL_TOP_LEFT, seed=12),
+    _wl("bf16_d256_causal_ragged", torch.bfloat16, 2, 4, 2, 300, 300, 256, 256, W.MASK_CAUSAL_TOP_LEFT, seed=13),
+    _wl("fp16_d256_window_sq_ne_sk", torch.float16, 1, 2, 1, 200, 333, 256, 256, W.MASK_WINDOW, 90, 10, seed=14),
+    _wl("bf16_d256_nomask_one_tile", torch.bfloat16, 1, 2, 2, 64, 128, 256, 256, W.MASK_NONE, seed=15),
 ]
 
 
