@@ -44,6 +44,24 @@ Layouts (the same as the C ABI): batch mode q [B,Sq,Hq,d], k [B,Sk,Hkv,d],
 v [B,Sk,Hkv,dv], o/do [B,Sq,Hq,dv], lse [B,Hq,Sq]; group mode drops B and
 uses the packed token axis: q [Tq,Hq,d], lse [Hq,Tq].
 
+Attention bias and dropout (TransformerEngine PR #446: the bias of shape
+(bias_b, bias_h, s_q, s_kv) in the BiasShape kinds 11SS / 1HSS / BHSS / B1SS,
+batch mode only, dbias returned in the BHSS shape; dropout driven by a philox
+seed / offset pair passed to the backward):
+
+8. The bias is added to the scaled scores before the mask:
+   S = s Q K^T + bias[b', h'] with b' = b, h' = h on the dimensions the shape
+   has and 0 on the broadcast ones; dbias[b, h] = dS (the gradient of the
+   biased scores), in the full [B, Hq, Sq, Sk] shape.
+9. Dropout keeps weight (i, j) of (batch or segment b, query head h) when a
+   Philox4x32-10 word (Salmon, Moraes, Dror and Shaw, "Parallel random
+   numbers: as easy as 1, 2, 3", SC'11) is at least floor(p * 2^32): key =
+   (seed mod 2^32, seed div 2^32); counter = (lo32(n), j, b * Hq + h,
+   hi32(n)) with n = offset + (i div 4); the word is number (i mod 4) of the
+   four.  O = (P o Z / (1 - p)) V, LSE is that of P; in the backward
+   dV = (P o Z / (1 - p))^T dO, dP = (dO V^T) o Z / (1 - p),
+   dS = P o (dP - D) with D = rowsum(dO o O) as before.
+
 Pins (tests/test_oracle.py): central finite differences, closed forms
 (one visible key, constant keys), the exact invariants sum_j dS_ij = 0,
 sum dV = sum dO, <Q,dQ> = <K,dK>, the block-diagonal and GQA invariants,
@@ -94,6 +112,61 @@ def visible(lq: int, lk: int, mask: int, left: int = -1, right: int = -1) -> tor
     return ok
 
 
+# ---------------------------------------------------------------------------
+# Philox counter-based generator, written from its published definition
+# (Salmon et al., SC'11): N = 4 words of W bits, key of 2 words; each of the R
+# rounds multiplies words 0 and 2 by M0 and M1 (full 2W-bit products), the
+# outputs are (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
+# lo(M0 c0)), and the key is bumped by the Weyl constants (W0, W1) between
+# rounds.  The W = 64 instance is compared with numpy's Philox bit generator
+# in the tests; the dropout mask uses W = 32.
+# ---------------------------------------------------------------------------
+PHILOX_CONSTANTS = {
+    32: (0xD2511F53, 0xCD9E8D57, 0x9E3779B9, 0xBB67AE85),
+    64: (0xD2E7470EE14C6C93, 0xCA5A826395121157, 0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B),
+}
+
+
+def philox(ctr, key, width=32, rounds=10):
+    """Philox-4xW-R on Python ints or (for W = 32) numpy uint64 arrays holding
+    W-bit values; returns the four output words."""
+    m0, m1, w0, w1 = PHILOX_CONSTANTS[width]
+    mask = (1 << width) - 1
+    c0, c1, c2, c3 = ctr
+    k0, k1 = key
+    for r in range(rounds):
+        if r > 0:
+            k0, k1 = (k0 + w0) & mask, (k1 + w1) & mask
+        p0, p1 = c0 * m0, c2 * m1          # W = 32: exact in uint64
+        c0, c1, c2, c3 = (p1 >> width) ^ c1 ^ k0, p1 & mask, (p0 >> width) ^ c3 ^ k1, p0 & mask
+    return c0, c1, c2, c3
+
+
+def dropout_keep(lq: int, lk: int, bh: int, p: float, seed: int, offset: int) -> torch.Tensor:
+    """Boolean [lq, lk] keep mask of one (batch or segment, query head) pair,
+    bh = b * Hq + h (reading 9)."""
+    import numpy as np
+    u64 = np.uint64
+    i = np.arange(lq, dtype=np.uint64).reshape(-1, 1)
+    j = np.arange(lk, dtype=np.uint64).reshape(1, -1)
+    n = (u64(offset) + (i >> u64(2))) & u64(0xFFFFFFFFFFFFFFFF)
+    m32 = u64(0xFFFFFFFF)
+    shape = (lq, lk)
+    ctr = (np.broadcast_to(n & m32, shape).astype(np.uint64), np.broadcast_to(j, shape).astype(np.uint64),
+           np.full(shape, bh, dtype=np.uint64), np.broadcast_to(n >> u64(32), shape).astype(np.uint64))
+    key = (u64(seed & 0xFFFFFFFF), u64((seed >> 32) & 0xFFFFFFFF))
+    words = np.stack(philox(ctr, key, 32), axis=0)            # [4, lq, lk]
+    sel = np.broadcast_to((i & u64(3)).astype(np.int64), shape)
+    r = np.take_along_axis(words, sel[None], axis=0)[0]
+    thr = int(math.floor(p * 4294967296.0))
+    return torch.from_numpy(r >= u64(thr))
+
+
+def _bias_for(bias, b, h):
+    """[Sq, Sk] bias of batch entry b, query head h (broadcast dims of size 1)."""
+    return bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0]
+
+
 def _rows(cu, st, b):
     """Physical rows of segment b: start st[b] (cu[b] when unpadded), length
     cu[b+1] - cu[b] (reading 7)."""
@@ -118,9 +191,12 @@ def _views(x, batch_mode, b, rows):
     return x[b, rows] if batch_mode else x[rows]
 
 
-def _head_forward(qh, kh, vh, scale, vis):
-    """One head: S = s Q K^T masked, LSE, P, O (all fp64)."""
+def _head_forward(qh, kh, vh, scale, vis, bias=None, keep=None, p_drop=0.0):
+    """One head: S = s Q K^T (+ bias) masked, LSE, P, O = (P o Z / (1 - p)) V
+    (all fp64); returns P before dropout."""
     s = scale * (qh @ kh.T)
+    if bias is not None:
+        s = s + bias
     s = s.masked_fill(~vis, -math.inf)
     m = s.max(dim=1, keepdim=True).values
     has = torch.isfinite(m)
@@ -129,7 +205,8 @@ def _head_forward(qh, kh, vh, scale, vis):
     lse = (torch.log(e.sum(dim=1, keepdim=True)) + m0).squeeze(1)
     lse = torch.where(has.squeeze(1), lse, torch.full_like(lse, -math.inf))
     p = _probs(s, lse)
-    return p, lse, p @ vh
+    pv = p if keep is None else p * keep.to(F64) / (1.0 - p_drop)
+    return p, lse, pv @ vh
 
 
 def _probs(s, lse):
@@ -144,10 +221,15 @@ def _probs(s, lse):
 
 def attn_forward(q, k, v, scale, mask=MASK_NONE, left=-1, right=-1,
                  cu_seqlens_q=None, cu_seqlens_k=None, cu_seqlens_q_padded=None,
-                 cu_seqlens_k_padded=None):
-    """Forward pass: returns (O, LSE) in fp64 with the layouts of the header."""
+                 cu_seqlens_k_padded=None, bias=None, dropout_p=0.0, philox_seed=0, philox_offset=0):
+    """Forward pass: returns (O, LSE) in fp64 with the layouts of the header.
+    `bias` ([bias_b, bias_h, Sq, Sk], batch mode) and dropout follow readings
+    8 and 9."""
     batch_mode = cu_seqlens_q is None
+    if bias is not None and not batch_mode:
+        raise ValueError("the attention bias is defined for batch mode only")
     q, k, v = _as64(q), _as64(k), _as64(v)
+    bias = None if bias is None else _as64(bias)
     if batch_mode:
         nseg, sq, hq = q.shape[0], q.shape[1], q.shape[2]
         sk, hkv = k.shape[1], k.shape[2]
@@ -167,7 +249,10 @@ def attn_forward(q, k, v, scale, mask=MASK_NONE, left=-1, right=-1,
             continue
         vis = visible(lq, lk, mask, left, right)
         for h in range(hq):
-            _, lse_h, o_h = _head_forward(qb[:, h], kb[:, h // g], vb[:, h // g], scale, vis)
+            keep = dropout_keep(lq, lk, b * hq + h, dropout_p, philox_seed, philox_offset) if dropout_p > 0 else None
+            bias_h = None if bias is None else _bias_for(bias, b, h)
+            _, lse_h, o_h = _head_forward(qb[:, h], kb[:, h // g], vb[:, h // g], scale, vis, bias_h, keep,
+                                          dropout_p)
             if batch_mode:
                 o[b, rq, h] = o_h
                 lse[b, h, rq] = lse_h
@@ -179,17 +264,28 @@ def attn_forward(q, k, v, scale, mask=MASK_NONE, left=-1, right=-1,
 
 def attn_backward(q, k, v, o, do, lse, scale, mask=MASK_NONE, left=-1, right=-1,
                   cu_seqlens_q=None, cu_seqlens_k=None, cu_seqlens_q_padded=None,
-                  cu_seqlens_k_padded=None):
-    """Backward pass given the forward's O and LSE: returns (dQ, dK, dV) fp64.
+                  cu_seqlens_k_padded=None, bias=None, dropout_p=0.0, philox_seed=0, philox_offset=0,
+                  return_dbias=False):
+    """Backward pass given the forward's O and LSE: returns (dQ, dK, dV) fp64,
+    plus dbias [B, Hq, Sq, Sk] when return_dbias.
 
     Per (segment, query head h, kv head g = h // G):
-      S = s Q K^T (masked -> -inf), P = exp(S - LSE), D_i = sum_c dO_ic O_ic,
-      dV_g += P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = s dS K,
-      dK_g += s dS^T Q.
+      S = s Q K^T (+ bias) (masked -> -inf), P = exp(S - LSE),
+      D_i = sum_c dO_ic O_ic, with F = Z / (1 - p) under dropout (else 1):
+      dV_g += (P o F)^T dO, dP = (dO V^T) o F, dS = P o (dP - D),
+      dQ = s dS K, dK_g += s dS^T Q, dbias = dS.
     """
     batch_mode = cu_seqlens_q is None
+    if bias is not None and not batch_mode:
+        raise ValueError("the attention bias is defined for batch mode only")
     q, k, v, o, do, lse = (_as64(t) for t in (q, k, v, o, do, lse))
+    bias = None if bias is None else _as64(bias)
     dq, dk, dv = torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v)
+    dbias = None
+    if return_dbias:
+        if not batch_mode:
+            raise ValueError("dbias is defined for batch mode only")
+        dbias = torch.zeros(q.shape[0], q.shape[2], q.shape[1], k.shape[1], dtype=F64)
     if batch_mode:
         nseg, sq, hq, sk, hkv = q.shape[0], q.shape[1], q.shape[2], k.shape[1], k.shape[2]
     else:
@@ -208,14 +304,24 @@ def attn_backward(q, k, v, o, do, lse, scale, mask=MASK_NONE, left=-1, right=-1,
             kvh = h // g
             lse_h = lse[b, h, rq] if batch_mode else lse[h, rq]
             qh, kh, vh, doh = qb[:, h], kb[:, kvh], vb[:, kvh], dob[:, h]
-            s = (scale * (qh @ kh.T)).masked_fill(~vis, -math.inf)
+            s = scale * (qh @ kh.T)
+            if bias is not None:
+                s = s + _bias_for(bias, b, h)
+            s = s.masked_fill(~vis, -math.inf)
             p = _probs(s, lse_h)
+            f = 1.0
+            if dropout_p > 0:
+                f = dropout_keep(lq, lk, b * hq + h, dropout_p, philox_seed, philox_offset).to(F64) / (1.0 - dropout_p)
             dvec = (doh * ob[:, h]).sum(dim=1)
-            dvb[:, kvh] += p.T @ doh
-            dp = doh @ vh.T
+            dvb[:, kvh] += (p * f).T @ doh
+            dp = (doh @ vh.T) * f
             ds = p * (dp - dvec.view(-1, 1))
             dqb[:, h] = scale * (ds @ kh)
             dkb[:, kvh] += scale * (ds.T @ qh)
+            if dbias is not None:
+                dbias[b, h] = ds
+    if return_dbias:
+        return dq, dk, dv, dbias
     return dq, dk, dv
 
 
