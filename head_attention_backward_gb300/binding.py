@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libattn_bwd.so")
 
 ATTN_BF16, ATTN_FP16, ATTN_FP32 = 0, 1, 2
 MASK_NONE, MASK_CAUSAL_TOP_LEFT, MASK_CAUSAL_BOTTOM_RIGHT, MASK_WINDOW = 0, 1, 2, 3
+BIAS_NONE, BIAS_11SS, BIAS_1HSS, BIAS_BHSS, BIAS_B1SS = 0, 1, 2, 3, 4   # attn_bias_t
 DET_ATOMIC, DET_ORDERED, DET_SPLIT = 0, 1, 2   # attn_det_t
 STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED_HEADDIM",
           -3: "ATTN_ERR_WORKSPACE_TOO_SMALL", -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_DEVICE_FLAG",
@@ -42,7 +43,9 @@ class AttnBwdParams(ctypes.Structure):
                 ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("dout", _vp), ("lse", _vp),
                 ("dq", _vp), ("dk", _vp), ("dv", _vp),
                 ("stride_q", _i64x3), ("stride_k", _i64x3), ("stride_v", _i64x3), ("stride_o", _i64x3),
-                ("stride_dout", _i64x3), ("stride_dq", _i64x3), ("stride_dk", _i64x3), ("stride_dv", _i64x3)]
+                ("stride_dout", _i64x3), ("stride_dq", _i64x3), ("stride_dk", _i64x3), ("stride_dv", _i64x3),
+                ("bias_type", _i32), ("dropout_p", _f32), ("bias", _vp), ("dbias", _vp), ("philox_seed", _vp),
+                ("philox_offset", _vp)]
 
 
 class AttnFwdParams(ctypes.Structure):
@@ -51,7 +54,8 @@ class AttnFwdParams(ctypes.Structure):
                 ("d_qk", _i32), ("d_v", _i32), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
                 ("cu_seqlens_q_padded", _vp), ("cu_seqlens_k_padded", _vp), ("mask", _i32), ("window_left", _i32), ("window_right", _i32),
                 ("softmax_scale", _f32), ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp),
-                ("stride_q", _i64x3), ("stride_k", _i64x3), ("stride_v", _i64x3), ("stride_o", _i64x3)]
+                ("stride_q", _i64x3), ("stride_k", _i64x3), ("stride_v", _i64x3), ("stride_o", _i64x3),
+                ("bias_type", _i32), ("dropout_p", _f32), ("bias", _vp), ("philox_seed", _vp), ("philox_offset", _vp)]
 
 
 class AttnHostTensors(ctypes.Structure):
@@ -215,9 +219,37 @@ def _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k):
                 seqlen_k=max_seqlen_k, total_q=tq, total_k=tk, d_qk=dqk, d_v=dv)
 
 
+def bias_type_of(bias: Optional[torch.Tensor], batch: int, nhead_q: int) -> int:
+    """attn_bias_t of a [bias_b, bias_h, Sq, Sk] bias (bias_b in {1, B}, bias_h
+    in {1, Hq})."""
+    if bias is None:
+        return BIAS_NONE
+    bb, bh = bias.shape[0], bias.shape[1]
+    if bias.dim() != 4 or bb not in (1, batch) or bh not in (1, nhead_q):
+        raise ValueError("bias must be [1 or B, 1 or Hq, Sq, Sk]")
+    if bb == 1 and bh == 1:
+        return BIAS_11SS
+    if bb == 1:
+        return BIAS_1HSS
+    return BIAS_B1SS if bh == 1 else BIAS_BHSS
+
+
+def _set_extras(p, q, bias, dropout_p, philox_seed, philox_offset, dbias=None):
+    if bias is not None:
+        if not bias.is_contiguous():
+            raise ValueError("the bias must be contiguous")
+        p.bias_type = bias_type_of(bias, q.shape[0], q.shape[2])
+        p.bias = bias.data_ptr()
+    if dbias is not None:
+        p.dbias = dbias.data_ptr()
+    p.dropout_p = float(dropout_p)
+    p.philox_seed, p.philox_offset = _ptr(philox_seed), _ptr(philox_offset)
+
+
 def bwd_params(q, k, v, o, do, lse, dq, dk, dv, *, scale, mask=MASK_NONE, left=-1, right=-1,
                deterministic=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0,
-               max_seqlen_k=0, cu_seqlens_q_padded=None, cu_seqlens_k_padded=None) -> AttnBwdParams:
+               max_seqlen_k=0, cu_seqlens_q_padded=None, cu_seqlens_k_padded=None, bias=None, dbias=None,
+               dropout_p=0.0, philox_seed=None, philox_offset=None) -> AttnBwdParams:
     p = AttnBwdParams()
     p.dtype = _DTYPES[q.dtype]
     for name, val in _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k).items():
@@ -230,12 +262,14 @@ def bwd_params(q, k, v, o, do, lse, dq, dk, dv, *, scale, mask=MASK_NONE, left=-
     p.q, p.k, p.v, p.o, p.dout, p.lse = (_ptr(t) for t in (q, k, v, o, do, lse))
     p.dq, p.dk, p.dv = _ptr(dq), _ptr(dk), _ptr(dv)
     _set_strides(p, cu_seqlens_q is not None, q=q, k=k, v=v, o=o, dout=do, dq=dq, dk=dk, dv=dv)
+    _set_extras(p, q, bias, dropout_p, philox_seed, philox_offset, dbias)
     return p
 
 
 def fwd_params(q, k, v, o, lse, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlens_q=None,
                cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, cu_seqlens_q_padded=None,
-               cu_seqlens_k_padded=None) -> AttnFwdParams:
+               cu_seqlens_k_padded=None, bias=None, dropout_p=0.0, philox_seed=None,
+               philox_offset=None) -> AttnFwdParams:
     p = AttnFwdParams()
     p.dtype = _DTYPES[q.dtype]
     for name, val in _shape_args(q, k, v, cu_seqlens_q, max_seqlen_q, max_seqlen_k).items():
@@ -246,6 +280,7 @@ def fwd_params(q, k, v, o, lse, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_
     p.softmax_scale = scale
     p.q, p.k, p.v, p.o, p.lse = (_ptr(t) for t in (q, k, v, o, lse))
     _set_strides(p, cu_seqlens_q is not None, q=q, k=k, v=v, o=o)
+    _set_extras(p, q, bias, dropout_p, philox_seed, philox_offset)
     return p
 
 
@@ -272,7 +307,8 @@ def _empty_in_order_of(t, last: int):
 
 def attn_forward(q, k, v, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlens_q=None,
                  cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0, cu_seqlens_q_padded=None,
-                 cu_seqlens_k_padded=None, stream=None):
+                 cu_seqlens_k_padded=None, stream=None, bias=None, dropout_p=0.0, philox_seed=None,
+                 philox_offset=None):
     """O and LSE from the library's forward helper (outputs allocated here; the
     padding rows of a padded layout, which the helper leaves alone, hold O = 0
     and LSE = -inf)."""
@@ -285,7 +321,8 @@ def attn_forward(q, k, v, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlen
     p = fwd_params(q, k, v, o, lse, scale=scale, mask=mask, left=left, right=right,
                    cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                    max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
-                   cu_seqlens_q_padded=cu_seqlens_q_padded, cu_seqlens_k_padded=cu_seqlens_k_padded)
+                   cu_seqlens_q_padded=cu_seqlens_q_padded, cu_seqlens_k_padded=cu_seqlens_k_padded,
+                   bias=bias, dropout_p=dropout_p, philox_seed=philox_seed, philox_offset=philox_offset)
     st = attn_fwd(p, _stream(stream))
     if st != 0:
         raise AttnError(st, "attn_fwd")
@@ -295,15 +332,25 @@ def attn_forward(q, k, v, *, scale, mask=MASK_NONE, left=-1, right=-1, cu_seqlen
 def attn_backward(q, k, v, o, do, lse, *, scale, mask=MASK_NONE, left=-1, right=-1,
                   deterministic=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0,
                   max_seqlen_k=0, cu_seqlens_q_padded=None, cu_seqlens_k_padded=None,
-                  workspace=None, out=None, stream=None, check_status=True):
-    """dQ, dK, dV through attn_bwd (outputs and workspace allocated here unless given)."""
+                  workspace=None, out=None, stream=None, check_status=True, bias=None, return_dbias=False,
+                  dropout_p=0.0, philox_seed=None, philox_offset=None):
+    """dQ, dK, dV (and dbias [B, Hq, Sq, Sk] when return_dbias) through attn_bwd
+    (outputs and workspace allocated here unless given).  `bias` is a
+    [1 or B, 1 or Hq, Sq, Sk] tensor in the dtype of q; dropout takes a
+    probability and one-element int64 device tensors for the philox seed and
+    offset."""
     if out is None:
         out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     dq, dk, dv = out
+    dbias = None
+    if return_dbias:
+        dbias = torch.empty((q.shape[0], q.shape[2], q.shape[1], k.shape[1]), dtype=q.dtype, device=q.device)
     p = bwd_params(q, k, v, o, do, lse, dq, dk, dv, scale=scale, mask=mask, left=left, right=right,
                    deterministic=deterministic, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                    max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
-                   cu_seqlens_q_padded=cu_seqlens_q_padded, cu_seqlens_k_padded=cu_seqlens_k_padded)
+                   cu_seqlens_q_padded=cu_seqlens_q_padded, cu_seqlens_k_padded=cu_seqlens_k_padded,
+                   bias=bias, dbias=dbias, dropout_p=dropout_p, philox_seed=philox_seed,
+                   philox_offset=philox_offset)
     n = workspace_bytes(p)
     if workspace is None or workspace.numel() < n:
         workspace = alloc_workspace(n, q.device)
@@ -317,4 +364,6 @@ def attn_backward(q, k, v, o, do, lse, *, scale, mask=MASK_NONE, left=-1, right=
             raise AttnError(st, "attn_bwd_read_status")
         if dev != 0:
             raise AttnError(dev, "attn_bwd (device status)")
+    if return_dbias:
+        return dq, dk, dv, dbias
     return dq, dk, dv

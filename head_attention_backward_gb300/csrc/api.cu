@@ -111,6 +111,10 @@ static int effective_fwd(const attn_fwd_params& p, attn_fwd_params* e, FwdLayout
   const int kind = fold_strides(t, 4, group, p.batch, p.dtype != ATTN_FP32, s);
   if (kind < 0) return ATTN_ERR_INVALID_ARG;
   L->q = s[0]; L->k = s[1]; L->v = s[2]; L->o = s[3];
+  L->hq0 = p.nhead_q;
+  const long long mat = (long long)p.seqlen_q * p.seqlen_k;
+  L->bias_sb = p.bias_type == ATTN_BIAS_BHSS ? p.nhead_q * mat : p.bias_type == ATTN_BIAS_B1SS ? mat : 0;
+  L->bias_sh = p.bias_type == ATTN_BIAS_BHSS || p.bias_type == ATTN_BIAS_1HSS ? mat : 0;
   *e = p;
   if (kind == 1) {
     if ((long long)p.batch * p.nhead_q > (1 << 24)) return ATTN_ERR_INVALID_ARG;
@@ -149,9 +153,33 @@ static int validate_common(const Prm* p) {
   return ATTN_OK;
 }
 
+// Attention bias and dropout fields shared by both parameter structs: the
+// bias needs batch mode and a 16-bit dtype, dropout a 16-bit dtype, a
+// probability in [0, 1) and both philox pointers (TE PR #446: the bias shapes
+// and the philox seed / offset pointers of ck_attn_bwd).
+template <typename Prm>
+static int validate_extras(const Prm* p) {
+  if (p->bias_type < ATTN_BIAS_NONE || p->bias_type > ATTN_BIAS_B1SS) return ATTN_ERR_INVALID_ARG;
+  if (p->bias_type != ATTN_BIAS_NONE) {
+    if (p->cu_seqlens_q != nullptr || p->dtype == ATTN_FP32) return ATTN_ERR_INVALID_ARG;
+    if (!p->bias || (reinterpret_cast<uintptr_t>(p->bias) & 1u) != 0) return ATTN_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(p->dropout_p) || p->dropout_p < 0.f || p->dropout_p >= 1.f) return ATTN_ERR_INVALID_ARG;
+  if (p->dropout_p > 0.f) {
+    if (p->dtype == ATTN_FP32) return ATTN_ERR_INVALID_ARG;
+    const void* rng[] = {p->philox_seed, p->philox_offset};
+    for (const void* x : rng)
+      if (!x || (reinterpret_cast<uintptr_t>(x) & 7u) != 0) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
 static int validate_bwd(const attn_bwd_params* p) {
   int st = validate_common(p);
   if (st != ATTN_OK) return st;
+  if ((st = validate_extras(p)) != ATTN_OK) return st;
+  if (p->dbias && (p->bias_type == ATTN_BIAS_NONE || (reinterpret_cast<uintptr_t>(p->dbias) & 1u) != 0))
+    return ATTN_ERR_INVALID_ARG;
   if (p->deterministic < ATTN_DET_ATOMIC || p->deterministic > ATTN_DET_SPLIT) return ATTN_ERR_INVALID_ARG;
   if (p->dtype == ATTN_FP32) {
     if (!simt_headdims(p->d_qk, p->d_v)) return ATTN_ERR_UNSUPPORTED_HEADDIM;
@@ -171,6 +199,7 @@ static int validate_bwd(const attn_bwd_params* p) {
 static int validate_fwd(const attn_fwd_params* p) {
   int st = validate_common(p);
   if (st != ATTN_OK) return st;
+  if ((st = validate_extras(p)) != ATTN_OK) return st;
   if (p->d_qk > 256 || p->d_v > 256) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   // 16-bit tensors feed tensor maps and 16-byte vector stores of O (the same
   // rule as the backward's); fp32 tensors and lse are accessed one element
@@ -183,8 +212,10 @@ static int validate_fwd(const attn_fwd_params* p) {
   return ATTN_OK;
 }
 
-// p: the effective problem (effective_bwd), s: its strides.
-static Problem make_problem(const attn_bwd_params& p, const Strides s[8], void* ws) {
+// p: the effective problem (effective_bwd), s: its strides; hq0: the
+// caller's query heads (p.nhead_q is B * hq0 when the batch is folded into
+// the heads).
+static Problem make_problem(const attn_bwd_params& p, const Strides s[8], void* ws, int hq0) {
   const WsLayout L = ws_layout(p);
   Problem P{};
   P.dtype = p.dtype;
@@ -228,6 +259,23 @@ static Problem make_problem(const attn_bwd_params& p, const Strides s[8], void* 
   P.turn = reinterpret_cast<unsigned*>(w + L.off_turn);
   P.klo = reinterpret_cast<int*>(w + L.off_klo);
   P.n_lse = L.n_lse;
+  P.hq0 = hq0;
+  P.extras = p.bias_type != ATTN_BIAS_NONE || p.dropout_p > 0.f;
+  if (p.bias_type != ATTN_BIAS_NONE) {
+    const long long mat = (long long)p.seqlen_q * p.seqlen_k;   // one [Sq, Sk] matrix
+    P.bias = p.bias;
+    P.bias_sb = p.bias_type == ATTN_BIAS_BHSS ? hq0 * mat : p.bias_type == ATTN_BIAS_B1SS ? mat : 0;
+    P.bias_sh = p.bias_type == ATTN_BIAS_BHSS || p.bias_type == ATTN_BIAS_1HSS ? mat : 0;
+    P.dbias = p.dbias;
+  }
+  if (p.dropout_p > 0.f) {
+    P.drop_p = p.dropout_p;
+    P.drop_scale = 1.f / (1.f - p.dropout_p);
+    const double t = std::floor((double)p.dropout_p * 4294967296.0);
+    P.drop_thr = t >= 4294967295.0 ? 4294967295u : (unsigned)t;
+    P.philox_seed = reinterpret_cast<const unsigned long long*>(p.philox_seed);
+    P.philox_offset = reinterpret_cast<const unsigned long long*>(p.philox_offset);
+  }
   return P;
 }
 
@@ -267,7 +315,7 @@ static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t
   const WsLayout L = ws_layout(e);
   if (ws_bytes < L.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   if (log_enabled()) log_config(e, L);
-  const Problem P = make_problem(e, sx, ws);
+  const Problem P = make_problem(e, sx, ws, p->nhead_q);
   if (ev) cudaEventRecord(ev[0], s);
   launch_schedule_preprocess(P, s, keep_status);
   if (ev) cudaEventRecord(ev[1], s);
@@ -498,8 +546,10 @@ extern "C" int attn_fwd(const attn_fwd_params* p, cudaStream_t stream) {
   FwdLayout L;
   const int s2 = effective_fwd(*p, &e, &L);
   if (s2 != ATTN_OK) return s2;
-  const int s3 = launch_fwd_tc(e, L, stream);
-  if (s3 == ATTN_ERR_UNSUPPORTED_HEADDIM) launch_fwd(e, L, stream);   // fp32, other head dims
+  // the tensor-core forward has no bias or dropout: the CUDA-core one takes those
+  const bool extras = e.bias_type != ATTN_BIAS_NONE || e.dropout_p > 0.f;
+  const int s3 = extras ? ATTN_ERR_UNSUPPORTED_HEADDIM : launch_fwd_tc(e, L, stream);
+  if (s3 == ATTN_ERR_UNSUPPORTED_HEADDIM) launch_fwd(e, L, stream);   // fp32, other head dims, extras
   else if (s3 != ATTN_OK) return s3;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

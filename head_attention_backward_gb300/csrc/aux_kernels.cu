@@ -410,6 +410,34 @@ static int num_sms() {
   return n > 0 ? n : 1;
 }
 
+// dbias [B, Hq, Sq, Sk] (batch mode, attention bias with its gradient): the
+// main kernel writes the rows of every (query tile, KV tile) pair it visits,
+// masked entries as zeros; this kernel zeroes the pairs that no KV tile's
+// query range reaches, one tile row (up to BN elements) per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) dbias_fill_kernel(Problem P) {
+  const MaskArgs m = mask_args(P.mask, P.left, P.right, P.sq, P.sk);
+  const int ntq = cdiv(P.sq, BM), nkv = cdiv(P.sk, BN);
+  const long long rows = (long long)P.nseg * P.hq * ntq * nkv * BM;
+  T* db = static_cast<T*>(P.dbias);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i % BM);
+    long long t = i / BM;
+    const int kt = (int)(t % nkv);
+    t /= nkv;
+    const int qt = (int)(t % ntq);
+    const long long bh = t / ntq;
+    const int q = qt * BM + r;
+    if (q >= P.sq) continue;
+    int lo, hi;
+    qtile_range(m, P.sq, P.sk, kt, lo, hi);
+    if (qt >= lo && qt < hi) continue;   // visited: the main kernel writes it
+    T* row = db + (bh * P.sq + q) * P.sk + (long long)kt * BN;
+    const int n = min(BN, P.sk - kt * BN);
+    for (int c = 0; c < n; ++c) row[c] = TypeOps<T>::from_f(0.f);
+  }
+}
+
 // sched: 0 = the scheduler kernel ran before; 1 / 2 = batch mode, this
 // kernel schedules (2: keep an earlier part's status).
 static void launch_preprocess_sched(const Problem& P, cudaStream_t st, int sched) {
@@ -437,6 +465,11 @@ void launch_preprocess(const Problem& P, cudaStream_t st) { launch_preprocess_sc
 // the preprocess kernel (debug builds keep the separate scheduler, whose
 // header reset then precedes every index check of the preprocess).
 void launch_schedule_preprocess(const Problem& P, cudaStream_t st, bool keep_status) {
+  if (P.dbias != nullptr) {
+    const int grid = num_sms() * 4;
+    if (P.dtype == ATTN_FP16) dbias_fill_kernel<__half><<<grid, 256, 0, st>>>(P);
+    else dbias_fill_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(P);
+  }
 #ifndef ATTN_DEBUG
   if (!P.group) {
     launch_preprocess_sched(P, st, keep_status ? 2 : 1);

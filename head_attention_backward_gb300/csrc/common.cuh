@@ -79,6 +79,17 @@ struct Problem {
   unsigned* turn;    // fold mode: [Hq][ntiles] partials folded so far per query tile
   int* klo;          // fold mode: [ntiles] first KV tile that reaches each query tile
   long long n_lse;   // rows of the LSE layout = B*Hq*Sq or Hq*Tq
+  // attention bias and dropout (the kernels' extras variant)
+  int extras;        // 1: bias or dropout in use
+  const void* bias;  // element (b, h, q, k) at b*bias_sb + h*bias_sh + q*sk + k
+  long long bias_sb, bias_sh;
+  int hq0;           // query heads of the caller's layout (the batch may be folded into the heads)
+  void* dbias;       // [B, Hq, Sq, Sk] output or null
+  float drop_p;      // 0 = no dropout
+  float drop_scale;  // 1 / (1 - p)
+  unsigned drop_thr; // keep when the Philox word >= drop_thr = floor(p * 2^32)
+  const unsigned long long* philox_seed;
+  const unsigned long long* philox_offset;
 };
 
 struct WsLayout {
@@ -322,6 +333,38 @@ static __device__ __noinline__ bool debug_index_fail(int* hdr, int id) {
 __host__ __device__ inline long long rows_q(const Problem& P) { return P.group ? (long long)P.tq : (long long)P.nseg * P.sq; }
 __host__ __device__ inline long long rows_k(const Problem& P) { return P.group ? (long long)P.tk : (long long)P.nseg * P.sk; }
 
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds of two 32x32 -> 64-bit products with
+// the published multipliers, the key bumped by the published Weyl constants
+// between rounds.  c holds the counter in, the four output words out.
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c[0]), lo0 = 0xD2511F53u * c[0];
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c[2]), lo1 = 0xCD9E8D57u * c[2];
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// Dropout keep bits of query rows 4j .. 4j+3 (bit i: row 4j + i) for key
+// column `col` of query head bh = b * Hq + h: counter (lo32(n), col, bh,
+// hi32(n)), n = offset + j, key (lo32(seed), hi32(seed)).
+__device__ __forceinline__ uint32_t dropout_keep4(unsigned long long seed, unsigned long long offset, uint32_t j,
+                                                  uint32_t col, uint32_t bh, uint32_t thr) {
+  const unsigned long long n = offset + j;
+  uint32_t c[4] = {(uint32_t)n, col, bh, (uint32_t)(n >> 32)};
+  philox4x32_10(c, (uint32_t)seed, (uint32_t)(seed >> 32));
+  return (c[0] >= thr ? 1u : 0u) | (c[1] >= thr ? 2u : 0u) | (c[2] >= thr ? 4u : 0u) | (c[3] >= thr ? 8u : 0u);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -337,6 +380,8 @@ int launch_bwd_tc(const Problem& P, cudaStream_t st);   // returns ATTN_* status
 int selftest_waits(void* scratch, size_t bytes, cudaStream_t st, int status[3]);
 struct FwdLayout {
   Strides q, k, v, o;
+  int hq0;                    // the caller's query heads (before a batch fold)
+  long long bias_sb, bias_sh; // bias element strides of batch entry and head
 };
 void launch_fwd(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st);
 

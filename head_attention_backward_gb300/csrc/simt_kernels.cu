@@ -52,6 +52,22 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, Fwd
     sQ[r * sq_stride + c] = x;
   }
   const MaskArgs m = mask_args(p.mask, p.window_left, p.window_right, lq, lk);
+  // attention bias (batch mode) and dropout: bh = b * Hq + h indexes the
+  // dropout counter, the caller's (batch entry, head) the bias
+  const T* bias = static_cast<const T*>(p.bias);
+  const long long bias_off = bias ? (long long)(b + h / L.hq0) * L.bias_sb + (long long)(h % L.hq0) * L.bias_sh : 0;
+  const uint32_t bh = (uint32_t)(b * p.nhead_q + h);
+  const bool drop = p.dropout_p > 0.f;
+  unsigned long long seed = 0, offset = 0;
+  uint32_t thr = 0;
+  float dscale = 1.f;
+  if (drop) {
+    seed = *p.philox_seed;
+    offset = *p.philox_offset;
+    const double t = floor((double)p.dropout_p * 4294967296.0);
+    thr = t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
+    dscale = 1.f / (1.f - p.dropout_p);
+  }
   // keys any row of this tile can see
   const int qe = min(qs + FWD_BQ, lq) - 1;
   long long klo = 0, khi = (long long)lk - 1;
@@ -89,6 +105,7 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, Fwd
       float x = 0.f;
       for (int c = 0; c < dqk; ++c) x += sQ[row * sq_stride + c] * sK[j * sk_stride + c];
       const bool ok = qi < lq && kk < lk && visible(m, qi, (int)kk);
+      if (ok && bias) x = fmaf(TypeOps<T>::to_f(bias[bias_off + (long long)qi * p.seqlen_k + kk]), 1.f / p.softmax_scale, x);
       s[t] = ok ? x * sl2 : -INFINITY;
       tmax = fmaxf(tmax, s[t]);
     }
@@ -107,7 +124,13 @@ __global__ void __launch_bounds__(FWD_THREADS) fwd_kernel(attn_fwd_params p, Fwd
       for (int t = 0; t < FWD_BK / 4; ++t) {
         const float e = fast_exp2(s[t] - mnew);
         psum += e;
-        sP[row * (FWD_BK + 1) + sub + 4 * t] = e;
+        float ev = e;
+        if (drop) {   // the row sum keeps every weight, the product with V only the kept ones
+          const long long kk = kb + sub + 4 * t;
+          const uint32_t bits = dropout_keep4(seed, offset, (uint32_t)(qi >> 2), (uint32_t)kk, bh, thr);
+          ev = ((bits >> (qi & 3)) & 1u) ? e * dscale : 0.f;
+        }
+        sP[row * (FWD_BK + 1) + sub + 4 * t] = ev;
       }
       mrow = mnew;
     }

@@ -97,6 +97,20 @@ typedef enum {
  * for in the review of TE PR #671). */
 typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1, ATTN_FP32 = 2 } attn_dtype_t;
 
+/* Attention bias shapes: the bias of shape (bias_b, bias_h, s_q, s_kv) of
+ * TransformerEngine PR #446 (review of ck_fused_attn_bwd.cpp, BiasShape
+ * k11SS / k1HSS / kBHSS / kB1SS), contiguous with row stride seqlen_k, in the
+ * dtype of q; bias_h counts query heads.  It is added to the scaled scores,
+ * S = softmax_scale * Q K^T + bias, before the mask.  Batch mode and the
+ * 16-bit dtypes only. */
+typedef enum {
+  ATTN_BIAS_NONE = 0,
+  ATTN_BIAS_11SS = 1,   /* [1, 1, Sq, Sk]: one matrix for every batch entry and head */
+  ATTN_BIAS_1HSS = 2,   /* [1, Hq, Sq, Sk] */
+  ATTN_BIAS_BHSS = 3,   /* [B, Hq, Sq, Sk] */
+  ATTN_BIAS_B1SS = 4    /* [B, 1, Sq, Sk] */
+} attn_bias_t;
+
 typedef struct {
   int32_t dtype;          /* attn_dtype_t                                          */
   int32_t batch;          /* batch mode: B; group mode: number of segments         */
@@ -156,6 +170,29 @@ typedef struct {
   int64_t stride_dq[3];
   int64_t stride_dk[3];
   int64_t stride_dv[3];
+  /* Attention bias and dropout (TE PR #446: the bias shapes above; dropout
+   * driven by the philox seed / offset pointers passed to ck_attn_bwd).  A
+   * zero-initialised tail means neither. */
+  int32_t bias_type;      /* attn_bias_t                                           */
+  float dropout_p;        /* probability of dropping an attention weight, in
+                             [0, 1); 0 = no dropout.  16-bit dtypes only       */
+  const void* bias;       /* device, attn_bias_t shape, dtype of q, 2-byte aligned */
+  void* dbias;            /* device output [B, Hq, Sq, Sk] in the dtype of q, the
+                             gradient of the biased scores (dS), or NULL; needs a
+                             bias.  Fully overwritten (zero where masked).  The
+                             gradient of a broadcast bias is its sum over the
+                             broadcast dimensions, left to the caller (the
+                             pages' CK kernels also emit dbias in BHSS only)  */
+  const uint64_t* philox_seed;   /* device, 8-byte aligned; read when dropout_p > 0 */
+  const uint64_t* philox_offset; /* device, 8-byte aligned.  Weight (i, j) of
+                             (batch or segment b, query head h) is kept when
+                             word (i mod 4) of Philox4x32-10 with key (seed mod
+                             2^32, seed div 2^32) and counter (lo32(n), j,
+                             b * Hq + h, hi32(n)), n = offset + i div 4, is at
+                             least floor(dropout_p * 2^32); kept weights are
+                             scaled by 1 / (1 - dropout_p).  O must come from a
+                             forward with the same mask (attn_fwd with the same
+                             seed, offset and dropout_p)                     */
 } attn_bwd_params;
 
 /* Forward helper that produces O and LSE for benchmark and test inputs
@@ -192,6 +229,11 @@ typedef struct {
   int64_t stride_k[3];
   int64_t stride_v[3];
   int64_t stride_o[3];
+  int32_t bias_type;      /* as in attn_bwd_params                                 */
+  float dropout_p;
+  const void* bias;
+  const uint64_t* philox_seed;
+  const uint64_t* philox_offset;
 } attn_fwd_params;
 
 /* dQ accumulation modes (attn_bwd_params.deterministic).  The per-KV-tile dQ

@@ -44,6 +44,10 @@ int main(void) {
   F(attn_bwd_params, deterministic) F(attn_bwd_params, q) F(attn_bwd_params, lse) F(attn_bwd_params, dv)
   F(attn_bwd_params, stride_q) F(attn_bwd_params, stride_dout) F(attn_bwd_params, stride_dv)
   F(attn_fwd_params, stride_q) F(attn_fwd_params, stride_o)
+  F(attn_bwd_params, bias_type) F(attn_bwd_params, dropout_p) F(attn_bwd_params, bias) F(attn_bwd_params, dbias)
+  F(attn_bwd_params, philox_seed) F(attn_bwd_params, philox_offset)
+  F(attn_fwd_params, bias_type) F(attn_fwd_params, dropout_p) F(attn_fwd_params, bias)
+  F(attn_fwd_params, philox_seed) F(attn_fwd_params, philox_offset)
   printf("attn_host_tensors.size %zu\n", sizeof(attn_host_tensors));
   F(attn_host_tensors, lse) F(attn_host_tensors, dv)
   F(attn_fwd_params, cu_seqlens_k) F(attn_fwd_params, cu_seqlens_k_padded) F(attn_fwd_params, softmax_scale) F(attn_fwd_params, q) F(attn_fwd_params, lse)
@@ -172,11 +176,29 @@ ERR = dict(inv=-1, hd=-2, ws=-3)
     (dict(dtype=B.ATTN_FP32, d_qk=256, d_v=256), "hd"),
     (dict(q=None), "inv"),
     (dict(dq=0x10008), "inv"),          # not 16-byte aligned
+    (dict(bias_type=5, bias=0x200000), "inv"),               # unknown bias shape
+    (dict(bias_type=1), "inv"),                              # bias shape without a bias
+    (dict(bias_type=1, bias=0x200001), "inv"),               # bias not 2-byte aligned
+    (dict(dbias=0x300000), "inv"),                           # dbias without a bias
+    (dict(dtype=B.ATTN_FP32, d_qk=64, d_v=64, bias_type=3, bias=0x200000), "inv"),   # extras: 16-bit only
+    (dict(dropout_p=1.0, philox_seed=0x400000, philox_offset=0x400008), "inv"),
+    (dict(dropout_p=-0.1, philox_seed=0x400000, philox_offset=0x400008), "inv"),
+    (dict(dropout_p=float("nan"), philox_seed=0x400000, philox_offset=0x400008), "inv"),
+    (dict(dropout_p=0.5), "inv"),                            # no philox seed / offset
+    (dict(dropout_p=0.5, philox_seed=0x400004, philox_offset=0x400008), "inv"),   # seed not 8-byte aligned
 ])
 def test_invalid_arguments_rejected_before_launch(lib, kw, code):
     p = make(**kw)
     st = B.attn_bwd(p, 0x100000, 1 << 40, 0)
     assert st == ERR[code], (kw, st)
+
+
+def test_bias_rejected_in_group_mode(lib):
+    """The attention bias is defined for batch mode only (TE PR #446 sets the
+    bias shape only outside group mode)."""
+    p = make(total_q=100, total_k=100, bias_type=1, bias=0x200000)
+    p.cu_seqlens_q, p.cu_seqlens_k = 0x1000, 0x2000
+    assert B.attn_bwd(p, 0x100000, 1 << 40, 0) == -1
 
 
 def test_group_mode_needs_both_seqstart_arrays(lib):
