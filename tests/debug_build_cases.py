@@ -26,7 +26,14 @@ def case_list():
         W.thd("thd_padded", [100, 0, 37, 250, 5], hq=4, hkv=2, mask=W.MASK_CAUSAL_BOTTOM_RIGHT,
               seed=97, seqlens_k=[300, 64, 0, 129, 200], gaps_q=[3, 0, 17, 140, 2, 9],
               gaps_k=[0, 5, 131, 7, 1, 30]),
+        wl("d256", torch.bfloat16, 1, 2, 1, 200, 200, 256, 256, W.MASK_CAUSAL_TOP_LEFT, -1, -1, False, 98, None),
+        wl("bias_dropout", torch.bfloat16, 2, 4, 2, 150, 150, 128, 128, W.MASK_CAUSAL_TOP_LEFT, -1, -1, False, 99,
+           None),
     ]
+
+
+# extras per case: a [B, Hq, Sq, Sk] bias with dbias, and dropout
+EXTRAS = {"bias_dropout": dict(dropout_p=0.25, seed=5, offset=9)}
 
 
 def main():
@@ -38,18 +45,27 @@ def main():
         kw = dict(mask=w.mask, left=w.left, right=w.right, cu_seqlens_q=cu, cu_seqlens_k=cuk)
         if stq is not None or stk is not None:
             kw.update(cu_seqlens_q_padded=stq, cu_seqlens_k_padded=stk)
-        o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], w.scale, **kw)
+        ex = EXTRAS.get(w.name)
+        okw, gkw = dict(kw), {}
+        if ex:
+            g = torch.Generator().manual_seed(w.seed)
+            bias = torch.randn((w.batch, w.hq, w.sq, w.sk), generator=g).to(w.dtype)
+            okw.update(bias=bias, dropout_p=ex["dropout_p"], philox_seed=ex["seed"], philox_offset=ex["offset"])
+            gkw = dict(bias=bias.cuda(), return_dbias=True, dropout_p=ex["dropout_p"],
+                       philox_seed=torch.tensor([ex["seed"]], dtype=torch.int64, device="cuda"),
+                       philox_offset=torch.tensor([ex["offset"]], dtype=torch.int64, device="cuda"))
+        o64, lse64 = R.attn_forward(x["q"], x["k"], x["v"], w.scale, **okw)
         o_in, lse_in = o64.to(w.dtype), lse64.to(torch.float32)
-        ref = R.attn_backward(x["q"], x["k"], x["v"], o_in, x["do"], lse_in, w.scale, **kw)
+        ref = R.attn_backward(x["q"], x["k"], x["v"], o_in, x["do"], lse_in, w.scale, return_dbias=bool(ex), **okw)
         d = {k: v.cuda() for k, v in x.items()}
         dkw = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
         tol, mcos = tolerances(w.dtype)
         for mode in (0, 1, 2):
             got = B.attn_backward(d["q"], d["k"], d["v"], o_in.cuda(), d["do"], lse_in.cuda(), scale=w.scale,
-                                  deterministic=mode, max_seqlen_q=w.sq, max_seqlen_k=w.sk, **dkw)
+                                  deterministic=mode, max_seqlen_q=w.sq, max_seqlen_k=w.sk, **dkw, **gkw)
             torch.cuda.synchronize()
             reps = []
-            for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            for name, g, r in zip(("dq", "dk", "dv", "dbias"), got, ref):
                 rep = compare(g.cpu(), r, tol, mcos)
                 rep["tensor"] = name
                 reps.append(rep)

@@ -20,4 +20,4 @@ def test_debug_build_index_checks_clean():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "debug_build_cases.py")],
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
-    assert r.stdout.count("ok ") == 21, r.stdout
+    assert r.stdout.count("ok ") == 27, r.stdout

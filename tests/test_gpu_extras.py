@@ -16,7 +16,7 @@ import torch
 
 from head_attention_backward_gb300 import workloads as W
 from oracle import attn_ref as R
-from tests.parity import assert_all_ok, compare, per_segment_report, tolerances
+from tests.parity import assert_all_ok, compare, layout_heads_outer, per_segment_report, tolerances
 from tests.test_gpu_parity import B  # noqa: F401  (fixture)
 
 pytestmark = pytest.mark.gpu
@@ -33,7 +33,7 @@ def _bias(kind, wl, seed):
     return torch.randn((bb, bh, wl.sq, wl.sk), generator=g, dtype=torch.float32).to(wl.dtype)
 
 
-def run_extras(B, wl, det, bias_kind=None, dropout_p=0.0, seed=0, offset=0):
+def run_extras(B, wl, det, bias_kind=None, dropout_p=0.0, seed=0, offset=0, layout=None):
     """Oracle forward -> rounded O / fp32 LSE -> GPU and oracle backward with
     the same bias and dropout; reports per tensor, per segment and per
     (batch, head) slice of dbias."""
@@ -52,7 +52,10 @@ def run_extras(B, wl, det, bias_kind=None, dropout_p=0.0, seed=0, offset=0):
     seed_t = torch.tensor([seed], dtype=torch.int64, device="cuda")
     off_t = torch.tensor([offset], dtype=torch.int64, device="cuda")
     out = tuple(torch.full_like(dev[n], float("nan")) for n in ("q", "k", "v"))
-    got = B.attn_backward(dev["q"], dev["k"], dev["v"], o_in.cuda(), dev["do"], lse_in.cuda(), scale=wl.scale,
+    dev["o"] = o_in.cuda()
+    if layout is not None:   # strided views with the same values (the host may fold the batch into the heads)
+        dev, out = layout(dev)
+    got = B.attn_backward(dev["q"], dev["k"], dev["v"], dev["o"], dev["do"], lse_in.cuda(), scale=wl.scale,
                           deterministic=det, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk, out=out,
                           bias=None if bias is None else bias.cuda(), return_dbias=bias is not None,
                           dropout_p=p32, philox_seed=seed_t, philox_offset=off_t, **dkw)
@@ -122,6 +125,16 @@ def test_dropout_with_bias_fp16_window(B):
 def test_dropout_packed_segments(B, det):
     wl = W.thd("drop_thd", [100, 80, 76], hq=8, hkv=2, seed=33)
     assert_all_ok(run_extras(B, wl, det, dropout_p=0.125, seed=7, offset=0), f"dropout THD det={det}")
+
+
+@pytest.mark.parametrize("kind", ["1HSS", "B1SS", "BHSS"])
+def test_bias_and_dropout_with_heads_outer_layout(B, kind):
+    """Heads-outer tensors ([B, H, S, D] memory order): the host runs the call
+    as one batch entry with B * H heads, so the kernel recovers the caller's
+    (batch entry, head) for the bias and keeps b * Hq + h for the dropout
+    counter and dbias."""
+    assert_all_ok(run_extras(B, BASE, 1, bias_kind=kind, dropout_p=0.25, seed=77, offset=1,
+                             layout=layout_heads_outer), f"heads-outer bias {kind}")
 
 
 @pytest.mark.parametrize("kind,p", [("BHSS", 0.0), (None, 0.25), ("11SS", 0.3)])
