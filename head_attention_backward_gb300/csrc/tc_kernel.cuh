@@ -109,11 +109,17 @@ struct Cfg {
   static constexpr int T_DV = DA;
   static constexpr int T_S = DA + DVA;
   static constexpr int T_DP = T_S + BM;
-  static constexpr bool ALIAS = T_DP + BM + NMB * BM + BM > (int)TMEM_COLS;
-  static constexpr int T_DQ = ALIAS ? T_S : T_DP + BM;
-  static constexpr int T_P = ALIAS ? T_DP + BM : T_DQ + NMB * BM;   // P^T buffers 0 and 1
-  static_assert(T_P + BM <= (int)TMEM_COLS, "TMEM overflow");
-  static_assert(!ALIAS || T_S + NMB * BM <= T_P, "aliased dQ must fit in S and dP");
+  static constexpr int T_DQ = T_DP + BM;
+  // SEQDQ (d_qk = 192): dK and dV take 320 columns, leaving no room for two P^T
+  // buffers beside S^T, dP^T and both M blocks of dQ^T.  Each thread then
+  // writes its P^T (bf16 pairs) over the first half of its own S^T columns,
+  // so K step ks of dV's A operand sits at T_S + 16 ks; the M blocks of dQ^T
+  // take turns in one 64-column region.  dP^T of the next step is issued once
+  // the P/dS warps have read dP^T, S^T of the next step once dV has read P^T.
+  static constexpr bool SEQDQ = T_DQ + NMB * BM + BM > (int)TMEM_COLS;
+  static constexpr int T_P = SEQDQ ? T_S : T_DQ + NMB * BM;   // P^T buffers 0 and 1 (SEQDQ: one, over S^T)
+  static_assert((SEQDQ ? T_DQ + BM : T_P + BM) <= (int)TMEM_COLS, "TMEM overflow");
+  static_assert(!SEQDQ || (NPASS == 1 && BM / 16 * 16 == BM), "SEQDQ: single pass");
   static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
   static constexpr uint32_t KV_BYTES = (NCK + NCV) * KCH;
   static constexpr uint32_t QDO_BYTES = (NCK + NCV) * QCH;
@@ -123,7 +129,9 @@ struct Cfg {
 // (B_PDS_FULL and B_PDS_EMPTY are pairs: one barrier per P/dS buffer)
 enum {
   B_KV_FULL = 0, B_KV_EMPTY, B_SDP_FULL, B_SDP_EMPTY, B_PDS_FULL, B_PDS_EMPTY = B_PDS_FULL + 2,
-  B_DQ_FULL = B_PDS_EMPTY + 2, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_DRAIN2, B_FIXED_END = 16
+  B_DQ_FULL = B_PDS_EMPTY + 2, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_DRAIN2,
+  B_P_FREE,   // SEQDQ: dV has read the P^T written over S^T
+  B_FIXED_END = 16
 };
 
 struct Ctx {
@@ -308,6 +316,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
     mbar_init(bar + B_DKV_EMPTY, NUM_EPI_WARPS);
     mbar_init(bar + B_DRAIN, 1);
     mbar_init(bar + B_DRAIN2, 1);
+    mbar_init(bar + B_P_FREE, 1);
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(bar + B_Q_FULL + s, 32 + 1);   // 32 cp.async arrivals + the TMA expect_tx arrival
       mbar_init(bar + B_Q_EMPTY + s, 1);
@@ -437,16 +446,30 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       // Inputs of S^T / dP^T for global step gs are ready and their TMEM free.
       auto wait_sdp = [&](uint32_t gs) -> bool {
         return wait_bar(ctx, B_Q_FULL + gs % C::ST, (gs / C::ST) & 1, 10) &&
-               wait_bar(ctx, B_SDP_EMPTY, (gs & 1) ^ 1, 11) &&
-               (!C::ALIAS || wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 12));
+               wait_bar(ctx, B_SDP_EMPTY, (gs & 1) ^ 1, 11);
       };
       // S^T = K Q^T and dP^T = V dO^T of step gs.
-      auto mma_sdp = [&](uint32_t gs) {
+      auto mma_sdp = [&](uint32_t gs) -> bool {
 #ifdef ATTN_WAIT_STATS
         const long long t0 = clock64();
 #endif
         const uint32_t st = gs % C::ST;
         const uint64_t q = dQ_k + ((st * C::NCK * C::QCH) >> 4), d = ddO_k + ((st * C::NCV * C::QCH) >> 4);
+        if constexpr (C::SEQDQ) {
+          // dP^T first; S^T once dV has read the previous P^T from its columns
+#pragma unroll
+          for (int ks = 0; ks < DV / 16; ++ks) {
+            const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
+            umma_ss(tmem + C::T_DP, dV_k + (off_a >> 4), d + (off_b >> 4), ID_SDP, ks > 0);
+          }
+          if (!wait_bar(ctx, B_P_FREE, (gs & 1) ^ 1, 12)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < DQK / 16; ++ks) {
+            const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
+            umma_ss(tmem + C::T_S, dK_k + (off_a >> 4), q + (off_b >> 4), ID_SDP, ks > 0);
+          }
+        } else {
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks) {
           const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
@@ -457,11 +480,13 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           const uint32_t off_a = (ks >> 2) * C::KCH + (ks & 3) * 32, off_b = (ks >> 2) * C::QCH + (ks & 3) * 32;
           umma_ss(tmem + C::T_DP, dV_k + (off_a >> 4), d + (off_b >> 4), ID_SDP, ks > 0);
         }
+        }
         umma_commit(bar + B_SDP_FULL);
 #ifdef ATTN_WAIT_STATS
         stat_add(g_wait_stats, 4, (unsigned long long)(clock64() - t0));   // S/dP group issue
         stat_add(g_wait_stats, 9, 1ull);                                   // steps
 #endif
+        return true;
       };
       // P^T / dS^T of step gs are in their buffer (gs & 1): P^T in TMEM, dS^T
       // in shared memory.
@@ -481,8 +506,8 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         const uint64_t a_ds = ddS_k + ((pb * C::DS_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
-          umma_ts(tmem + C::T_DV, tmem + C::T_P + pb * (BM / 2) + ks * 8, d + ((ks * 2048) >> 4), ID_DV,
-                  ks > 0 ? 1u : acc_first);
+          umma_ts(tmem + C::T_DV, tmem + (C::SEQDQ ? C::T_S + ks * 16 : C::T_P + pb * (BM / 2) + ks * 8),
+                  d + ((ks * 2048) >> 4), ID_DV, ks > 0 ? 1u : acc_first);
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
           umma_ss(tmem + C::T_DK, a_ds + ((ks * 32) >> 4), q + ((ks * 2048) >> 4), ID_DK, ks > 0 ? 1u : acc_first);
@@ -493,7 +518,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       };
       // The dQ^T TMEM of the previous step has been drained.
       auto wait_dq = [&](uint32_t gs) -> bool {
-        return C::ALIAS || wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16);
+        return wait_bar(ctx, B_DQ_EMPTY, (gs & 1) ^ 1, 16);
       };
       // dQ^T = K^T dS^T of step gs (the rows of pass `pass`); its commit
       // also frees the P/dS buffer.
@@ -511,6 +536,15 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         umma_commit(bar + B_DQ_FULL);
         umma_commit(bar + B_PDS_EMPTY + pb);
       };
+      // SEQDQ: M block mb of dQ^T = K^T dS^T of step gs, into the one dQ^T region
+      auto mma_dq_mb = [&](uint32_t gs, int mb) {
+        const uint64_t b_ds = ddS_mn + (((gs & 1) * C::DS_BYTES) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          umma_ss(tmem + C::T_DQ, dK_mn + (((mb * 2) * C::KCH + ks * 2048) >> 4), b_ds + ((ks * 2048) >> 4), ID_DQ,
+                  ks > 0);
+        umma_commit(bar + B_DQ_FULL);
+      };
       while (ok) {
         const int slot = n_item % NI;
         if (!wait_bar(ctx, B_IT_FULL + slot, (n_item / NI) & 1, 13)) break;
@@ -527,7 +561,11 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           for (uint32_t gs = g; gs <= last; ++gs) {
             if (!(ok = wait_sdp(gs))) break;
             tc_fence_after();
-            mma_sdp(gs);
+            if constexpr (C::SEQDQ) {
+              if (!(ok = mma_sdp(gs))) break;
+            } else {
+              mma_sdp(gs);
+            }
           }
         } else {
           if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (kvp & 1) ^ 1, 17))) break;
@@ -544,9 +582,21 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
             if (!(ok = wait_pds(gs))) break;
             tc_fence_after();
             mma_dvdk(gs, pass_first ? 0u : 1u, pass);
+            if constexpr (C::SEQDQ) {
+              umma_commit(bar + B_P_FREE);
+#pragma unroll 1
+              for (int mb = 0; mb < C::NMB; ++mb) {
+                if (!(ok = wait_bar(ctx, B_DQ_EMPTY, ((gs * C::NMB + mb) & 1) ^ 1, 16))) break;
+                tc_fence_after();
+                mma_dq_mb(gs, mb);
+              }
+              if (!ok) break;
+              umma_commit(bar + B_PDS_EMPTY + (gs & 1));
+            } else {
             if (!(ok = wait_dq(gs))) break;
             tc_fence_after();
             mma_dq(gs, pass);
+            }
           }
           if (!ok) break;
           // the item's last dQ/dV/dK followed its last P/dS, which followed
@@ -694,7 +744,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         const uint32_t pb = gs & 1;
         if (!(ok = wait_bar(ctx, B_PDS_EMPTY + pb, ((gs >> 1) & 1) ^ 1, 23))) break;
         tc_fence_after();
-        tmem_st8(lane_addr + C::T_P + pb * (BM / 2) + c0 / 2, pk);
+        tmem_st8(lane_addr + (C::SEQDQ ? C::T_S + c0 : C::T_P + pb * (BM / 2) + c0 / 2), pk);
 #pragma unroll
         for (int j = 0; j < CW / 8; ++j) {
           const int ch = grp * (CW / 8) + j;
@@ -842,20 +892,26 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           rank = (uint32_t)(I.kt - k0);
           if (ATTN_INDEX_OK(P, k0 >= 0 && k0 <= I.kt, 6)) seen = ld_acquire_gpu(P.turn + idx);
         }
-        if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
-        tc_fence_after();
+        if constexpr (!C::SEQDQ) {
+          if (!(ok = wait_bar(ctx, B_DQ_FULL, gs & 1, 31))) break;
+          tc_fence_after();
+        }
         float* dst_tile = dq_tile(P, DQM == DQ_SPLIT ? I.kt : 0, h, tile);
         const bool dq_ok = ATTN_INDEX_OK(P, h >= 0 && h < P.hq && tile >= 0 && tile < P.ntiles &&
                                                 (DQM != DQ_SPLIT || (I.kt >= 0 && I.kt < P.nsplits)), 1);
 #pragma unroll 1
         for (int mb = 0; mb < C::NMB && ok; ++mb) {
           const int rows = min(128, C::DA - mb * 128);
+          if constexpr (C::SEQDQ) {   // the M blocks take turns in one region
+            if (!(ok = wait_bar(ctx, B_DQ_FULL, (gs * C::NMB + mb) & 1, 31))) break;
+            tc_fence_after();
+          }
 #pragma unroll 1
           for (int hx = 0; hx < 2; ++hx) {     // query columns 0-31, then 32-63
             uint32_t v[32];
-            tmem_ld32(lane_addr + C::T_DQ + mb * BM + hx * 32, v);
+            tmem_ld32(lane_addr + C::T_DQ + (C::SEQDQ ? 0 : mb * BM) + hx * 32, v);
             tmem_wait_ld();
-            if (mb == C::NMB - 1 && hx == 1) {
+            if ((C::SEQDQ || mb == C::NMB - 1) && hx == 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(bar + B_DQ_EMPTY);
