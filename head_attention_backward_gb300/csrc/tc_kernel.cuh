@@ -90,20 +90,6 @@ struct Cfg {
   static constexpr int ST = DQK <= 128 ? 3 : DQK <= 192 ? 2 : 1;   // Q/dO pipeline stages
   static constexpr int KCH = BN * 128;                  // bytes of one 64-wide k/v chunk
   static constexpr int QCH = BM * 128;                  // bytes of one 64-wide q/dO chunk
-  // shared memory map (1024-byte aligned regions)
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + NCK_PAD * KCH;
-  static constexpr int OFF_Q = OFF_V + NCV * KCH;
-  static constexpr int OFF_DO = OFF_Q + ST * NCK * QCH;
-  static constexpr int DS_BYTES = BN * BM * 2;            // one dS^T buffer, bf16 [128 keys][64 queries]
-  static constexpr int OFF_DS = OFF_DO + ST * NCV * QCH;   // two dS^T buffers (steps alternate)
-  static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;      // [ST][BM] -LSE*log2(e)
-  static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
-  static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
-  static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NR;
-  static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_MISC = OFF_RING + NI * 16;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + NR * 8 + 1024;  // + alignment slack
   // TMEM column map; the two P^T buffers (bf16, two per column) are MMA A operands
   static constexpr int T_DK = 0;
   static constexpr int T_DV = DA;
@@ -120,7 +106,22 @@ struct Cfg {
   static constexpr int T_P = SEQDQ ? T_S : T_DQ + NMB * BM;   // P^T buffers 0 and 1 (SEQDQ: one, over S^T)
   static_assert((SEQDQ ? T_DQ + BM : T_P + BM) <= (int)TMEM_COLS, "TMEM overflow");
   static_assert(!SEQDQ || (NPASS == 1 && BM / 16 * 16 == BM), "SEQDQ: single pass");
+  // shared memory map (1024-byte aligned regions)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NCK_PAD * KCH;
+  static constexpr int OFF_Q = OFF_V + NCV * KCH;
+  static constexpr int OFF_DO = OFF_Q + ST * NCK * QCH;
+  static constexpr int DS_BYTES = BN * BM * 2;            // one dS^T buffer, bf16 [128 keys][64 queries]
+  static constexpr int OFF_DS = OFF_DO + ST * NCV * QCH;   // two dS^T buffers (steps alternate)
+  static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;      // [ST][BM] -LSE*log2(e)
+  static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
+  static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
+  static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NR;
+  static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_MISC = OFF_RING + NI * 16;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + NR * 8 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+  static_assert(OFF_BAR % 16 == 0 && OFF_RING % 16 == 0 && OFF_MISC % 16 == 0, "barrier / ring alignment");
   static constexpr uint32_t KV_BYTES = (NCK + NCV) * KCH;
   static constexpr uint32_t QDO_BYTES = (NCK + NCV) * QCH;
 };
@@ -131,6 +132,7 @@ enum {
   B_KV_FULL = 0, B_KV_EMPTY, B_SDP_FULL, B_SDP_EMPTY, B_PDS_FULL, B_PDS_EMPTY = B_PDS_FULL + 2,
   B_DQ_FULL = B_PDS_EMPTY + 2, B_DQ_EMPTY, B_DKV_FULL, B_DKV_EMPTY, B_DRAIN, B_DRAIN2,
   B_P_FREE,   // SEQDQ: dV has read the P^T written over S^T
+  B_P_FULL,   // SEQDQ: P^T is in TMEM (dS^T follows with B_PDS_FULL)
   B_FIXED_END = 16
 };
 
@@ -317,6 +319,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
     mbar_init(bar + B_DRAIN, 1);
     mbar_init(bar + B_DRAIN2, 1);
     mbar_init(bar + B_P_FREE, 1);
+    mbar_init(bar + B_P_FULL, NUM_SOFTMAX_WARPS);
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(bar + B_Q_FULL + s, 32 + 1);   // 32 cp.async arrivals + the TMA expect_tx arrival
       mbar_init(bar + B_Q_EMPTY + s, 1);
@@ -506,8 +509,8 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         const uint64_t a_ds = ddS_k + ((pb * C::DS_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
-          umma_ts(tmem + C::T_DV, tmem + (C::SEQDQ ? C::T_S + ks * 16 : C::T_P + pb * (BM / 2) + ks * 8),
-                  d + ((ks * 2048) >> 4), ID_DV, ks > 0 ? 1u : acc_first);
+          umma_ts(tmem + C::T_DV, tmem + C::T_P + pb * (BM / 2) + ks * 8, d + ((ks * 2048) >> 4), ID_DV,
+                  ks > 0 ? 1u : acc_first);
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks)
           umma_ss(tmem + C::T_DK, a_ds + ((ks * 32) >> 4), q + ((ks * 2048) >> 4), ID_DK, ks > 0 ? 1u : acc_first);
@@ -515,6 +518,23 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
 #ifdef ATTN_WAIT_STATS
         stat_add(g_wait_stats, 5, (unsigned long long)(clock64() - t0));   // dV/dK group issue
 #endif
+      };
+      // SEQDQ (single pass): dV += P^T dO with P^T over S^T, then separately
+      // dK += dS^T Q, whose commit frees the Q/dO stage
+      auto mma_dv = [&](uint32_t gs, uint32_t acc_first) {
+        const uint64_t d = ddO_mn + (((gs % C::ST) * C::NCV * C::QCH) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          umma_ts(tmem + C::T_DV, tmem + C::T_S + ks * 16, d + ((ks * 2048) >> 4), ID_DV, ks > 0 ? 1u : acc_first);
+      };
+      auto mma_dk = [&](uint32_t gs, uint32_t acc_first) {
+        const uint32_t st = gs % C::ST;
+        const uint64_t q = dQ_mn + ((st * C::NCK * C::QCH) >> 4);
+        const uint64_t a_ds = ddS_k + (((gs & 1) * C::DS_BYTES) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          umma_ss(tmem + C::T_DK, a_ds + ((ks * 32) >> 4), q + ((ks * 2048) >> 4), ID_DK, ks > 0 ? 1u : acc_first);
+        umma_commit(bar + B_Q_EMPTY + st);
       };
       // The dQ^T TMEM of the previous step has been drained.
       auto wait_dq = [&](uint32_t gs) -> bool {
@@ -579,11 +599,16 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
               ++kvp;
               if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (kvp & 1) ^ 1, 17))) break;
             }
-            if (!(ok = wait_pds(gs))) break;
-            tc_fence_after();
-            mma_dvdk(gs, pass_first ? 0u : 1u, pass);
             if constexpr (C::SEQDQ) {
+              // dV as soon as P^T is written (S^T of the next step waits for
+              // it), dK and the dQ^T blocks once dS^T is
+              if (!(ok = wait_bar(ctx, B_P_FULL, gs & 1, 24))) break;
+              tc_fence_after();
+              mma_dv(gs, pass_first ? 0u : 1u);
               umma_commit(bar + B_P_FREE);
+              if (!(ok = wait_pds(gs))) break;
+              tc_fence_after();
+              mma_dk(gs, pass_first ? 0u : 1u);
 #pragma unroll 1
               for (int mb = 0; mb < C::NMB; ++mb) {
                 if (!(ok = wait_bar(ctx, B_DQ_EMPTY, ((gs * C::NMB + mb) & 1) ^ 1, 16))) break;
@@ -593,6 +618,9 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
               if (!ok) break;
               umma_commit(bar + B_PDS_EMPTY + (gs & 1));
             } else {
+            if (!(ok = wait_pds(gs))) break;
+            tc_fence_after();
+            mma_dvdk(gs, pass_first ? 0u : 1u, pass);
             if (!(ok = wait_dq(gs))) break;
             tc_fence_after();
             mma_dq(gs, pass);
@@ -716,6 +744,46 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
             pk[c >> 1] = pack2(p2[0], p2[1], (T*)nullptr);
             dk[c >> 1] = pack2(d2[0], d2[1], (T*)nullptr);
           }
+        } else if constexpr (C::SEQDQ) {
+          // P^T first, handed over on its own (dV and the next S^T need only
+          // it), then dS^T
+          float pf[CW];
+#pragma unroll
+          for (int c4 = 0; c4 < CW / 4; ++c4) {
+            const float4 nl = nl4[c4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int c = 4 * c4 + 2 * hh;
+              const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2,
+                                    hh ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y));
+              float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+              if (!full) {
+                const int q = q_first + c0 + c;
+                p0 = (key_ok && q < I.sg.lq && visible(I.m, q, kk)) ? p0 : 0.f;
+                p1 = (key_ok && q + 1 < I.sg.lq && visible(I.m, q + 1, kk)) ? p1 : 0.f;
+              }
+              pf[c] = p0;
+              pf[c + 1] = p1;
+              pk[c >> 1] = pack2(p0, p1, (T*)nullptr);
+            }
+          }
+          tmem_st8(lane_addr + C::T_S + c0, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar + B_P_FULL);
+#pragma unroll
+          for (int c4 = 0; c4 < CW / 4; ++c4) {
+            const float4 dd = d4[c4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int c = 4 * c4 + 2 * hh;
+              const float2 ds = mul2(make_float2(pf[c], pf[c + 1]),
+                                     sub2(make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                          hh ? make_float2(dd.z, dd.w) : make_float2(dd.x, dd.y)));
+              dk[c >> 1] = pack2(ds.x, ds.y, (T*)nullptr);
+            }
+          }
         } else {
 #pragma unroll
         for (int c4 = 0; c4 < CW / 4; ++c4) {
@@ -742,16 +810,29 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         // P^T and dS^T go to buffer gs & 1; the other one may still be read
         // by the previous step's dV / dK / dQ^T MMAs
         const uint32_t pb = gs & 1;
-        if (!(ok = wait_bar(ctx, B_PDS_EMPTY + pb, ((gs >> 1) & 1) ^ 1, 23))) break;
-        tc_fence_after();
-        tmem_st8(lane_addr + (C::SEQDQ ? C::T_S + c0 : C::T_P + pb * (BM / 2) + c0 / 2), pk);
+        if constexpr (C::SEQDQ) {
+          // P^T over this thread's own S^T columns (read above) needs no wait
+          if constexpr (FX) {
+            tmem_st8(lane_addr + C::T_S + c0, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + B_P_FULL);
+          }
+          if (!(ok = wait_bar(ctx, B_PDS_EMPTY + pb, ((gs >> 1) & 1) ^ 1, 23))) break;
+          tc_fence_after();
+        } else {
+          if (!(ok = wait_bar(ctx, B_PDS_EMPTY + pb, ((gs >> 1) & 1) ^ 1, 23))) break;
+          tc_fence_after();
+          tmem_st8(lane_addr + C::T_P + pb * (BM / 2) + c0 / 2, pk);
+        }
 #pragma unroll
         for (int j = 0; j < CW / 8; ++j) {
           const int ch = grp * (CW / 8) + j;
           *reinterpret_cast<uint4*>(dsRow + pb * C::DS_BYTES + ((ch ^ (r & 7)) << 4)) =
               make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
         }
-        tmem_wait_st();
+        if constexpr (!C::SEQDQ) tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
