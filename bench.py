@@ -109,9 +109,9 @@ def dq_mode(wl):
 
 def dq_mode_run(wl):
     """The dQ accumulation the library runs for the workload: the ordered fold
-    is served by the split slices for fp32 inputs and head dim 256."""
+    is served by the split slices for fp32 inputs."""
     m = dq_mode(wl)
-    if m == DQ_MODES["ordered"] and (wl.dtype == torch.float32 or wl.d_qk > 192):
+    if m == DQ_MODES["ordered"] and wl.dtype == torch.float32:
         return DQ_MODES["split"]
     return m
 

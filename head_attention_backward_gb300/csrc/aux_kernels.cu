@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(256, PRE_BLOCKS_PER_SM) preprocess_kernel(Prob
   if (P.fold) {
     // ordered fold: no partial folded yet, and the first KV tile reaching
     // each query tile (a partial's rank is its KV tile minus that one)
-    const long long n = (long long)P.hq * P.ntiles;
+    const long long n = (long long)tc_passes(P.dqk) * P.hq * P.ntiles;
     for (long long i = tid; i < n; i += nthreads) P.turn[i] = 0u;
     for (long long t = tid; t < P.ntiles; t += nthreads) {
       int b, qt, k = -1;

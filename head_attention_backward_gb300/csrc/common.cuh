@@ -76,7 +76,7 @@ struct Problem {
   int* tile_off;     // group mode: first query-tile index of each segment [nseg+1]
   int ntiles;        // query tiles per (slice, head): B*ceil(Sq/BM) or an upper bound
   float* dq_acc;     // [nsplits][Hq][ntiles] query-major tiles of BM x dqk fp32 (see dq_tile)
-  unsigned* turn;    // fold mode: [Hq][ntiles] partials folded so far per query tile
+  unsigned* turn;    // fold mode: [passes][Hq][ntiles] partials folded so far per query tile
   int* klo;          // fold mode: [ntiles] first KV tile that reaches each query tile
   long long n_lse;   // rows of the LSE layout = B*Hq*Sq or Hq*Tq
   // attention bias and dropout (the kernels' extras variant)
@@ -105,11 +105,15 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Workspace layout: pure function of the scalar problem fields, used by both
 // attn_bwd_workspace_size and attn_bwd.
 // Deterministic dQ by the ordered fold: the tensor-core kernel in
-// ATTN_DET_ORDERED mode with one pass per KV tile (the fp32 kernel and the
-// two-pass head dim 256 use split slices).
+// ATTN_DET_ORDERED mode (the fp32 kernel uses split slices).
 inline bool det_fold(const attn_bwd_params& p) {
-  return p.deterministic == ATTN_DET_ORDERED && p.dtype != ATTN_FP32 && p.d_qk <= 192;
+  return p.deterministic == ATTN_DET_ORDERED && p.dtype != ATTN_FP32;
 }
+
+// Passes per KV tile of the tensor-core kernel: head dim 256 works its dK /
+// dV / dQ columns in two halves; the ordered fold keeps one turn counter per
+// (pass, query head, query tile).
+__host__ __device__ constexpr int tc_passes(int d_qk) { return d_qk > 192 ? 2 : 1; }
 
 inline WsLayout ws_layout(const attn_bwd_params& p) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -141,7 +145,7 @@ inline WsLayout ws_layout(const attn_bwd_params& p) {
   L.off_dvec = o;  o = up(o + (size_t)L.n_lse * sizeof(float));
   L.off_items = o; o = up(o + (size_t)(L.max_items > 0 ? L.max_items : 1) * sizeof(int4));
   L.off_tiles = o; o = up(o + (size_t)(p.batch + 1) * sizeof(int));
-  L.off_turn = o;  o = up(o + (L.fold ? (size_t)p.nhead_q * L.ntiles : 1) * sizeof(unsigned));
+  L.off_turn = o;  o = up(o + (L.fold ? (size_t)tc_passes(p.d_qk) * p.nhead_q * L.ntiles : 1) * sizeof(unsigned));
   L.off_klo = o;   o = up(o + (L.fold ? (size_t)L.ntiles : 1) * sizeof(int));
   L.off_dqacc = o;
   o = up(o + (size_t)L.nsplits * p.nhead_q * (size_t)L.ntiles * p.d_qk * BM * sizeof(float));

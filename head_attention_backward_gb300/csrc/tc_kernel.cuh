@@ -74,9 +74,12 @@ struct TmaMaps {
 template <int DQK, int DV>
 struct Cfg {
   // Head dims above 192 (256): dK, dV and dQ^T of a 128-key tile do not fit
-  // TMEM at full width, so each item runs NPASS passes over its query tiles,
-  // pass p accumulating the 128 columns [128 p, 128 p + 128) of dK, dV and
-  // dQ (S^T and dP^T are recomputed at full depth in every pass).
+  // TMEM at full width, so a KV tile is worked in NPASS passes over its query
+  // tiles, pass p accumulating the 128 columns [128 p, 128 p + 128) of dK, dV
+  // and dQ (S^T and dP^T are recomputed at full depth in every pass).  The
+  // passes touch disjoint columns, so each is a work item of its own (the
+  // work counter runs over items x passes; the item carries its pass in .w),
+  // which doubles the items a GPU's SMs share.
   static constexpr int DA = DQK > 192 ? 128 : DQK;      // dK / dQ columns per pass
   static constexpr int DVA = DQK > 192 ? 128 : DV;      // dV columns per pass
   static constexpr int NPASS = DQK / DA;
@@ -249,7 +252,7 @@ __device__ __forceinline__ bool acquire_turn(const Ctx& c, const uint32_t* turn,
   return true;
 }
 
-// Ordered fold: (query head, query tile) addresses a turn counter.
+// Ordered fold: (pass, query head, query tile) addresses a turn counter.
 __device__ __forceinline__ bool dq_ok_turn(const Problem& P, int h, int tile) {
   return h >= 0 && h < P.hq && tile >= 0 && tile < P.ntiles;
 }
@@ -272,7 +275,7 @@ template <int DQK, int DV, typename T, int DQM, bool FX>
 __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const __grid_constant__ TmaMaps maps, const Problem P) {
   using C = Cfg<DQK, DV>;
   constexpr bool FOLD = DQM == DQ_FOLD;
-  static_assert(!FOLD || C::NPASS == 1, "the ordered fold keeps one turn per query tile: single pass only");
+  static_assert(C::NPASS == tc_passes(DQK), "turn table and workspace are sized by tc_passes()");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -359,7 +362,11 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       int idx = 0;
       if (lane == 0) idx = atomicAdd(P.hdr + HDR_NEXT, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
-      const int4 item = idx < nitems ? P.items[idx] : make_int4(-1, 0, 0, 0);
+      int4 item = make_int4(-1, 0, 0, 0);
+      if (idx < nitems * C::NPASS) {
+        item = P.items[idx / C::NPASS];
+        item.w = idx % C::NPASS;   // the pass
+      }
       const int slot = n_item % NI;
       if (!wait_bar(ctx, B_IT_EMPTY + slot, ((n_item / NI) & 1) ^ 1, 1)) break;
       if (lane == 0) {
@@ -381,11 +388,11 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           tma_load_3d(smem + C::OFF_V + c * C::KCH, &maps.v, bar + B_KV_FULL, c * 64, I.hk, krow);
       }
       bool ok = true;
-      const int nrun = I.nsteps * C::NPASS;   // every pass reloads the query tiles
+      const int nrun = I.nsteps;
       for (int s = 0; s < nrun; ++s) {
         const uint32_t gs = g + s, st = gs % C::ST;
         int h, qt;
-        step_coords(P, I, C::NPASS == 1 ? s : s % I.nsteps, h, qt);
+        step_coords(P, I, s, h, qt);
         if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
         // -LSE*log2(e) and D of the tile's 64 query rows, copied asynchronously;
         // rows past the segment end read as zeros (their columns are masked)
@@ -574,8 +581,9 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         if (item.x < 0) break;
         const ItemInfo I = item_info(P, item);
         if (I.nsteps == 0) continue;
-        const int nrun = I.nsteps * C::NPASS;
+        const int nrun = I.nsteps;
         const uint32_t last = g + nrun - 1;
+        const int pass = C::NPASS == 1 ? 0 : item.w;
         if (is_sdp) {
           if (!(ok = wait_bar(ctx, B_KV_FULL, it & 1, 14))) break;
           for (uint32_t gs = g; gs <= last; ++gs) {
@@ -590,15 +598,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         } else {
           if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (kvp & 1) ^ 1, 17))) break;
           for (uint32_t gs = g; gs <= last; ++gs) {
-            const int pass = C::NPASS == 1 ? 0 : (int)(gs - g) / I.nsteps;
-            const bool pass_first = C::NPASS == 1 ? gs == g : (int)(gs - g) == pass * I.nsteps;
-            if (C::NPASS > 1 && pass_first && pass > 0) {
-              // the previous pass's dK/dV columns are complete: to the drain,
-              // and wait until it has read them before accumulating the next
-              umma_commit(bar + B_DKV_FULL);
-              ++kvp;
-              if (!(ok = wait_bar(ctx, B_DKV_EMPTY, (kvp & 1) ^ 1, 17))) break;
-            }
+            const bool pass_first = gs == g;
             if constexpr (C::SEQDQ) {
               // dV as soon as P^T is written (S^T of the next step waits for
               // it), dK and the dQ^T blocks once dS^T is
@@ -665,11 +665,11 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       const int kk = I.kt * BN + r;                    // segment-local key index
       const bool key_ok = r < I.klen;
       bool ok = true;
-      const int nrun = I.nsteps * C::NPASS;   // every pass recomputes P and dS
+      const int nrun = I.nsteps;
       for (int s = 0; s < nrun; ++s) {
         const uint32_t gs = g + s, st = gs % C::ST;
         int h, qt;
-        step_coords(P, I, C::NPASS == 1 ? s : s % I.nsteps, h, qt);
+        step_coords(P, I, s, h, qt);
         // extras: this thread's 16 bias values (key kk, the step's query
         // columns), loaded before the S/dP wait so that it hides their latency
         uint32_t braw[FX ? CW / 2 : 1];
@@ -898,12 +898,13 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       // loop: measured faster than at the stores)
       const long long kofs = elem_off(P.sdk_, krow, I.hk);
       const long long vofs = elem_off(P.sdv_, krow, I.hk);
-      if (I.nsteps == 0) {
+      if (I.nsteps == 0) {   // no query reaches these keys: zero dK / dV (this pass's columns)
         if (L < I.klen && ATTN_INDEX_OK(P, krow >= 0 && krow < rows_k(P), 2)) {
-          T* dk = dKg + kofs;
-          T* dv = dVg + vofs;
-          for (int e = 0; e < DQK; ++e) dk[e] = TypeOps<T>::from_f(0.f);
-          for (int e = 0; e < DV; ++e) dv[e] = TypeOps<T>::from_f(0.f);
+          const int pz = C::NPASS == 1 ? 0 : item.w;
+          T* dk = dKg + kofs + pz * C::DA;
+          T* dv = dVg + vofs + pz * C::DVA;
+          for (int e = 0; e < C::DA; ++e) dk[e] = TypeOps<T>::from_f(0.f);
+          for (int e = 0; e < C::DVA; ++e) dv[e] = TypeOps<T>::from_f(0.f);
         }
         continue;
       }
@@ -956,19 +957,18 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         return true;
       };
       bool ok = true;
-      const int nrun = I.nsteps * C::NPASS;
+      const int nrun = I.nsteps;
+      const int pass = C::NPASS == 1 ? 0 : item.w;
       for (int s = 0; s < nrun; ++s) {
         const uint32_t gs = g + s;
-        const int pass = C::NPASS == 1 ? 0 : s / I.nsteps;
-        const int sl = C::NPASS == 1 ? s : s - pass * I.nsteps;
         int h, qt;
-        step_coords(P, I, sl, h, qt);
+        step_coords(P, I, s, h, qt);
         const int tile = qtile_index(P, I.b, qt);
         // ordered fold: this partial is number `rank` of the tile's sum; lane 0
         // of each warp reads the tile's counter before the dQ tile is ready
         uint32_t idx = 0, rank = 0, seen = ~0u;
         if (FOLD && lane == 0 && ATTN_INDEX_OK(P, dq_ok_turn(P, h, tile), 5)) {
-          idx = (uint32_t)(h * P.ntiles + tile);
+          idx = (uint32_t)((pass * P.hq + h) * P.ntiles + tile);
           const int k0 = __ldg(P.klo + tile);
           rank = (uint32_t)(I.kt - k0);
           if (ATTN_INDEX_OK(P, k0 >= 0 && k0 <= I.kt, 6)) seen = ld_acquire_gpu(P.turn + idx);
@@ -1039,12 +1039,10 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
-        // multi-pass: the dK/dV columns of a pass are complete after its last step
-        if (C::NPASS > 1 && sl == I.nsteps - 1 && pass < C::NPASS - 1 && !(ok = write_dkdv(pass))) break;
       }
       if (!ok) break;
       g += nrun;
-      if (!write_dkdv(C::NPASS - 1)) break;
+      if (!write_dkdv(pass)) break;
     }
   }
 
@@ -1120,7 +1118,8 @@ static int launch_typed(const Problem& P, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int grid = sms > 0 ? sms : 1;
-  if (P.max_items < grid) grid = P.max_items;
+  const int nvirt = P.max_items * Cfg<DQK, DV>::NPASS;   // work items x passes
+  if (nvirt < grid) grid = nvirt;
   if (grid <= 0) return ATTN_OK;
   // The ordered fold makes CTAs wait for one another (a partial waits for the
   // partials of lower KV tiles, which items dealt earlier hold), so that mode
@@ -1144,9 +1143,7 @@ static int launch_dims(const Problem& P, cudaStream_t st) {
   if (P.dqk == 128 && P.dv == 128) return launch_typed<128, 128, T, DQM, FX>(P, st);
   if (P.dqk == 64 && P.dv == 64) return launch_typed<64, 64, T, DQM, FX>(P, st);
   if (P.dqk == 192 && P.dv == 128) return launch_typed<192, 128, T, DQM, FX>(P, st);
-  if constexpr (DQM != DQ_FOLD) {
-    if (P.dqk == 256 && P.dv == 256) return launch_typed<256, 256, T, DQM, FX>(P, st);
-  }
+  if (P.dqk == 256 && P.dv == 256) return launch_typed<256, 256, T, DQM, FX>(P, st);
   return ATTN_ERR_UNSUPPORTED_HEADDIM;
 }
 

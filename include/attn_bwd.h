@@ -242,8 +242,8 @@ typedef struct {
  *   ATTN_DET_ORDERED: in ascending KV-tile order, each partial added into one
  *     fp32 dq_acc tile in turn (a per-tile turn counter serialises the adds,
  *     so the sum is bitwise repeatable; partials never leave the L2 cache
- *     as separate slices).  FP32 inputs and head dim 256 (whose two passes add
- *     each partial in two column halves) use the split slices instead;
+ *     as separate slices; at head dim 256 each column half has its own
+ *     counters).  FP32 inputs use the split slices instead;
  *   ATTN_DET_SPLIT: each partial stored to its own dq_acc slice, nsplits =
  *     ceil(seqlen_k / 128), then summed in ascending slice order by a
  *     reduction kernel -- the split workspace of aiter PR #2216 (Motivation).
@@ -262,9 +262,9 @@ typedef enum { ATTN_DET_ATOMIC = 0, ATTN_DET_ORDERED = 1, ATTN_DET_SPLIT = 2 } a
  * group mode (each segment's rows start a new tile: a per-segment padded
  * layout, the kind TransformerEngine PR #671's Fix switches dq_acc to, with
  * one layout shared by the sizing call and the kernels).  ATTN_DET_SPLIT (and
- * ATTN_DET_ORDERED with FP32 inputs or d_qk = 256) uses nsplits = ceil(seqlen_k / 128)
+ * ATTN_DET_ORDERED with FP32 inputs) uses nsplits = ceil(seqlen_k / 128)
  * slices, the other modes one; ATTN_DET_ORDERED adds a turn counter per
- * query tile and head.  Small per-row and per-tile tables come on top.
+ * query tile and head (two at d_qk = 256, one per column half).  Small per-row and per-tile tables come on top.
  * Writes the size to *bytes.  Returns ATTN_OK or an error code. */
 int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes);
 

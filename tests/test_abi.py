@@ -120,12 +120,16 @@ def test_workspace_size_fp32_ordered_uses_split_slices(lib):
     assert n >= (4096 // 128) * 2 * 32 * 4096 * 64 * 4
 
 
-def test_workspace_size_head_dim_256_ordered_uses_split_slices(lib):
-    """d_qk = 256 runs two passes per KV tile (one per column half), so the
-    deterministic request is served by the split slices."""
+def test_workspace_size_head_dim_256_ordered_folds_into_one_slice(lib):
+    """d_qk = 256 runs two passes per KV tile (one per column half); the
+    ordered fold keeps one slice, with a turn counter per pass, head and
+    query tile."""
     st, n = B.attn_bwd_workspace_size(make(d_qk=256, d_v=256, deterministic=B.DET_ORDERED))
     assert st == 0
-    assert n >= (4096 // 128) * 2 * 32 * 4096 * 256 * 4
+    one = 2 * 32 * 4096 * 256 * 4
+    assert one <= n < one + 16 * 2**20
+    st, n_split = B.attn_bwd_workspace_size(make(d_qk=256, d_v=256, deterministic=B.DET_SPLIT))
+    assert st == 0 and n_split >= (4096 // 128) * one
 
 
 def test_workspace_size_atomic_one_slice(lib):

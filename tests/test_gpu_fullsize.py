@@ -87,13 +87,22 @@ def test_window_dqk192_dv128_S8192(B, det):
     assert_all_ok(_check_batch(wl, x, got, [(0, 0), (0, 15)], [(0, 5)], 5), f"window det={det}")
 
 
-@pytest.mark.parametrize("det", [0, 1], ids=["atomic", "det"])
+@pytest.mark.parametrize("det", [0, 1, 2], ids=["atomic", "ordered", "split"])
 def test_head_dim_256_B1_Hq16_Hkv4_S4096(B, det):
-    """Head dim 256: two passes per KV tile, one per column half of dK, dV, dQ
-    (the deterministic request runs on the split slices)."""
+    """Head dim 256: two passes per KV tile, one per column half of dK, dV, dQ,
+    each pass a work item of its own (the ordered fold keeps turn counters
+    per pass)."""
     wl = W.gqa_d256(deterministic=det)
     x, _, got = _run(B, wl, det)
     assert_all_ok(_check_batch(wl, x, got, [(0, 0), (0, 15), (0, 6)], [(0, 0), (0, 3)], 6), f"d256 det={det}")
+
+
+def test_head_dim_256_ordered_fold_equals_split_bits(B):
+    wl = W.gqa_d256(deterministic=True)
+    _, _, a = _run(B, wl, 1)
+    _, _, b = _run(B, wl, 2)
+    for name, x, y in zip(("dq", "dk", "dv"), a, b):
+        assert torch.equal(x, y), name
 
 
 @pytest.mark.parametrize("det", [0, 1, 2], ids=["atomic", "ordered", "split"])

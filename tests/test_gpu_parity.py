@@ -343,6 +343,9 @@ DET_CASES = [
     _wl("det_win192", torch.bfloat16, 1, 4, 2, 700, 700, 192, 128, W.MASK_WINDOW, 200, 0, seed=42),
     _wl("det_br_short_k", torch.bfloat16, 1, 4, 4, 500, 300, 128, 128, W.MASK_CAUSAL_BOTTOM_RIGHT, seed=43),
     W.thd("det_thd", [700, 1, 129, 300, 64], hq=8, hkv=2, seed=44),
+    # head dim 256: two column-half passes per KV tile, each with its own turn counters
+    _wl("det_d256", torch.bfloat16, 1, 4, 2, 600, 600, 256, 256, W.MASK_CAUSAL_TOP_LEFT, seed=45),
+    W.thd("det_thd_d256", [300, 1, 129, 200], hq=4, hkv=2, d_qk=256, d_v=256, seed=46),
 ]
 
 
