@@ -75,8 +75,8 @@ def peaks():
 KERNEL_SOURCES = ("tc_kernel.cuh", "tc_kernel.cu", "common.cuh", "sm100_ptx.cuh")
 KERNEL_TRAFFIC = {
     "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:ordered": {
-        "bytes": 622.7e6 + 281.4e6,
-        "src": "1de98bb1c424320e",
+        "bytes": 621.5e6 + 278.6e6,
+        "src": "b731cec2bb213e57",
         "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
 }
 
