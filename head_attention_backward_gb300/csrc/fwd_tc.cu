@@ -12,7 +12,8 @@
 //   O += P V                   (M = queries, N = d_v,  K = keys)   TMEM x SMEM
 //
 // S is double-buffered in TMEM, so S of the next tile is computed while the
-// softmax warps work on this one; K and V come in by TMA, two stages deep.
+// softmax warps work on this one; K and V come in by TMA in rings of their
+// own (K three tiles deep at d_qk <= 128 and freed once S is computed, V two).
 // The running max is only moved (and O rescaled in TMEM) when a row's max
 // grows by more than 2^8, so that P = exp2(x - m) <= 256 stays exact enough
 // in 16 bits and most tiles skip the rescale.  At the end O / l goes to
@@ -41,7 +42,7 @@ constexpr int NUM_SM_WARPS = 8;          // softmax / epilogue warps: two per TM
 constexpr int SM_COLS = FN / 2;          // key columns of one softmax warp
 constexpr int FIRST_SM_WARP = 2;
 constexpr int NTHREADS = 32 * (FIRST_SM_WARP + NUM_SM_WARPS);
-constexpr int STAGES = 2;                // K/V pipeline depth
+constexpr int V_STAGES = 2;              // V ring depth (K has its own ring, FCfg::KST)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t SLEEP_HINT_NS = 20000;
 constexpr uint32_t TMEM_COLS = 512;
@@ -53,15 +54,21 @@ struct FCfg {
   static constexpr int NCV = DV / 64;
   static constexpr int CH = 128 * 128;                    // one 64-wide chunk of 128 rows
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + NCK * CH;
-  static constexpr int STAGE = (NCK + NCV) * CH;
-  static constexpr int OFF_BAR = OFF_KV + STAGES * STAGE;
+  // K and V in rings of their own: a K tile is free once S = Q K^T is done,
+  // so K runs KST - 1 tiles ahead; a V tile waits for its P V
+  static constexpr int KST = DQK <= 128 ? 3 : 2;
+  static constexpr int KSTAGE = NCK * CH;
+  static constexpr int VSTAGE = NCV * CH;
+  static constexpr int OFF_K = OFF_Q + NCK * CH;
+  static constexpr int OFF_V = OFF_K + KST * KSTAGE;
+  static constexpr int OFF_BAR = OFF_V + V_STAGES * VSTAGE;
   static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RED = OFF_MISC + 64;            // [3 slots][2 halves][128 rows] fp32
   static constexpr int SMEM_BYTES = OFF_RED + 3 * 2 * 128 * 4 + 1024;   // + alignment slack
   static constexpr uint32_t Q_BYTES = NCK * CH;
-  static constexpr uint32_t KV_BYTES = (NCK + NCV) * CH;
+  static constexpr uint32_t K_BYTES = NCK * CH;
+  static constexpr uint32_t V_BYTES = NCV * CH;
   // TMEM columns: two S buffers, O, P (bf16/fp16 pairs, the A operand of P V)
   static constexpr int T_S = 0;
   static constexpr int T_O = 2 * FN;
@@ -71,7 +78,8 @@ struct FCfg {
 };
 
 enum {
-  B_Q_FULL = 0, B_KV_FULL = 1, B_KV_EMPTY = B_KV_FULL + STAGES, B_S_FULL = B_KV_EMPTY + STAGES,
+  B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = B_K_FULL + 3, B_V_FULL = B_K_EMPTY + 3, B_V_EMPTY = B_V_FULL + V_STAGES,
+  B_S_FULL = B_V_EMPTY + V_STAGES,
   B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2, B_PV_DONE, B_DRAIN,
   // the two warps of a row block exchange row maxima per tile ([quarter][tile parity])
   // and row sums at the end ([quarter]); two lane-0 arrivals each
@@ -140,6 +148,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
 template <int DQK, int DV, typename T>
 __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_constant__ Maps maps, const Args A) {
   using C = FCfg<DQK, DV>;
+  static_assert(C::KST <= 3 && B_END <= C::NBAR, "barrier slots");
   const int qt = gridDim.x - 1 - blockIdx.x;   // the longest causal tiles first
   const int h = blockIdx.y, b = blockIdx.z, hk = h / A.g;
   int q0, lq, k0, lk;
@@ -173,9 +182,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar + B_Q_FULL, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar + B_KV_FULL + s, 1);
-      mbar_init(bar + B_KV_EMPTY + s, 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(bar + B_K_FULL + s, 1);
+      mbar_init(bar + B_K_EMPTY + s, 1);
+    }
+    for (int s = 0; s < V_STAGES; ++s) {
+      mbar_init(bar + B_V_FULL + s, 1);
+      mbar_init(bar + B_V_EMPTY + s, 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar + B_S_FULL + s, 1);
@@ -205,20 +218,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       mbar_arrive_expect_tx(bar + B_Q_FULL, C::Q_BYTES);
       for (int c = 0; c < C::NCK; ++c)
         tma_load_3d(smem + C::OFF_Q + c * C::CH, &maps.q, bar + B_Q_FULL, c * 64, h, q0 + qs);
-      int j = 0;
-      for (; j < nkv; ++j) {
-        const int s = j % STAGES;
-        if (!wait_bar(ctx, B_KV_EMPTY + s, ((j / STAGES) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(bar + B_KV_FULL + s, C::KV_BYTES);
-        const int krow = k0 + (kt0 + j) * FN;
-        uint8_t* kv = smem + C::OFF_KV + s * C::STAGE;
-        for (int c = 0; c < C::NCK; ++c) tma_load_3d(kv + c * C::CH, &maps.k, bar + B_KV_FULL + s, c * 64, hk, krow);
-        for (int c = 0; c < C::NCV; ++c)
-          tma_load_3d(kv + (C::NCK + c) * C::CH, &maps.v, bar + B_KV_FULL + s, c * 64, hk, krow);
+      // K tile i and V tile i - (KST - 1) in turn: K runs ahead
+      constexpr int LEAD = C::KST - 1;
+      int jk = 0, jv = 0;   // K / V tiles issued
+      for (int i = 0; i < nkv + LEAD; ++i) {
+        if (i < nkv) {
+          const int s = i % C::KST;
+          if (!wait_bar(ctx, B_K_EMPTY + s, ((i / C::KST) & 1) ^ 1)) break;
+          mbar_arrive_expect_tx(bar + B_K_FULL + s, C::K_BYTES);
+          const int krow = k0 + (kt0 + i) * FN;
+          for (int c = 0; c < C::NCK; ++c)
+            tma_load_3d(smem + C::OFF_K + s * C::KSTAGE + c * C::CH, &maps.k, bar + B_K_FULL + s, c * 64, hk, krow);
+          ++jk;
+        }
+        const int v = i - LEAD;
+        if (v >= 0 && v < nkv) {
+          const int s = v % V_STAGES;
+          if (!wait_bar(ctx, B_V_EMPTY + s, ((v / V_STAGES) & 1) ^ 1)) break;
+          mbar_arrive_expect_tx(bar + B_V_FULL + s, C::V_BYTES);
+          const int krow = k0 + (kt0 + v) * FN;
+          for (int c = 0; c < C::NCV; ++c)
+            tma_load_3d(smem + C::OFF_V + s * C::VSTAGE + c * C::CH, &maps.v, bar + B_V_FULL + s, c * 64, hk, krow);
+          ++jv;
+        }
       }
       // no copy may still be writing this CTA's shared memory when it exits
       wait_bar(ctx, B_Q_FULL, 0);
-      for (int i = j - 1; i >= 0 && i >= j - STAGES; --i) wait_bar(ctx, B_KV_FULL + i % STAGES, (i / STAGES) & 1);
+      for (int i = jk - 1; i >= 0 && i >= jk - C::KST; --i) wait_bar(ctx, B_K_FULL + i % C::KST, (i / C::KST) & 1);
+      for (int i = jv - 1; i >= 0 && i >= jv - V_STAGES; --i) wait_bar(ctx, B_V_FULL + i % V_STAGES, (i / V_STAGES) & 1);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
@@ -227,32 +254,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       constexpr uint32_t ID_S = idesc_f16(FM, FN, false, false, F16);
       constexpr uint32_t ID_PV = idesc_f16(FM, DV, false, true, F16);
       const uint64_t dQ = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);        // K-major
-      const uint64_t dK = sdesc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);       // K-major, stage 0
-      const uint64_t dV = sdesc_sw128(smem_u32(smem + C::OFF_KV + C::NCK * C::CH), C::CH, 1024);   // MN-major
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);        // K-major, stage 0
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + C::OFF_V), C::CH, 1024);     // MN-major, stage 0
       bool ok = wait_bar(ctx, B_Q_FULL, 0);
       auto issue_pv = [&](int j) -> bool {
-        if (!wait_bar(ctx, B_P_FULL, j & 1)) return false;
+        if (!wait_bar(ctx, B_P_FULL, j & 1) || !wait_bar(ctx, B_V_FULL + j % V_STAGES, (j / V_STAGES) & 1))
+          return false;
         tc_fence_after();
-        const uint64_t v = dV + (((j % STAGES) * C::STAGE) >> 4);
+        const uint64_t v = dV + (((j % V_STAGES) * C::VSTAGE) >> 4);
 #pragma unroll
         for (int ks = 0; ks < FN / 16; ++ks)
           umma_ts(tmem + C::T_O, tmem + C::T_P + ks * 8, v + ((ks * 2048) >> 4), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
         umma_commit(bar + B_PV_DONE);
-        umma_commit(bar + B_KV_EMPTY + j % STAGES);
+        umma_commit(bar + B_V_EMPTY + j % V_STAGES);
         return true;
       };
       for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % STAGES, sb = j & 1;
-        if (!(ok = wait_bar(ctx, B_KV_FULL + s, (j / STAGES) & 1))) break;
+        const int s = j % C::KST, sb = j & 1;
+        if (!(ok = wait_bar(ctx, B_K_FULL + s, (j / C::KST) & 1))) break;
         if (!(ok = wait_bar(ctx, B_S_EMPTY + sb, ((j >> 1) & 1) ^ 1))) break;
         tc_fence_after();
-        const uint64_t k = dK + ((s * C::STAGE) >> 4);
+        const uint64_t k = dK + ((s * C::KSTAGE) >> 4);
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::CH + (ks & 3) * 32;
           umma_ss(tmem + C::T_S + sb * FN, dQ + (off >> 4), k + (off >> 4), ID_S, ks > 0 ? 1u : 0u);
         }
         umma_commit(bar + B_S_FULL + sb);
+        umma_commit(bar + B_K_EMPTY + s);
         // O += P V of the previous tile runs behind this tile's S
         if (j > 0 && !(ok = issue_pv(j - 1))) break;
       }
