@@ -19,10 +19,11 @@
 // in 16 bits and most tiles skip the rescale.  At the end O / l goes to
 // global memory and LSE = (m + log2 l) ln 2.
 //
-// Warp roles (320 threads): warp 0 lane 0 loads (TMA), warp 1 allocates TMEM
-// and its lane 0 issues the MMAs, warps 2-9 run the softmax and the epilogue
-// (two warps per query row block, 64 key columns each).  Every wait is bounded by %globaltimer; a CTA
-// whose wait expires writes NaN into its rows' LSE instead of a result.
+// Warp roles (352 threads): warp 0 lane 0 loads (TMA), warp 1 allocates TMEM
+// and its lane 0 issues O += P V, warps 2-9 run the softmax and the epilogue
+// (two warps per query row block, 64 key columns each), warp 10 lane 0 issues
+// S = Q K^T.  Every wait is bounded by %globaltimer; a CTA whose wait expires
+// writes NaN into its rows' LSE instead of a result.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,7 +42,8 @@ constexpr int FN = 128;                  // keys per KV tile
 constexpr int NUM_SM_WARPS = 8;          // softmax / epilogue warps: two per TMEM lane quarter
 constexpr int SM_COLS = FN / 2;          // key columns of one softmax warp
 constexpr int FIRST_SM_WARP = 2;
-constexpr int NTHREADS = 32 * (FIRST_SM_WARP + NUM_SM_WARPS);
+constexpr int S_ISSUER_WARP = FIRST_SM_WARP + NUM_SM_WARPS;   // issues S = Q K^T
+constexpr int NTHREADS = 32 * (S_ISSUER_WARP + 1);
 constexpr int V_STAGES = 2;              // V ring depth (K has its own ring, FCfg::KST)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t SLEEP_HINT_NS = 20000;
@@ -80,7 +82,7 @@ struct FCfg {
 enum {
   B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = B_K_FULL + 3, B_V_FULL = B_K_EMPTY + 3, B_V_EMPTY = B_V_FULL + V_STAGES,
   B_S_FULL = B_V_EMPTY + V_STAGES,
-  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2, B_PV_DONE, B_DRAIN,
+  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2, B_PV_DONE, B_DRAIN, B_DRAIN2,
   // the two warps of a row block exchange row maxima per tile ([quarter][tile parity])
   // and row sums at the end ([quarter]); two lane-0 arrivals each
   B_RED, B_EPI = B_RED + 8, B_END = B_EPI + 4
@@ -197,6 +199,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     mbar_init(bar + B_P_FULL, NUM_SM_WARPS);
     mbar_init(bar + B_PV_DONE, 1);
     mbar_init(bar + B_DRAIN, 1);
+    mbar_init(bar + B_DRAIN2, 1);
     for (int i = B_RED; i < B_END; ++i) mbar_init(bar + i, 2);
     fence_mbar_init();
   }
@@ -247,48 +250,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       for (int i = jk - 1; i >= 0 && i >= jk - C::KST; --i) wait_bar(ctx, B_K_FULL + i % C::KST, (i / C::KST) & 1);
       for (int i = jv - 1; i >= 0 && i >= jv - V_STAGES; --i) wait_bar(ctx, B_V_FULL + i % V_STAGES, (i / V_STAGES) & 1);
     }
-  } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == S_ISSUER_WARP) {
+    // -------------------------------------------------------- MMA issuers
+    // Two single-thread issuers: warp S_ISSUER_WARP issues S = Q K^T (as soon
+    // as K is in and the S buffer has been read), warp 1 (which owns the TMEM
+    // allocation) issues O += P V (as soon as P is written).  With one thread
+    // issuing both, the next tile's S waited behind this tile's P V group.
     if (lane == 0) {
+      const bool is_s = warp == S_ISSUER_WARP;
       constexpr bool F16 = IsHalf<T>::value;
       constexpr uint32_t ID_S = idesc_f16(FM, FN, false, false, F16);
       constexpr uint32_t ID_PV = idesc_f16(FM, DV, false, true, F16);
       const uint64_t dQ = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);        // K-major
       const uint64_t dK = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);        // K-major, stage 0
       const uint64_t dV = sdesc_sw128(smem_u32(smem + C::OFF_V), C::CH, 1024);     // MN-major, stage 0
-      bool ok = wait_bar(ctx, B_Q_FULL, 0);
-      auto issue_pv = [&](int j) -> bool {
-        if (!wait_bar(ctx, B_P_FULL, j & 1) || !wait_bar(ctx, B_V_FULL + j % V_STAGES, (j / V_STAGES) & 1))
-          return false;
-        tc_fence_after();
-        const uint64_t v = dV + (((j % V_STAGES) * C::VSTAGE) >> 4);
+      bool ok = true;
+      if (is_s) {
+        ok = wait_bar(ctx, B_Q_FULL, 0);
+        for (int j = 0; ok && j < nkv; ++j) {
+          const int s = j % C::KST, sb = j & 1;
+          if (!(ok = wait_bar(ctx, B_K_FULL + s, (j / C::KST) & 1))) break;
+          if (!(ok = wait_bar(ctx, B_S_EMPTY + sb, ((j >> 1) & 1) ^ 1))) break;
+          tc_fence_after();
+          const uint64_t k = dK + ((s * C::KSTAGE) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < FN / 16; ++ks)
-          umma_ts(tmem + C::T_O, tmem + C::T_P + ks * 8, v + ((ks * 2048) >> 4), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(bar + B_PV_DONE);
-        umma_commit(bar + B_V_EMPTY + j % V_STAGES);
-        return true;
-      };
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % C::KST, sb = j & 1;
-        if (!(ok = wait_bar(ctx, B_K_FULL + s, (j / C::KST) & 1))) break;
-        if (!(ok = wait_bar(ctx, B_S_EMPTY + sb, ((j >> 1) & 1) ^ 1))) break;
-        tc_fence_after();
-        const uint64_t k = dK + ((s * C::KSTAGE) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::CH + (ks & 3) * 32;
-          umma_ss(tmem + C::T_S + sb * FN, dQ + (off >> 4), k + (off >> 4), ID_S, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < DQK / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::CH + (ks & 3) * 32;
+            umma_ss(tmem + C::T_S + sb * FN, dQ + (off >> 4), k + (off >> 4), ID_S, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(bar + B_S_FULL + sb);
+          umma_commit(bar + B_K_EMPTY + s);
         }
-        umma_commit(bar + B_S_FULL + sb);
-        umma_commit(bar + B_K_EMPTY + s);
-        // O += P V of the previous tile runs behind this tile's S
-        if (j > 0 && !(ok = issue_pv(j - 1))) break;
+      } else {
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (!(ok = wait_bar(ctx, B_P_FULL, j & 1))) break;
+          if (!(ok = wait_bar(ctx, B_V_FULL + j % V_STAGES, (j / V_STAGES) & 1))) break;
+          tc_fence_after();
+          const uint64_t v = dV + (((j % V_STAGES) * C::VSTAGE) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < FN / 16; ++ks)
+            umma_ts(tmem + C::T_O, tmem + C::T_P + ks * 8, v + ((ks * 2048) >> 4), ID_PV,
+                    (j > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(bar + B_PV_DONE);
+          umma_commit(bar + B_V_EMPTY + j % V_STAGES);
+        }
       }
-      if (ok && nkv > 0) issue_pv(nkv - 1);
-      // no MMA of this CTA may be in flight when TMEM is released
-      umma_commit(bar + B_DRAIN);
-      wait_bar(ctx, B_DRAIN, 0);
+      // no MMA of this issuer may be in flight when TMEM is released
+      umma_commit(bar + (is_s ? B_DRAIN2 : B_DRAIN));
+      wait_bar(ctx, is_s ? B_DRAIN2 : B_DRAIN, 0);
     }
   } else {
     // ----------------------------------------------- softmax and epilogue
