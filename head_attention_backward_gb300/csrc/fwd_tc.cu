@@ -71,18 +71,21 @@ struct FCfg {
   static constexpr uint32_t Q_BYTES = NCK * CH;
   static constexpr uint32_t K_BYTES = NCK * CH;
   static constexpr uint32_t V_BYTES = NCV * CH;
-  // TMEM columns: two S buffers, O, P (bf16/fp16 pairs, the A operand of P V)
+  // TMEM columns: two S buffers, O, two P buffers (bf16/fp16 pairs, the A
+  // operand of P V; tile j uses buffer j & 1)
   static constexpr int T_S = 0;
   static constexpr int T_O = 2 * FN;
   static constexpr int T_P = T_O + 128;
-  static_assert(T_P + FN / 2 <= (int)TMEM_COLS, "TMEM overflow");
+  static_assert(T_P + FN <= (int)TMEM_COLS, "TMEM overflow");
   static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
 
 enum {
   B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = B_K_FULL + 3, B_V_FULL = B_K_EMPTY + 3, B_V_EMPTY = B_V_FULL + V_STAGES,
   B_S_FULL = B_V_EMPTY + V_STAGES,
-  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2, B_PV_DONE, B_DRAIN, B_DRAIN2,
+  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2,
+  B_PV_DONE,   // one per P buffer: P V of tile j done, j & 1
+  B_DRAIN = B_PV_DONE + 2, B_DRAIN2,
   // the two warps of a row block exchange row maxima per tile ([quarter][tile parity])
   // and row sums at the end ([quarter]); two lane-0 arrivals each
   B_RED, B_EPI = B_RED + 8, B_END = B_EPI + 4
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     }
     mbar_init(bar + B_P_FULL, NUM_SM_WARPS);
     mbar_init(bar + B_PV_DONE, 1);
+    mbar_init(bar + B_PV_DONE + 1, 1);
     mbar_init(bar + B_DRAIN, 1);
     mbar_init(bar + B_DRAIN2, 1);
     for (int i = B_RED; i < B_END; ++i) mbar_init(bar + i, 2);
@@ -289,9 +293,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
           const uint64_t v = dV + (((j % V_STAGES) * C::VSTAGE) >> 4);
 #pragma unroll
           for (int ks = 0; ks < FN / 16; ++ks)
-            umma_ts(tmem + C::T_O, tmem + C::T_P + ks * 8, v + ((ks * 2048) >> 4), ID_PV,
+            umma_ts(tmem + C::T_O, tmem + C::T_P + (j & 1) * (FN / 2) + ks * 8, v + ((ks * 2048) >> 4), ID_PV,
                     (j > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(bar + B_PV_DONE);
+          umma_commit(bar + B_PV_DONE + (j & 1));
           umma_commit(bar + B_V_EMPTY + j % V_STAGES);
         }
       }
@@ -387,12 +391,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         pk[c >> 1] = pack2(p.x, p.y, (T*)nullptr);
       }
       l = l * alpha + (((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y)));
-      // O and the P buffer are free once the previous tile's O += P V is done
-      if (j > 0) {
-        if (!(ok = wait_bar_warp(ctx, B_PV_DONE, (j - 1) & 1))) break;
+      // P buffer j & 1 is free once P V of tile j - 2 is done; O may be
+      // rescaled only once P V of tile j - 1 is (each buffer's barrier completes
+      // once per two tiles, and tile j + 2 cannot finish before this P is written)
+      if (j >= 2) {
+        if (!(ok = wait_bar_warp(ctx, B_PV_DONE + (j & 1), ((j >> 1) - 1) & 1))) break;
         tc_fence_after();
       }
-      if (__any_sync(0xffffffffu, rescale)) {
+      const bool any_rescale = __any_sync(0xffffffffu, rescale);
+      if (any_rescale) {
+        if (!(ok = wait_bar_warp(ctx, B_PV_DONE + ((j - 1) & 1), ((j - 1) >> 1) & 1))) break;
+        tc_fence_after();
+      }
+      if (any_rescale) {
 #pragma unroll 1
         for (int c = 0; c < OC / 32; ++c) {
           uint32_t o[32];
@@ -411,7 +422,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       }
 #pragma unroll
       for (int c = 0; c < SM_COLS / 32; ++c)
-        tmem_st16(lane_addr + C::T_P + half * (SM_COLS / 2) + c * 16,
+        tmem_st16(lane_addr + C::T_P + (j & 1) * (FN / 2) + half * (SM_COLS / 2) + c * 16,
                   *reinterpret_cast<const uint32_t(*)[16]>(pk + c * 16));
       tmem_wait_st();
       tc_fence_before();
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     // the columns) and the LSE
     ok = __all_sync(0xffffffffu, ok);
     if (ok && nkv > 0) {
-      ok = wait_bar_warp(ctx, B_PV_DONE, (nkv - 1) & 1);
+      ok = wait_bar_warp(ctx, B_PV_DONE + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1);
       tc_fence_after();
     }
     float lo_other = 0.f;
