@@ -64,7 +64,7 @@ struct FCfg {
   static constexpr int OFF_K = OFF_Q + NCK * CH;
   static constexpr int OFF_V = OFF_K + KST * KSTAGE;
   static constexpr int OFF_BAR = OFF_V + V_STAGES * VSTAGE;
-  static constexpr int NBAR = 32;
+  static constexpr int NBAR = 40;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RED = OFF_MISC + 64;            // [3 slots][2 halves][128 rows] fp32
   static constexpr int SMEM_BYTES = OFF_RED + 3 * 2 * 128 * 4 + 1024;   // + alignment slack
@@ -83,8 +83,12 @@ struct FCfg {
 enum {
   B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = B_K_FULL + 3, B_V_FULL = B_K_EMPTY + 3, B_V_EMPTY = B_V_FULL + V_STAGES,
   B_S_FULL = B_V_EMPTY + V_STAGES,
-  B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2,
-  B_PV_DONE,   // one per P buffer: P V of tile j done, j & 1
+  B_S_EMPTY = B_S_FULL + 2,
+  // one per P buffer (tile j: j & 1).  With a single P_FULL barrier a warp
+  // that has run a tile ahead would add its arrival for tile j to tile j - 1's
+  // phase and release P V of j - 1 before a slower warp had written its P.
+  B_P_FULL = B_S_EMPTY + 2,
+  B_PV_DONE = B_P_FULL + 2,   // P V of tile j done, j & 1
   B_DRAIN = B_PV_DONE + 2, B_DRAIN2,
   // the two warps of a row block exchange row maxima per tile ([quarter][tile parity])
   // and row sums at the end ([quarter]); two lane-0 arrivals each
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       mbar_init(bar + B_S_EMPTY + s, NUM_SM_WARPS);
     }
     mbar_init(bar + B_P_FULL, NUM_SM_WARPS);
+    mbar_init(bar + B_P_FULL + 1, NUM_SM_WARPS);
     mbar_init(bar + B_PV_DONE, 1);
     mbar_init(bar + B_PV_DONE + 1, 1);
     mbar_init(bar + B_DRAIN, 1);
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         }
       } else {
         for (int j = 0; ok && j < nkv; ++j) {
-          if (!(ok = wait_bar(ctx, B_P_FULL, j & 1))) break;
+          if (!(ok = wait_bar(ctx, B_P_FULL + (j & 1), (j >> 1) & 1))) break;
           if (!(ok = wait_bar(ctx, B_V_FULL + j % V_STAGES, (j / V_STAGES) & 1))) break;
           tc_fence_after();
           const uint64_t v = dV + (((j % V_STAGES) * C::VSTAGE) >> 4);
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar + B_P_FULL);
+      if (lane == 0) mbar_arrive(bar + B_P_FULL + (j & 1));
     }
     // epilogue: the row's sum over both halves, O / l (each warp its half of
     // the columns) and the LSE
