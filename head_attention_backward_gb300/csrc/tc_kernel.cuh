@@ -394,6 +394,26 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         int h, qt;
         step_coords(P, I, s, h, qt);
         if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
+        auto load_tiles = [&]() {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar + B_Q_FULL + st, C::QDO_BYTES);
+            int qrow = I.sg.q0 + qt * BM;
+            if (!ATTN_INDEX_OK(P, qrow >= 0 && qrow < rows_q(P) && h >= 0 && h < P.hq, 4)) qrow = 0;
+            for (int c = 0; c < C::NCK; ++c)
+              tma_load_3d(smem + C::OFF_Q + (st * C::NCK + c) * C::QCH, &maps.q, bar + B_Q_FULL + st, c * 64, h,
+                          qrow);
+            for (int c = 0; c < C::NCV; ++c)
+              tma_load_3d(smem + C::OFF_DO + (st * C::NCV + c) * C::QCH, &maps.dout, bar + B_Q_FULL + st, c * 64, h,
+                          qrow);
+          }
+        };
+        // The Q / dO tiles (TMA) go first: the row statistics' per-lane copies
+        // take ~1,300 cycles, which issuing the tiles after them puts on the
+        // cycle a Q/dO stage goes round.  Measured faster in every mode and
+        // head dim except the ordered fold at d_qk <= 128, whose cross-CTA
+        // hand-offs got slower with the earlier tiles; it keeps the old order.
+        constexpr bool TILES_FIRST = !FOLD || DQK > 128;
+        if (TILES_FIRST) load_tiles();
         // -LSE*log2(e) and D of the tile's 64 query rows, copied asynchronously;
         // rows past the segment end read as zeros (their columns are masked)
         for (int c = lane; c < BM; c += 32) {
@@ -406,16 +426,7 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
           cp_async_4(sD + st * BM + c, P.dvec + li, valid && li_ok ? 4u : 0u);
         }
         cp_async_arrive_noinc(bar + B_Q_FULL + st);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar + B_Q_FULL + st, C::QDO_BYTES);
-          int qrow = I.sg.q0 + qt * BM;
-          if (!ATTN_INDEX_OK(P, qrow >= 0 && qrow < rows_q(P) && h >= 0 && h < P.hq, 4)) qrow = 0;
-          for (int c = 0; c < C::NCK; ++c)
-            tma_load_3d(smem + C::OFF_Q + (st * C::NCK + c) * C::QCH, &maps.q, bar + B_Q_FULL + st, c * 64, h, qrow);
-          for (int c = 0; c < C::NCV; ++c)
-            tma_load_3d(smem + C::OFF_DO + (st * C::NCV + c) * C::QCH, &maps.dout, bar + B_Q_FULL + st, c * 64, h,
-                        qrow);
-        }
+        if (!TILES_FIRST) load_tiles();
       }
       if (!ok) break;
       g += nrun;
