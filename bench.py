@@ -75,8 +75,8 @@ def peaks():
 KERNEL_SOURCES = ("tc_kernel.cuh", "tc_kernel.cu", "common.cuh", "sm100_ptx.cuh")
 KERNEL_TRAFFIC = {
     "gqa_B2_Hq32_Hkv8_S4096_d128_causal_det:ordered": {
-        "bytes": 621.5e6 + 278.6e6,
-        "src": "b731cec2bb213e57",
+        "bytes": 623.6e6 + 281.4e6,
+        "src": "25889a474514f233",
         "profile": "profiles/bwd_tc_kernel_gqa_B2_S4096_det_traffic.md"},
 }
 
@@ -268,17 +268,29 @@ def run_ours(args, wl):
     kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
               cu_seqlens_k=cuk_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
     o, lse = B.attn_forward(d["q"], d["k"], d["v"], **kw)
-    # the forward that made O and LSE, timed for the record (not part of a step)
+    # the forward that made O and LSE, timed for the record (not part of a step):
+    # the attn_fwd C-ABI call on prebuilt parameters, L2 flushed before each call
+    # (the flush also keeps the GPU busy while the host enqueues the launch)
+    fo, flse = torch.empty_like(o), torch.empty_like(lse)
+    fo.copy_(o)
+    flse.copy_(lse)
+    pf = B.fwd_params(d["q"], d["k"], d["v"], fo, flse, **kw)
+    fflush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device=dev)
+    fstream = torch.cuda.current_stream(dev).cuda_stream
     fwd_ms = []
     for i in range(13):
+        fflush.fill_(1.0)
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record()
-        B.attn_forward(d["q"], d["k"], d["v"], **kw)
+        fst = B.attn_fwd(pf, fstream)
         f1.record()
         f1.synchronize()
+        if fst != 0:
+            raise RuntimeError(f"attn_fwd failed with status {fst}")
         if i >= 3:
             fwd_ms.append(f0.elapsed_time(f1))
     fwd_ms = sorted(fwd_ms)[len(fwd_ms) // 2]
+    del fflush
     outs = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]))
     p = B.bwd_params(d["q"], d["k"], d["v"], o, d["do"], lse, *outs, deterministic=dq_mode(wl), **kw)
     nbytes = B.workspace_bytes(p)
@@ -387,7 +399,7 @@ def run_ours(args, wl):
         "gpu_launches": (4 if wl.group_mode else 3) * args.steps,
         "forward": {"kernel": "fwd_tc_kernel" if wl.dtype != torch.float32 else "fwd_kernel",
                     "ms": fwd_ms, "TFLOP/s": fl * (wl.d_qk + wl.d_v) / (3 * wl.d_qk + 2 * wl.d_v) / fwd_ms / 1e9,
-                    "note": "median of 10 attn_fwd calls on the same inputs; not part of the timed step"},
+                    "note": "median of 10 attn_fwd C-ABI calls on prebuilt parameters, L2 flushed before each; not part of the timed step"},
         "split_slices": split_leg,
         "clocks": clk,
         "workspace_bytes": nbytes,
