@@ -195,3 +195,55 @@ def test_forward_bitwise_repeatable_and_matches_oracle_full_size(B):
         rep.update(tensor="lse", batch=b, head=h)
         reps.append(rep)
     assert_all_ok(reps, "forward full size")
+
+
+@pytest.mark.parametrize("name", ["thd_packed", "window_192"])
+def test_forward_bitwise_repeatable_other_workloads(B, name):
+    """The forward on the packed THD and d_qk = 192 window workloads: five
+    calls give the same bits."""
+    wl = getattr(W, name)()
+    d = {k: v.cuda() for k, v in wl.inputs().items()}
+    cu = wl.cu_seqlens()
+    cu = None if cu is None else cu.cuda()
+    kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu, cu_seqlens_k=cu,
+              max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+    o0, l0 = B.attn_forward(d["q"], d["k"], d["v"], **kw)
+    for i in range(5):
+        o, lse = B.attn_forward(d["q"], d["k"], d["v"], **kw)
+        assert torch.equal(o, o0) and torch.equal(lse, l0), f"{name}: call {i + 1} differs from the first"
+
+
+def test_window_dqk192_ordered_fold_equals_split_bits(B):
+    wl = W.window_192(deterministic=True)
+    _, _, a = _run(B, wl, 1)
+    _, _, b = _run(B, wl, 2)
+    for name, x, y in zip(("dq", "dk", "dv"), a, b):
+        assert torch.equal(x, y), name
+
+
+def test_bias_dropout_full_size_bitwise_repeatable(B):
+    """The bias / dbias / dropout instantiation at a larger size (B1 Hq16 Hkv4
+    S2048 d128 causal, a [1, Hq, S, S] bias, p = 0.1): five ordered-fold runs
+    give the same bits, equal to the split slices' (values are checked against
+    the oracle on small cases in test_gpu_extras.py)."""
+    wl = W.Workload("bias_drop_B1_Hq16_S2048", torch.bfloat16, 1, 16, 4, 2048, 2048, 128, 128,
+                    W.MASK_CAUSAL_TOP_LEFT, seed=31)
+    d = {k: v.cuda() for k, v in wl.inputs().items()}
+    g = torch.Generator().manual_seed(32)
+    bias = torch.randn(1, wl.hq, wl.sq, wl.sk, generator=g).to(torch.bfloat16).cuda()
+    seed = torch.tensor([1234], dtype=torch.int64, device="cuda")
+    offset = torch.tensor([5], dtype=torch.int64, device="cuda")
+    ex = dict(scale=wl.scale, mask=wl.mask, bias=bias, dropout_p=0.1, philox_seed=seed, philox_offset=offset)
+    o, lse = B.attn_forward(d["q"], d["k"], d["v"], **ex)
+    runs = {}
+    for mode in (B.DET_ORDERED, B.DET_SPLIT):
+        for i in range(5 if mode == B.DET_ORDERED else 1):
+            got = B.attn_backward(d["q"], d["k"], d["v"], o, d["do"], lse, deterministic=mode, return_dbias=True, **ex)
+            torch.cuda.synchronize()
+            if mode not in runs:
+                runs[mode] = got
+            else:
+                for name, a, b in zip(("dq", "dk", "dv", "dbias"), runs[mode], got):
+                    assert torch.equal(a, b), f"run {i}: {name} differs"
+    for name, a, b in zip(("dq", "dk", "dv", "dbias"), runs[B.DET_ORDERED], runs[B.DET_SPLIT]):
+        assert torch.equal(a, b), f"ordered fold and split slices differ in {name}"
