@@ -116,6 +116,16 @@ def test_thd_splits_per_segment(B, segs, heads, det):
     assert_all_ok(reps, f"segments {segs}")
 
 
+@pytest.mark.parametrize("det", **DET_MODES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+def test_thd_head_dim_256_per_segment(B, dtype, det):
+    """Packed THD at head dim 256: each KV tile's two column-half passes are
+    work items of their own, and in the ordered fold each half has its own
+    turn counters; every segment is compared with the oracle."""
+    wl = W.thd("thd_d256", [300, 1, 129, 200, 64], hq=4, hkv=2, d_qk=256, d_v=256, dtype=dtype, seed=47)
+    assert_all_ok(run_backward_vs_oracle(B, wl, det), "thd d256")
+
+
 # Cross-attention varlen: every segment has its own query and key length,
 # including segments with no keys (their dQ is zero) and no queries (their
 # dK, dV are zero), lengths off the 128-row tile and segments longer than one
