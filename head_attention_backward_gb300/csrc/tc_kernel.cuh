@@ -119,7 +119,7 @@ struct Cfg {
   static constexpr int OFF_L = OFF_DS + 2 * DS_BYTES;      // [ST][BM] -LSE*log2(e)
   static constexpr int OFF_D = OFF_L + ST * BM * 4;        // [ST][BM] D
   static constexpr int OFF_BAR = OFF_D + ST * BM * 4;
-  static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NR;
+  static constexpr int NBAR = 16 + 2 * ST + 2 * NI + 2 * NR + (NPASS > 1 ? 2 : 0);
   static constexpr int OFF_RING = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MISC = OFF_RING + NI * 16;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + NR * 8 + 1024;  // + alignment slack
@@ -292,6 +292,13 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
   // ordered fold: a partial's adds issued (drain -> turn thread) / release
   // slot free again (turn thread -> drain)
   const int B_REDS_DONE = B_IT_EMPTY + NI, B_REDS_FREE = B_REDS_DONE + NR;
+  // Head dim 256 (one Q/dO stage): in pass p the column half 1 - p of Q and
+  // dO feeds only S^T and dP^T, so it is loaded and released on a barrier pair
+  // of its own (QA: freed by issuer A once S^T / dP^T are done, reloaded for
+  // the next step during the P/dS work); the pass's own half and the row
+  // statistics keep the Q_FULL / Q_EMPTY pair (freed after dV / dK).
+  constexpr bool SPLITQ = C::NPASS > 1;
+  const int B_QA_FULL = B_REDS_FREE + NR, B_QA_EMPTY = B_QA_FULL + 1;
   constexpr int NTHREADS = kernel_threads<DQM>();
 
   // zero the k padding chunks read by the dQ^T MMA of padded head dims
@@ -326,6 +333,10 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(bar + B_Q_FULL + s, 32 + 1);   // 32 cp.async arrivals + the TMA expect_tx arrival
       mbar_init(bar + B_Q_EMPTY + s, 1);
+    }
+    if (SPLITQ) {
+      mbar_init(bar + B_QA_FULL, 1);
+      mbar_init(bar + B_QA_EMPTY, 1);
     }
     for (int s = 0; s < NI; ++s) {
       mbar_init(bar + B_IT_FULL + s, 1);
@@ -393,18 +404,35 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
         const uint32_t gs = g + s, st = gs % C::ST;
         int h, qt;
         step_coords(P, I, s, h, qt);
+        int qrow = I.sg.q0 + qt * BM;
+        if (!ATTN_INDEX_OK(P, qrow >= 0 && qrow < rows_q(P) && h >= 0 && h < P.hq, 4)) qrow = 0;
+        // chunks [c0, c1) of the step's Q and dO tiles onto barrier `b`
+        auto load_chunks = [&](int c0, int c1, int b) {
+          mbar_arrive_expect_tx(bar + b, (uint32_t)(2 * (c1 - c0)) * C::QCH);
+          for (int c = c0; c < c1; ++c) {
+            tma_load_3d(smem + C::OFF_Q + (st * C::NCK + c) * C::QCH, &maps.q, bar + b, c * 64, h, qrow);
+            tma_load_3d(smem + C::OFF_DO + (st * C::NCV + c) * C::QCH, &maps.dout, bar + b, c * 64, h, qrow);
+          }
+        };
+        const int pass = C::NPASS == 1 ? 0 : item.w;
+        if constexpr (SPLITQ) {   // the other column half, as soon as the last S^T / dP^T are done with it
+          if (!(ok = wait_bar(ctx, B_QA_EMPTY, (gs & 1) ^ 1, 7))) break;
+          if (lane == 0) load_chunks((1 - pass) * C::NCA, (2 - pass) * C::NCA, B_QA_FULL);
+        }
         if (!(ok = wait_bar(ctx, B_Q_EMPTY + st, ((gs / C::ST) & 1) ^ 1, 3))) break;
         auto load_tiles = [&]() {
           if (lane == 0) {
-            mbar_arrive_expect_tx(bar + B_Q_FULL + st, C::QDO_BYTES);
-            int qrow = I.sg.q0 + qt * BM;
-            if (!ATTN_INDEX_OK(P, qrow >= 0 && qrow < rows_q(P) && h >= 0 && h < P.hq, 4)) qrow = 0;
-            for (int c = 0; c < C::NCK; ++c)
-              tma_load_3d(smem + C::OFF_Q + (st * C::NCK + c) * C::QCH, &maps.q, bar + B_Q_FULL + st, c * 64, h,
-                          qrow);
-            for (int c = 0; c < C::NCV; ++c)
-              tma_load_3d(smem + C::OFF_DO + (st * C::NCV + c) * C::QCH, &maps.dout, bar + B_Q_FULL + st, c * 64, h,
-                          qrow);
+            if constexpr (SPLITQ) {
+              load_chunks(pass * C::NCA, (pass + 1) * C::NCA, B_Q_FULL + st);
+            } else {
+              mbar_arrive_expect_tx(bar + B_Q_FULL + st, C::QDO_BYTES);
+              for (int c = 0; c < C::NCK; ++c)
+                tma_load_3d(smem + C::OFF_Q + (st * C::NCK + c) * C::QCH, &maps.q, bar + B_Q_FULL + st, c * 64, h,
+                            qrow);
+              for (int c = 0; c < C::NCV; ++c)
+                tma_load_3d(smem + C::OFF_DO + (st * C::NCV + c) * C::QCH, &maps.dout, bar + B_Q_FULL + st, c * 64,
+                            h, qrow);
+            }
           }
         };
         // The Q / dO tiles (TMA) go first: the row statistics' per-lane copies
@@ -466,8 +494,38 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
       //
       // Inputs of S^T / dP^T for global step gs are ready and their TMEM free.
       auto wait_sdp = [&](uint32_t gs) -> bool {
-        return wait_bar(ctx, B_Q_FULL + gs % C::ST, (gs / C::ST) & 1, 10) &&
+        return wait_bar(ctx, SPLITQ ? B_QA_FULL : B_Q_FULL + gs % C::ST, (gs / C::ST) & 1, 10) &&
                wait_bar(ctx, B_SDP_EMPTY, (gs & 1) ^ 1, 11);
+      };
+      // Head dim 256, pass `pass`: the K steps over the other column half of
+      // Q / dO (already in) first, then, once the pass's own half is in, the
+      // rest; the commit after the group frees the other half
+      auto mma_sdp_split = [&](uint32_t gs, int pass) -> bool {
+        const uint32_t st = gs % C::ST;
+        const uint64_t q = dQ_k + ((st * C::NCK * C::QCH) >> 4), d = ddO_k + ((st * C::NCV * C::QCH) >> 4);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (hf == 1) {
+            if (!wait_bar(ctx, B_Q_FULL + st, (gs / C::ST) & 1, 8)) return false;
+            tc_fence_after();
+          }
+          const uint32_t cbase = (uint32_t)((hf == 0 ? 1 - pass : pass) * C::NCA);
+          const uint64_t ka = dK_k + ((cbase * C::KCH) >> 4), va = dV_k + ((cbase * C::KCH) >> 4);
+          const uint64_t qb = q + ((cbase * C::QCH) >> 4), db = d + ((cbase * C::QCH) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < C::NCA * 4; ++kk) {
+            const uint32_t off_a = (kk >> 2) * C::KCH + (kk & 3) * 32, off_b = (kk >> 2) * C::QCH + (kk & 3) * 32;
+            umma_ss(tmem + C::T_S, ka + (off_a >> 4), qb + (off_b >> 4), ID_SDP, (hf | kk) > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < C::NCA * 4; ++kk) {
+            const uint32_t off_a = (kk >> 2) * C::KCH + (kk & 3) * 32, off_b = (kk >> 2) * C::QCH + (kk & 3) * 32;
+            umma_ss(tmem + C::T_DP, va + (off_a >> 4), db + (off_b >> 4), ID_SDP, (hf | kk) > 0);
+          }
+        }
+        umma_commit(bar + B_SDP_FULL);
+        umma_commit(bar + B_QA_EMPTY);
+        return true;
       };
       // S^T = K Q^T and dP^T = V dO^T of step gs.
       auto mma_sdp = [&](uint32_t gs) -> bool {
@@ -602,6 +660,8 @@ __global__ void __launch_bounds__(kernel_threads<DQM>(), 1) bwd_tc_kernel(const 
             tc_fence_after();
             if constexpr (C::SEQDQ) {
               if (!(ok = mma_sdp(gs))) break;
+            } else if constexpr (SPLITQ) {
+              if (!(ok = mma_sdp_split(gs, pass))) break;
             } else {
               mma_sdp(gs);
             }
