@@ -372,6 +372,35 @@ def test_deterministic_bitwise_repeatable(B, wl):
         assert torch.equal(a, b), "ordered fold differs from split slices"
 
 
+@pytest.mark.parametrize("wl", [DET_CASES[0], DET_CASES[2], DET_CASES[3], DET_CASES[5]], ids=lambda w: w.name)
+def test_ordered_fold_ignores_workspace_contents(B, wl):
+    """The ordered fold initialises what it reads: its dQ slice, the turn
+    counters and the tables (det_br_short_k has query tiles no KV tile reaches,
+    whose dQ rows are zero).  A workspace filled with NaN bytes gives the same
+    bits as a zeroed one."""
+    x = {k: v.cuda() for k, v in wl.inputs().items()}
+    cu = wl.cu_seqlens()
+    cu_d = None if cu is None else cu.cuda()
+    kw = dict(scale=wl.scale, mask=wl.mask, left=wl.left, right=wl.right, cu_seqlens_q=cu_d,
+              cu_seqlens_k=cu_d, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk)
+    o, lse = B.attn_forward(x["q"], x["k"], x["v"], **kw)
+    res = []
+    for fill in (0, 0xFF):
+        outs = (torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]))
+        p = B.bwd_params(x["q"], x["k"], x["v"], o, x["do"], lse, *outs, deterministic=B.DET_ORDERED, **kw)
+        n = B.workspace_bytes(p)
+        ws = B.alloc_workspace(n, x["q"].device)
+        ws.fill_(fill)
+        s = torch.cuda.current_stream().cuda_stream
+        assert B.attn_bwd(p, ws.data_ptr(), n, s) == 0
+        st, dev = B.attn_bwd_read_status(ws.data_ptr(), s)
+        assert st == 0 and dev == 0
+        res.append(outs)
+    for a, b in zip(*res):
+        assert not torch.isnan(b.float()).any()
+        assert torch.equal(a, b)
+
+
 def test_bad_cu_seqlens_reported_by_device(B):
     wl = W.thd("bad", [100, 80, 76], hq=4, hkv=2)
     x = {k: v.cuda() for k, v in wl.inputs().items()}
