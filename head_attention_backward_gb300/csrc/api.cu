@@ -304,8 +304,8 @@ int launch_fwd_tc(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st)
 // earlier parts left).
 void launch_schedule_preprocess(const Problem& P, cudaStream_t st, bool keep_status);
 
-static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t s,
-               cudaEvent_t* ev /* 4 events or null */, bool keep_status = false) {
+// The validated problem the kernels of one call (or of one part of a call) run.
+static int prepare(const attn_bwd_params* p, void* ws, size_t ws_bytes, Problem* P) {
   int st = validate_bwd(p);
   if (st != ATTN_OK) return st;
   attn_bwd_params e;
@@ -315,16 +315,29 @@ static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t
   const WsLayout L = ws_layout(e);
   if (ws_bytes < L.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   if (log_enabled()) log_config(e, L);
-  const Problem P = make_problem(e, sx, ws, p->nhead_q);
+  *P = make_problem(e, sx, ws, p->nhead_q);
+  return ATTN_OK;
+}
+
+// The main kernel: tensor cores for 16-bit inputs, CUDA cores for fp32.  It
+// leaves dK and dV final; dQ is final after the reduce/convert kernel.
+static int launch_main(const Problem& P, cudaStream_t s) {
+  if (P.dtype == ATTN_FP32) {
+    launch_bwd_simt(P, s);
+    return ATTN_OK;
+  }
+  return launch_bwd_tc(P, s);
+}
+
+static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t s,
+               cudaEvent_t* ev /* 4 events or null */, bool keep_status = false) {
+  Problem P;
+  int st = prepare(p, ws, ws_bytes, &P);
+  if (st != ATTN_OK) return st;
   if (ev) cudaEventRecord(ev[0], s);
   launch_schedule_preprocess(P, s, keep_status);
   if (ev) cudaEventRecord(ev[1], s);
-  if (P.dtype == ATTN_FP32) {
-    launch_bwd_simt(P, s);
-  } else {
-    st = launch_bwd_tc(P, s);
-    if (st != ATTN_OK) return st;
-  }
+  if ((st = launch_main(P, s)) != ATTN_OK) return st;
   if (ev) cudaEventRecord(ev[2], s);
   launch_reduce_convert(P, s);
   if (ev) cudaEventRecord(ev[3], s);
@@ -408,38 +421,45 @@ static int run_host(const attn_bwd_params* p, const attn_host_tensors* h, void* 
   const void* hsrc[5] = {h->q, h->k, h->v, h->o, h->dout};
   void* hdst[3] = {h->dq, h->dk, h->dv};
   const void* dptr[8] = {p->q, p->k, p->v, p->o, p->dout, p->dq, p->dk, p->dv};
-  cudaEvent_t ev_in[64], ev_c[64], ev_out;
+  // per chunk: O, dO and LSE in (the preprocess reads only those), all inputs
+  // in, main kernel done (dK, dV final), reduce/convert done (dQ final)
+  enum { E_PRE, E_IN, E_MAIN, E_CONV, E_N };
+  cudaEvent_t ev[64][E_N], ev_out;
   int made = 0;
   for (; made < nchunks; ++made) {
-    if (cudaEventCreateWithFlags(&ev_in[made], cudaEventDisableTiming) != cudaSuccess) break;
-    if (cudaEventCreateWithFlags(&ev_c[made], cudaEventDisableTiming) != cudaSuccess) {
-      cudaEventDestroy(ev_in[made]);
+    int k = 0;
+    while (k < E_N && cudaEventCreateWithFlags(&ev[made][k], cudaEventDisableTiming) == cudaSuccess) ++k;
+    if (k < E_N) {
+      while (k > 0) cudaEventDestroy(ev[made][--k]);
       break;
     }
   }
   const bool have_out = made == nchunks && cudaEventCreateWithFlags(&ev_out, cudaEventDisableTiming) == cudaSuccess;
   bool ok = have_out;
   // the caller's earlier work on `s` comes before the first copy
-  if (ok) ok = cudaEventRecord(ev_c[0], s) == cudaSuccess && cudaStreamWaitEvent(in, ev_c[0], 0) == cudaSuccess &&
-               cudaStreamWaitEvent(out, ev_c[0], 0) == cudaSuccess;
+  if (ok) ok = cudaEventRecord(ev[0][E_CONV], s) == cudaSuccess && cudaStreamWaitEvent(in, ev[0][E_CONV], 0) == cudaSuccess &&
+               cudaStreamWaitEvent(out, ev[0][E_CONV], 0) == cudaSuccess;
   for (int c = 0; ok && c < nchunks; ++c) {
     const int bg = c / nhg, hg = c % nhg;
     const int b0 = (int)((long long)nb * bg / nbg), b1 = (int)((long long)nb * (bg + 1) / nbg);
     const int k0 = (int)((long long)p->nhead_kv * hg / nhg), k1 = (int)((long long)p->nhead_kv * (hg + 1) / nhg);
     const int q0 = k0 * G, q1 = k1 * G;
     auto heads = [&](int i, int& x0, int& x1) { x0 = kv_side[i] ? k0 : q0; x1 = kv_side[i] ? k1 : q1; };
-    for (int i = 0; ok && i < 5; ++i) {
+    auto copy_in = [&](int i) {
       int x0, x1;
       heads(i, x0, x1);
-      ok = copy_part(ht[i], const_cast<void*>(dptr[i]), hsrc[i], b0, b1, x0, x1, cudaMemcpyHostToDevice, in);
-    }
-    // LSE rows of the chunk: [b0, b1) x [q0, q1) x rows, one block (either the
-    // heads are all of them or the chunk has one batch entry)
+      return copy_part(ht[i], const_cast<void*>(dptr[i]), hsrc[i], b0, b1, x0, x1, cudaMemcpyHostToDevice, in);
+    };
+    // O, dO, then the LSE rows of the chunk: [b0, b1) x [q0, q1) x rows, one
+    // block (either the heads are all of them or the chunk has one batch entry)
+    ok = copy_in(3) && copy_in(4);
     const size_t lse_off = ((size_t)b0 * p->nhead_q + q0) * rq;
     const size_t lse_n = (size_t)(b1 - b0) * (q1 - q0) * rq;
     ok = ok && cudaMemcpyAsync(const_cast<float*>(p->lse) + lse_off, h->lse + lse_off, lse_n * sizeof(float),
                                cudaMemcpyHostToDevice, in) == cudaSuccess;
-    ok = ok && cudaEventRecord(ev_in[c], in) == cudaSuccess && cudaStreamWaitEvent(s, ev_in[c], 0) == cudaSuccess;
+    ok = ok && cudaEventRecord(ev[c][E_PRE], in) == cudaSuccess;
+    // then Q, K, V, which only the main kernel reads
+    ok = ok && copy_in(0) && copy_in(1) && copy_in(2) && cudaEventRecord(ev[c][E_IN], in) == cudaSuccess;
     if (!ok) break;
     attn_bwd_params part = *p;
     if (!group) part.batch = b1 - b0;
@@ -461,21 +481,30 @@ static int run_host(const attn_bwd_params* p, const attn_host_tensors* h, void* 
     part.q = views[0]; part.k = views[1]; part.v = views[2]; part.o = views[3]; part.dout = views[4];
     part.dq = views[5]; part.dk = views[6]; part.dv = views[7];
     part.lse = p->lse + lse_off;
-    if ((st = run(&part, ws, ws_bytes, s, nullptr, c > 0)) != ATTN_OK) break;
-    ok = cudaEventRecord(ev_c[c], s) == cudaSuccess && cudaStreamWaitEvent(out, ev_c[c], 0) == cudaSuccess;
-    for (int i = 0; ok && i < 3; ++i) {
+    Problem P;
+    if ((st = prepare(&part, ws, ws_bytes, &P)) != ATTN_OK) break;
+    // the preprocess overlaps the copies of Q, K and V
+    if (!(ok = cudaStreamWaitEvent(s, ev[c][E_PRE], 0) == cudaSuccess)) break;
+    launch_schedule_preprocess(P, s, c > 0);
+    if (!(ok = cudaStreamWaitEvent(s, ev[c][E_IN], 0) == cudaSuccess)) break;
+    if ((st = launch_main(P, s)) != ATTN_OK) break;
+    if (!(ok = cudaEventRecord(ev[c][E_MAIN], s) == cudaSuccess)) break;
+    launch_reduce_convert(P, s);
+    if (!(ok = cudaEventRecord(ev[c][E_CONV], s) == cudaSuccess && cudaGetLastError() == cudaSuccess)) break;
+    auto copy_out = [&](int i) {
       int x0, x1;
       heads(5 + i, x0, x1);
-      ok = copy_part(ht[5 + i], hdst[i], dptr[5 + i], b0, b1, x0, x1, cudaMemcpyDeviceToHost, out);
-    }
+      return copy_part(ht[5 + i], hdst[i], dptr[5 + i], b0, b1, x0, x1, cudaMemcpyDeviceToHost, out);
+    };
+    // dK and dV come down while dQ is converted
+    ok = cudaStreamWaitEvent(out, ev[c][E_MAIN], 0) == cudaSuccess && copy_out(1) && copy_out(2) &&
+         cudaStreamWaitEvent(out, ev[c][E_CONV], 0) == cudaSuccess && copy_out(0);
   }
   // `s` completes only after the last gradients are back on the host
   if (ok && st == ATTN_OK)
     ok = cudaEventRecord(ev_out, out) == cudaSuccess && cudaStreamWaitEvent(s, ev_out, 0) == cudaSuccess;
-  for (int i = 0; i < made; ++i) {
-    cudaEventDestroy(ev_in[i]);
-    cudaEventDestroy(ev_c[i]);
-  }
+  for (int i = 0; i < made; ++i)
+    for (int k = 0; k < E_N; ++k) cudaEventDestroy(ev[i][k]);
   if (have_out) cudaEventDestroy(ev_out);
   if (st != ATTN_OK) return st;
   return ok ? ATTN_OK : ATTN_ERR_CUDA;

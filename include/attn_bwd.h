@@ -320,8 +320,11 @@ typedef struct {
  * their query heads, whose head slices travel as 2-D copies (one line per
  * row; on a GB300 these run far below the plain copies' ~200 GB/s, so
  * chunks <= batch is the fast choice).  Chunk c's inputs are copied on
- * `copy_in`, its backward runs on `stream`, its gradients are copied on
- * `copy_out`, so one chunk's copies overlap another chunk's compute.  The three streams must be distinct; the copies
+ * `copy_in` (O, dO and LSE first, so that its preprocess overlaps the copies
+ * of Q, K and V), its backward runs on `stream`, its gradients are copied on
+ * `copy_out` (dK and dV once the main kernel is done, during the dQ
+ * conversion, then dQ), so one chunk's copies overlap another chunk's
+ * compute.  The three streams must be distinct; the copies
  * start after the work already queued on `stream`, and `stream` completes
  * only once the last gradients are in host memory (synchronise it before
  * reading them).  Each chunk runs the same kernels in the same order as
