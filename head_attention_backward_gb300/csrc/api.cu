@@ -64,14 +64,15 @@ static bool resolve3(const TensorDesc& t, bool group, int batch, bool vec16, Str
 // Resolves the n tensors' strides into out[] and returns 0 (rows layout),
 // 1 (heads layout: fold the batch into the heads) or -1 (rejected).  A
 // tensor with one row per batch entry (or one head) never uses its row (or
-// head) stride, so the batch stride stands in for it.
+// head) stride, so the batch stride stands in for it; one with no rows uses
+// none of its strides and constrains neither layout.
 static int fold_strides(const TensorDesc* t, int n, bool group, int batch, bool vec16, Strides* out) {
   Stride3 x[8];
   bool rows = true, heads = true;
   for (int i = 0; i < n; ++i) {
     if (!resolve3(t[i], group, batch, vec16, &x[i])) return -1;
-    rows &= t[i].seqlen == 1 || x[i].b == (long long)t[i].seqlen * x[i].r;
-    heads &= t[i].heads == 1 || x[i].b == (long long)t[i].heads * x[i].h;
+    rows &= t[i].seqlen <= 1 || x[i].b == (long long)t[i].seqlen * x[i].r;
+    heads &= t[i].seqlen == 0 || t[i].heads == 1 || x[i].b == (long long)t[i].heads * x[i].h;
   }
   const int kind = (group || batch == 1 || rows) ? 0 : heads ? 1 : -1;
   for (int i = 0; i < n && kind >= 0; ++i) {
@@ -187,12 +188,18 @@ static int validate_bwd(const attn_bwd_params* p) {
     return ATTN_ERR_UNSUPPORTED_HEADDIM;
   }
   // 16-bit tensors feed tensor maps and 16-byte vector accesses; fp32 tensors
-  // and lse are read and written one element at a time
+  // and lse are read and written one element at a time.  The tensors of a
+  // side with no rows at all (no queries, or no keys) may be null.
+  const bool gq = p->cu_seqlens_q != nullptr;
+  const bool no_q = (gq ? (long long)p->total_q : (long long)p->batch * p->seqlen_q) == 0;
+  const bool no_k = (gq ? (long long)p->total_k : (long long)p->batch * p->seqlen_k) == 0;
   const uintptr_t amask = p->dtype == ATTN_FP32 ? 3u : 15u;
   const void* ptrs[] = {p->q, p->k, p->v, p->o, p->dout, p->dq, p->dk, p->dv};
-  for (const void* x : ptrs)
-    if (!x || (reinterpret_cast<uintptr_t>(x) & amask) != 0) return ATTN_ERR_INVALID_ARG;
-  if (!p->lse || (reinterpret_cast<uintptr_t>(p->lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  const bool may_be_null[] = {no_q, no_k, no_k, no_q, no_q, no_q, no_k, no_k};
+  for (int i = 0; i < 8; ++i)
+    if ((!ptrs[i] && !may_be_null[i]) || (reinterpret_cast<uintptr_t>(ptrs[i]) & amask) != 0)
+      return ATTN_ERR_INVALID_ARG;
+  if ((!p->lse && !no_q) || (reinterpret_cast<uintptr_t>(p->lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -203,12 +210,17 @@ static int validate_fwd(const attn_fwd_params* p) {
   if (p->d_qk > 256 || p->d_v > 256) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   // 16-bit tensors feed tensor maps and 16-byte vector stores of O (the same
   // rule as the backward's); fp32 tensors and lse are accessed one element
-  // at a time
+  // at a time.  The tensors of a side with no rows at all may be null.
+  const bool gq = p->cu_seqlens_q != nullptr;
+  const bool no_q = (gq ? (long long)p->total_q : (long long)p->batch * p->seqlen_q) == 0;
+  const bool no_k = (gq ? (long long)p->total_k : (long long)p->batch * p->seqlen_k) == 0;
   const uintptr_t amask = p->dtype == ATTN_FP32 ? 3u : 15u;
   const void* ptrs[] = {p->q, p->k, p->v, p->o};
-  for (const void* x : ptrs)
-    if (!x || (reinterpret_cast<uintptr_t>(x) & amask) != 0) return ATTN_ERR_INVALID_ARG;
-  if (!p->lse || (reinterpret_cast<uintptr_t>(p->lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  const bool may_be_null[] = {no_q, no_k, no_k, no_q};
+  for (int i = 0; i < 4; ++i)
+    if ((!ptrs[i] && !may_be_null[i]) || (reinterpret_cast<uintptr_t>(ptrs[i]) & amask) != 0)
+      return ATTN_ERR_INVALID_ARG;
+  if ((!p->lse && !no_q) || (reinterpret_cast<uintptr_t>(p->lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -329,12 +341,21 @@ static int launch_main(const Problem& P, cudaStream_t s) {
   return launch_bwd_tc(P, s);
 }
 
+// No query rows or no key rows in total: the gradients of the other side are
+// zero and no attention kernel runs.
+static bool empty_problem(const Problem& P) { return rows_q(P) == 0 || rows_k(P) == 0; }
+
 static int run(const attn_bwd_params* p, void* ws, size_t ws_bytes, cudaStream_t s,
                cudaEvent_t* ev /* 4 events or null */, bool keep_status = false) {
   Problem P;
   int st = prepare(p, ws, ws_bytes, &P);
   if (st != ATTN_OK) return st;
   if (ev) cudaEventRecord(ev[0], s);
+  if (empty_problem(P)) {
+    launch_empty(P, s, keep_status);
+    for (int i = 1; ev && i < 4; ++i) cudaEventRecord(ev[i], s);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
   launch_schedule_preprocess(P, s, keep_status);
   if (ev) cudaEventRecord(ev[1], s);
   if ((st = launch_main(P, s)) != ATTN_OK) return st;
@@ -382,8 +403,14 @@ static int run_host(const attn_bwd_params* p, const attn_host_tensors* h, void* 
                     cudaStream_t in, cudaStream_t out, int chunks) {
   int st = validate_bwd(p);
   if (st != ATTN_OK) return st;
-  if (!h || !h->q || !h->k || !h->v || !h->o || !h->dout || !h->lse || !h->dq || !h->dk || !h->dv)
-    return ATTN_ERR_INVALID_ARG;
+  if (!h) return ATTN_ERR_INVALID_ARG;
+  {  // as on the device side, a side with no rows at all may have null tensors
+    const bool gq = p->cu_seqlens_q != nullptr;
+    const bool no_q = (gq ? (long long)p->total_q : (long long)p->batch * p->seqlen_q) == 0;
+    const bool no_k = (gq ? (long long)p->total_k : (long long)p->batch * p->seqlen_k) == 0;
+    if ((!no_q && (!h->q || !h->o || !h->dout || !h->lse || !h->dq)) || (!no_k && (!h->k || !h->v || !h->dk || !h->dv)))
+      return ATTN_ERR_INVALID_ARG;
+  }
   if (s == in || s == out || in == out) return ATTN_ERR_INVALID_ARG;
   // the staging buffers are contiguous (zero strides, or the contiguous ones spelt out)
   const bool group = p->cu_seqlens_q != nullptr;
@@ -483,13 +510,19 @@ static int run_host(const attn_bwd_params* p, const attn_host_tensors* h, void* 
     part.lse = p->lse + lse_off;
     Problem P;
     if ((st = prepare(&part, ws, ws_bytes, &P)) != ATTN_OK) break;
-    // the preprocess overlaps the copies of Q, K and V
-    if (!(ok = cudaStreamWaitEvent(s, ev[c][E_PRE], 0) == cudaSuccess)) break;
-    launch_schedule_preprocess(P, s, c > 0);
-    if (!(ok = cudaStreamWaitEvent(s, ev[c][E_IN], 0) == cudaSuccess)) break;
-    if ((st = launch_main(P, s)) != ATTN_OK) break;
-    if (!(ok = cudaEventRecord(ev[c][E_MAIN], s) == cudaSuccess)) break;
-    launch_reduce_convert(P, s);
+    if (empty_problem(P)) {
+      if (!(ok = cudaStreamWaitEvent(s, ev[c][E_IN], 0) == cudaSuccess)) break;
+      launch_empty(P, s, c > 0);
+      if (!(ok = cudaEventRecord(ev[c][E_MAIN], s) == cudaSuccess)) break;
+    } else {
+      // the preprocess overlaps the copies of Q, K and V
+      if (!(ok = cudaStreamWaitEvent(s, ev[c][E_PRE], 0) == cudaSuccess)) break;
+      launch_schedule_preprocess(P, s, c > 0);
+      if (!(ok = cudaStreamWaitEvent(s, ev[c][E_IN], 0) == cudaSuccess)) break;
+      if ((st = launch_main(P, s)) != ATTN_OK) break;
+      if (!(ok = cudaEventRecord(ev[c][E_MAIN], s) == cudaSuccess)) break;
+      launch_reduce_convert(P, s);
+    }
     if (!(ok = cudaEventRecord(ev[c][E_CONV], s) == cudaSuccess && cudaGetLastError() == cudaSuccess)) break;
     auto copy_out = [&](int i) {
       int x0, x1;
@@ -575,6 +608,12 @@ extern "C" int attn_fwd(const attn_fwd_params* p, cudaStream_t stream) {
   FwdLayout L;
   const int s2 = effective_fwd(*p, &e, &L);
   if (s2 != ATTN_OK) return s2;
+  const bool gq = e.cu_seqlens_q != nullptr;
+  if ((gq ? (long long)e.total_q : (long long)e.batch * e.seqlen_q) == 0) return ATTN_OK;   // no rows to write
+  if ((gq ? (long long)e.total_k : (long long)e.batch * e.seqlen_k) == 0) {
+    launch_fwd_no_keys(e, L, stream);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
   // the tensor-core forward has no bias or dropout: the CUDA-core one takes those
   const bool extras = e.bias_type != ATTN_BIAS_NONE || e.dropout_p > 0.f;
   const int s3 = extras ? ATTN_ERR_UNSUPPORTED_HEADDIM : launch_fwd_tc(e, L, stream);

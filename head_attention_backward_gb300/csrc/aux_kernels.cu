@@ -261,6 +261,36 @@ __device__ void zero_padding_rows(const int* st, const int* cu, int nseg, int to
   }
 }
 
+// Rows [0, rows) x heads of a strided gradient tensor set to zero (each
+// (row, head) vector a whole number of 4-byte words at a word boundary).
+__device__ void zero_all_rows(long long rows, int heads, int dim, const Strides& x, int esize, void* out) {
+  const int wpv = dim * esize / 4;
+  uint32_t* o = static_cast<uint32_t*>(out);
+  const long long n = rows * heads * wpv;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long rr = i / ((long long)heads * wpv);
+    const int rem = (int)(i - rr * heads * wpv), hh = rem / wpv, wd = rem - hh * wpv;
+    o[elem_off(x, rr, hh) * esize / 4 + wd] = 0u;
+  }
+}
+
+// No keys at all: every query row sees nothing, dQ = 0.  No queries at all:
+// no key is seen, dK = dV = 0.
+__global__ void __launch_bounds__(256) empty_problem_kernel(Problem P, int keep_status) {
+  if (blockIdx.x == 0 && !keep_status)
+    for (int i = threadIdx.x; i < HDR_WORDS; i += blockDim.x) P.hdr[i] = 0;
+  const int w = P.dtype == ATTN_FP32 ? 4 : 2;
+  if (rows_k(P) == 0) zero_all_rows(rows_q(P), P.hq, P.dqk, P.sdq_, w, P.dq);
+  if (rows_q(P) == 0) {
+    zero_all_rows(rows_k(P), P.hkv, P.dqk, P.sdk_, w, P.dk);
+    zero_all_rows(rows_k(P), P.hkv, P.dv, P.sdv_, w, P.dv_out);
+  }
+}
+
+void launch_empty(const Problem& P, cudaStream_t st, bool keep_status) {
+  empty_problem_kernel<<<256, 256, 0, st>>>(P, keep_status ? 1 : 0);
+}
+
 constexpr int PRE_BLOCKS_PER_SM = 3;
 
 // Batch mode needs no cu_seqlens validation, so the preprocess kernel also

@@ -379,6 +379,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 void launch_preprocess(const Problem& P, cudaStream_t st);
 void launch_reduce_convert(const Problem& P, cudaStream_t st);
+// A problem with no query rows or no key rows in total: resets the workspace
+// header (unless keep_status) and zeroes the gradients of the other side.
+void launch_empty(const Problem& P, cudaStream_t st, bool keep_status);
 void launch_bwd_simt(const Problem& P, cudaStream_t st);
 int launch_bwd_tc(const Problem& P, cudaStream_t st);   // returns ATTN_* status
 int selftest_waits(void* scratch, size_t bytes, cudaStream_t st, int status[3]);
@@ -388,5 +391,7 @@ struct FwdLayout {
   long long bias_sb, bias_sh; // bias element strides of batch entry and head
 };
 void launch_fwd(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st);
+// Forward of a problem with no key rows at all (O = 0, LSE = -inf).
+void launch_fwd_no_keys(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st);
 
 }  // namespace attn

@@ -192,6 +192,29 @@ void launch_fwd(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
   }
 }
 
+// Forward with no keys at all: every query row sees nothing, so O = 0 and
+// LSE = -inf, the values of a fully masked row.  O rows are (row, head)
+// vectors of whole 4-byte words at word boundaries; LSE is dense.
+__global__ void __launch_bounds__(256) fwd_no_keys_kernel(attn_fwd_params p, Strides so, long long rows) {
+  const int esize = p.dtype == ATTN_FP32 ? 4 : 2;
+  const int wpv = p.d_v * esize / 4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t* o = static_cast<uint32_t*>(p.o);
+  const long long n = rows * p.nhead_q * wpv;
+  for (long long i = i0; i < n; i += stride) {
+    const long long rr = i / ((long long)p.nhead_q * wpv);
+    const int rem = (int)(i - rr * p.nhead_q * wpv), hh = rem / wpv, wd = rem - hh * wpv;
+    o[elem_off(so, rr, hh) * esize / 4 + wd] = 0u;
+  }
+  for (long long i = i0; i < rows * p.nhead_q; i += stride) p.lse[i] = -INFINITY;
+}
+
+void launch_fwd_no_keys(const attn_fwd_params& p, const FwdLayout& L, cudaStream_t st) {
+  const long long rows = p.cu_seqlens_q != nullptr ? (long long)p.total_q : (long long)p.batch * p.seqlen_q;
+  if (rows > 0) fwd_no_keys_kernel<<<256, 256, 0, st>>>(p, L.o, rows);
+}
+
 // ------------------------------------------------------------- SIMT backward
 // One block per work item (segment, kv head, KV tile of BN keys); thread r
 // owns key row r: it forms row r of S^T, P^T, dP^T, dS^T for each query tile

@@ -272,7 +272,12 @@ int attn_bwd_workspace_size(const attn_bwd_params* p, size_t* bytes);
  * at least attn_bwd_workspace_size bytes, 256-byte aligned; its contents on
  * entry are irrelevant (the library initialises what it needs) and it must
  * not be used by another attn_bwd call in flight.  dq, dk, dv are fully
- * overwritten.  Invalid arguments return an error before any launch;
+ * overwritten.  A problem with no query rows or no key rows in total (batch
+ * x seqlen, or total_q / total_k in group mode, equal to 0) runs no attention
+ * kernel: the other side's gradients are zeroed (no keys: every row sees
+ * nothing, dQ = 0; no queries: dK = dV = 0), the tensors of the empty side
+ * may be null and cu_seqlens are not read.  Invalid arguments return an
+ * error before any launch;
  * problems found on the device (cu_seqlens inconsistent with the declared
  * bounds, an expired wait) are recorded in the workspace and returned by
  * attn_bwd_read_status. */
@@ -289,7 +294,10 @@ int attn_bwd_timed(const attn_bwd_params* p, void* workspace, size_t workspace_b
  * attn_bwd run on `workspace` (ATTN_OK or an attn_status_t) in *status. */
 int attn_bwd_read_status(const void* workspace, cudaStream_t stream, int* status);
 
-/* Enqueue the forward helper on `stream`. */
+/* Enqueue the forward helper on `stream`.  With no key rows in total every
+ * query row sees nothing: O = 0 and LSE = -inf, the values of a fully masked
+ * row; with no query rows nothing is written.  The tensors of an empty side
+ * may be null. */
 int attn_fwd(const attn_fwd_params* p, cudaStream_t stream);
 
 /* Static description of a status code. */

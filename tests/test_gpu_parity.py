@@ -401,6 +401,52 @@ def test_ordered_fold_ignores_workspace_contents(B, wl):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("det", **DET_MODES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("sq,sk", [(0, 200), (200, 0), (0, 0)], ids=["no_queries", "no_keys", "neither"])
+def test_batch_problem_with_an_empty_side(B, sq, sk, dtype, det):
+    """No keys at all: the forward gives O = 0 and LSE = -inf (a fully masked
+    row's values) and the backward dQ = 0; no queries at all: dK = dV = 0.  The
+    outputs start as NaN, so every row must be written; the status is ok even
+    after a failed call on the same workspace."""
+    g = torch.Generator().manual_seed(sq + sk)
+    rnd = lambda *shape: torch.randn(*shape, generator=g).to(dtype).cuda()  # noqa: E731
+    d = 64 if dtype == torch.float32 else 128   # head dims of each dtype's backward
+    q, k, v = rnd(2, sq, 4, d), rnd(2, sk, 2, d), rnd(2, sk, 2, d)
+    do = rnd(2, sq, 4, d)
+    o, lse = B.attn_forward(q, k, v, scale=0.088, mask=W.MASK_CAUSAL_BOTTOM_RIGHT)
+    if sk == 0:
+        assert (o == 0).all() and torch.isneginf(lse).all()
+    ws = B.alloc_workspace(16 << 20, q.device)   # above the size these problems need
+    ws[:4].copy_(torch.tensor([-6], dtype=torch.int32).view(torch.uint8))   # a stale failure status
+    out = tuple(torch.full_like(t, float("nan")) for t in (q, k, v))
+    dq, dk, dv = B.attn_backward(q, k, v, o, do, lse, scale=0.088, mask=W.MASK_CAUSAL_BOTTOM_RIGHT,
+                                 deterministic=det, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    if sk == 0:
+        assert (dq == 0).all()
+    if sq == 0:
+        assert (dk == 0).all() and (dv == 0).all()
+
+
+@pytest.mark.parametrize("det", **DET_MODES)
+def test_packed_problem_without_keys(B, det):
+    """Packed THD whose key side is empty in every segment: dQ = 0 for every
+    row, the forward's O = 0 and LSE = -inf."""
+    cu_q = torch.tensor([0, 100, 100, 163], dtype=torch.int32, device="cuda")
+    cu_k = torch.zeros(4, dtype=torch.int32, device="cuda")
+    q = torch.randn(163, 4, 128, device="cuda").to(torch.bfloat16)
+    k = torch.empty(0, 2, 128, device="cuda", dtype=torch.bfloat16)
+    kw = dict(scale=0.088, mask=W.MASK_CAUSAL_BOTTOM_RIGHT, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+              max_seqlen_q=100, max_seqlen_k=0)
+    o, lse = B.attn_forward(q, k, k, **kw)
+    assert (o == 0).all() and torch.isneginf(lse).all()
+    out = (torch.full_like(q, float("nan")), torch.empty_like(k), torch.empty_like(k))
+    dq, _, _ = B.attn_backward(q, k, k, o, torch.randn_like(q), lse, deterministic=det, out=out, **kw)
+    torch.cuda.synchronize()
+    assert (dq == 0).all()
+
+
 def test_bad_cu_seqlens_reported_by_device(B):
     wl = W.thd("bad", [100, 80, 76], hq=4, hkv=2)
     x = {k: v.cuda() for k, v in wl.inputs().items()}

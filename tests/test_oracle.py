@@ -160,6 +160,24 @@ def test_finite_differences_cross_attention_varlen():
     assert (dk[8:11] == 0).all() and (dv[8:11] == 0).all()   # segment with no queries
 
 
+def test_batch_problem_with_an_empty_side():
+    """Batch layout with no keys at all: every row's softmax runs over nothing,
+    so O = 0, LSE = -inf and dQ = 0 (the values of a fully masked row).  With
+    no queries at all no key is seen: dK = dV = 0."""
+    q, do = rnd((2, 5, 4, 6), 31), rnd((2, 5, 4, 3), 32)
+    k0, v0 = rnd((2, 0, 2, 6), 33), rnd((2, 0, 2, 3), 34)
+    o, lse = R.attn_forward(q, k0, v0, 0.4)
+    assert o.shape == (2, 5, 4, 3) and (o == 0).all()
+    assert lse.shape == (2, 4, 5) and torch.isneginf(lse).all()
+    dq, dk, dv = R.attn_backward(q, k0, v0, o, do, lse, 0.4)
+    assert (dq == 0).all() and dk.shape == k0.shape and dv.shape == v0.shape
+    q0, k, v = rnd((2, 0, 4, 6), 35), rnd((2, 7, 2, 6), 36), rnd((2, 7, 2, 3), 37)
+    for mask in (0, 1, 2):
+        o, lse = R.attn_forward(q0, k, v, 0.4, mask=mask)
+        dq, dk, dv = R.attn_backward(q0, k, v, o, torch.zeros_like(o), lse, 0.4, mask=mask)
+        assert dq.shape == q0.shape and (dk == 0).all() and (dv == 0).all()
+
+
 # ------------------------------------------------------------ closed forms
 
 def test_single_key_closed_form():
