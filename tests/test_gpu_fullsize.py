@@ -97,6 +97,38 @@ def test_head_dim_256_B1_Hq16_Hkv4_S4096(B, det):
     assert_all_ok(_check_batch(wl, x, got, [(0, 0), (0, 15), (0, 6)], [(0, 0), (0, 3)], 6), f"d256 det={det}")
 
 
+@pytest.mark.parametrize("det", [1, 0], ids=["ordered", "atomic"])
+def test_long_sequence_S131072_window_slices(B, det):
+    """A 131,072-token sequence (its row, tile and LSE indices run far past the
+    other workloads'; the split slices would need 137 GB here, so ordered fold
+    and atomic only), window (1024, 0).  Each query row sees at most 1,025
+    keys, so any 4,096-row slice starting on a tile boundary is self-contained
+    for dQ rows 1,024 and up and for dK / dV key rows 1,024 to 3,071 (only
+    queries inside the slice see them): those rows, in the first and in the
+    last slice of the sequence, are compared with the oracle run on the slice
+    alone."""
+    wl = W.Workload("win_B1_Hq2_Hkv1_S131072_left1024", torch.bfloat16, 1, 2, 1, 131072, 131072, 128, 128,
+                    W.MASK_WINDOW, left=1024, right=0, seed=61)
+    x, _, got = _run(B, wl, det)
+    dq, dk, dv = got
+    okw = dict(mask=W.MASK_WINDOW, left=1024, right=0)
+    rng = np.random.default_rng(61)
+    for a in (0, 131072 - 4096):
+        xs = {n: x[n][:, a:a + 4096] for n in ("q", "k", "v", "do")}
+        qrows = sorted(set([1024, 1087, 2048, 4095]) | set(int(r) for r in rng.integers(1024, 4096, size=6)))
+        krows = sorted(set([1024, 1151, 3071]) | set(int(r) for r in rng.integers(1024, 3072, size=5)))
+        gq = torch.cat([dq[0, [a + r for r in qrows], h] for h in range(2)])
+        rq = torch.cat([R.dq_rows(xs["q"], xs["k"], xs["v"], xs["do"], wl.scale, 0, h, qrows, **okw) for h in range(2)])
+        ek, ev = R.dkv_rows(xs["q"], xs["k"], xs["v"], xs["do"], wl.scale, 0, 0, krows, **okw)
+        reps = []
+        for name, g, r in (("dq", gq, rq), ("dk", dk[0, [a + r for r in krows], 0], ek),
+                           ("dv", dv[0, [a + r for r in krows], 0], ev)):
+            rep = compare(g, r, 2e-2, 0.9999)
+            rep["tensor"] = name
+            reps.append(rep)
+        assert_all_ok(reps, f"slice at {a}")
+
+
 def test_head_dim_256_ordered_fold_equals_split_bits(B):
     wl = W.gqa_d256(deterministic=True)
     _, _, a = _run(B, wl, 1)
