@@ -10,7 +10,7 @@ sys.path.insert(0, __file__.rsplit("/tests/", 1)[0])
 from head_attention_backward_gb300 import binding as B  # noqa: E402
 from head_attention_backward_gb300 import build, workloads as W  # noqa: E402
 from oracle import attn_ref as R  # noqa: E402
-from tests.parity import assert_all_ok, compare, per_segment_report, tolerances  # noqa: E402
+from tests.parity import assert_all_ok, call_scale, compare, per_segment_report, tolerances  # noqa: E402
 
 
 def case_list():
@@ -65,14 +65,15 @@ def main():
                                   deterministic=mode, max_seqlen_q=w.sq, max_seqlen_k=w.sk, **dkw, **gkw)
             torch.cuda.synchronize()
             reps = []
+            cf = call_scale(ref)
             for name, g, r in zip(("dq", "dk", "dv", "dbias"), got, ref):
-                rep = compare(g.cpu(), r, tol, mcos)
+                rep = compare(g.cpu(), r, tol, mcos, cf)
                 rep["tensor"] = name
                 reps.append(rep)
                 if cu is not None:
                     offs, st = (cu, stq) if name == "dq" else (cuk, stk)
                     reps.extend(per_segment_report(g.cpu(), r, offs.tolist(), name, tol, mcos,
-                                                   None if st is None else st.tolist()))
+                                                   None if st is None else st.tolist(), call_floor=cf))
             assert_all_ok(reps, f"{w.name} mode {mode} (debug build)")
             print(f"ok {w.name} mode {mode}")
 

@@ -26,16 +26,24 @@ def tolerances(dtype):
 ZERO_SIGNAL_REL = 1e-9
 
 
+def call_scale(refs):
+    """The largest max|ref| over the gradients of one call.  A whole tensor
+    whose exact value is zero (with a single visible key per row, dQ and dK
+    vanish while dV = sum of dO does not) is judged at this scale."""
+    return max((float(r.detach().abs().max()) for r in refs if r.numel()), default=0.0)
+
+
 def compare(got, ref, tol_rel, min_cos, scale_floor=0.0):
     """Max-abs-error and cosine check of one tensor (or one segment of it).
 
     Every tensor or segment with signal must satisfy, on its own scale,
     max|got - ref| <= tol_rel * max|ref| and (16-bit inputs) cosine >= min_cos.
     `scale_floor` is the max|ref| of the whole tensor when a segment is
-    compared on its own; it is used only for a zero-signal segment (its
+    compared on its own, or the call's scale (`call_scale`) when a whole
+    tensor is; it is used only for a zero-signal tensor or segment (its
     reference is at most ZERO_SIGNAL_REL * scale_floor, i.e. exactly zero up
-    to fp64 round-off), whose bound is rounding noise at the tensor's scale
-    because a fp32 kernel cannot reproduce an exact cancellation.
+    to fp64 round-off), whose bound is rounding noise at that scale because a
+    fp32 kernel cannot reproduce an exact cancellation.
     """
     got = got.detach().to("cpu", torch.float64).reshape(-1)
     ref = ref.detach().to("cpu", torch.float64).reshape(-1)
@@ -59,13 +67,15 @@ def compare(got, ref, tol_rel, min_cos, scale_floor=0.0):
     return dict(ok=ok, cos=cos, max_err=err, max_ref=max_ref, finite=finite, zero_signal=zero_signal)
 
 
-def per_segment_report(got, ref, cu, name, tol_rel, min_cos, starts=None):
+def per_segment_report(got, ref, cu, name, tol_rel, min_cos, starts=None, call_floor=0.0):
     """One comparison per segment of a [T, H, D] tensor; segment b has length
-    cu[b+1] - cu[b] and starts at row starts[b] (cu[b] when packed)."""
+    cu[b+1] - cu[b] and starts at row starts[b] (cu[b] when packed).  A
+    zero-signal segment is judged at the tensor's scale, or at `call_floor`
+    (the call's scale) when that is larger."""
     out = []
     cu = [int(x) for x in cu]
     starts = cu if starts is None else [int(x) for x in starts]
-    floor = float(ref.detach().abs().max()) if ref.numel() else 0.0
+    floor = max(float(ref.detach().abs().max()) if ref.numel() else 0.0, call_floor)
     for b in range(len(cu) - 1):
         n = cu[b + 1] - cu[b]
         rows = slice(starts[b], starts[b] + n)

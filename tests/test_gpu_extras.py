@@ -16,7 +16,7 @@ import torch
 
 from head_attention_backward_gb300 import workloads as W
 from oracle import attn_ref as R
-from tests.parity import assert_all_ok, compare, layout_heads_outer, per_segment_report, tolerances
+from tests.parity import assert_all_ok, call_scale, compare, layout_heads_outer, per_segment_report, tolerances
 from tests.test_gpu_parity import B  # noqa: F401  (fixture)
 
 pytestmark = pytest.mark.gpu
@@ -63,13 +63,14 @@ def run_extras(B, wl, det, bias_kind=None, dropout_p=0.0, seed=0, offset=0, layo
     tol, mcos = tolerances(wl.dtype)
     reps = []
     names = ("dq", "dk", "dv", "dbias")[:len(ref)]
+    cf = call_scale(ref)
     for name, g, r in zip(names, got, ref):
         g = g.cpu()
-        rep = compare(g, r, tol, mcos)
+        rep = compare(g, r, tol, mcos, cf)
         rep["tensor"] = name
         reps.append(rep)
         if name == "dbias":
-            floor = float(r.abs().max())
+            floor = max(float(r.abs().max()), cf)
             for b in range(r.shape[0]):
                 for h in range(r.shape[1]):
                     rr = compare(g[b, h], r[b, h], tol, mcos, floor)
@@ -77,7 +78,7 @@ def run_extras(B, wl, det, bias_kind=None, dropout_p=0.0, seed=0, offset=0, layo
                     reps.append(rr)
         elif cu is not None:
             offs = cu if name == "dq" else cuk
-            reps.extend(per_segment_report(g, r, offs.tolist(), name, tol, mcos))
+            reps.extend(per_segment_report(g, r, offs.tolist(), name, tol, mcos, call_floor=cf))
     return reps
 
 

@@ -14,8 +14,8 @@ import torch
 
 from head_attention_backward_gb300 import workloads as W
 from oracle import attn_ref as R
-from tests.parity import (STRIDED_LAYOUTS, assert_all_ok, compare, layout_heads_outer, layout_packed,
-                          layout_sbhd, per_segment_report, tolerances)
+from tests.parity import (STRIDED_LAYOUTS, assert_all_ok, call_scale, compare, layout_heads_outer,
+                          layout_packed, layout_sbhd, per_segment_report, tolerances)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,16 +56,17 @@ def run_backward_vs_oracle(B, wl, deterministic, ref_fwd=True):
                           max_seqlen_k=wl.sk, out=out, **dkw)
     torch.cuda.synchronize()
     tol, mcos = tolerances(wl.dtype)
+    cf = call_scale(ref)
     reps = []
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         g = g.cpu()
-        rep = compare(g, r, tol, mcos)
+        rep = compare(g, r, tol, mcos, cf)
         rep["tensor"] = name
         reps.append(rep)
         if cu is not None:
             offs, st = (cu, stq) if name == "dq" else (cuk, stk)
             reps.extend(per_segment_report(g, r, offs.tolist(), name, tol, mcos,
-                                           None if st is None else st.tolist()))
+                                           None if st is None else st.tolist(), call_floor=cf))
             pad = wl.padding_rows("q" if name == "dq" else "k")
             if pad:
                 zero = bool((g[pad] == 0).all())
@@ -90,6 +91,10 @@ SMALL = [
     _wl("bf16_d256_causal_ragged", torch.bfloat16, 2, 4, 2, 300, 300, 256, 256, W.MASK_CAUSAL_TOP_LEFT, seed=13),
     _wl("fp16_d256_window_sq_ne_sk", torch.float16, 1, 2, 1, 200, 333, 256, 256, W.MASK_WINDOW, 90, 10, seed=14),
     _wl("bf16_d256_nomask_one_tile", torch.bfloat16, 1, 2, 2, 64, 128, 256, 256, W.MASK_NONE, seed=15),
+    # a single key: dQ and dK are exactly zero (dS = P (dP - D) cancels), dV = sum of dO
+    _wl("bf16_single_key", torch.bfloat16, 2, 4, 2, 150, 1, 128, 128, W.MASK_NONE, seed=16),
+    _wl("fp32_single_key", torch.float32, 1, 2, 1, 70, 1, 32, 32, W.MASK_NONE, seed=17),
+    _wl("fp16_d192_single_key_window", torch.float16, 1, 2, 2, 90, 1, 192, 128, W.MASK_WINDOW, 5, 0, seed=18),
 ]
 
 
@@ -196,16 +201,17 @@ def run_strided_vs_oracle(B, wl, det, layout):
                           deterministic=det, max_seqlen_q=wl.sq, max_seqlen_k=wl.sk, out=out, **dkw)
     torch.cuda.synchronize()
     tol, mcos = tolerances(wl.dtype)
+    cf = call_scale(ref)
     reps = []
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         g = g.cpu()
-        rep = compare(g, r, tol, mcos)
+        rep = compare(g, r, tol, mcos, cf)
         rep["tensor"] = name
         reps.append(rep)
         if cu is not None:
             offs, st = (cu, stq) if name == "dq" else (cuk, stk)
             reps.extend(per_segment_report(g, r, offs.tolist(), name, tol, mcos,
-                                           None if st is None else st.tolist()))
+                                           None if st is None else st.tolist(), call_floor=cf))
     return reps
 
 

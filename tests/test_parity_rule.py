@@ -6,7 +6,7 @@ signal is judged on its own scale; only a segment whose exact gradient is zero
 (fp64 round-off in the reference) is judged against the tensor's scale."""
 import torch
 
-from tests.parity import ZERO_SIGNAL_REL, compare, per_segment_report
+from tests.parity import ZERO_SIGNAL_REL, call_scale, compare, per_segment_report
 
 
 def _tensor(seed, rows):
@@ -64,3 +64,26 @@ def test_fp32_rule_has_no_cosine_and_a_tight_bound():
     ref = _tensor(5, 10)
     assert compare(ref * (1 + 5e-5), ref, 1e-4, 0.0)["ok"]
     assert not compare(ref * (1 + 5e-4), ref, 1e-4, 0.0)["ok"]
+
+
+def test_zero_gradient_tensor_is_judged_on_the_call_scale():
+    """A single visible key per row: dQ and dK are exactly zero (dS = P (dP - D)
+    cancels) while dV = sum of dO is not.  The kernel's fp32 residue of that
+    cancellation is judged at the call's largest gradient; an error of 5 % of
+    that scale still fails, and without a call scale the strict rule stays."""
+    dv = _tensor(5, 20)
+    dq = 1e-17 * _tensor(6, 20)               # exact zero up to fp64 round-off
+    cf = call_scale([dq, dv])
+    assert cf == float(dv.abs().max())
+    residue = dq + 1e-7 * cf * _tensor(7, 20) / float(_tensor(7, 20).abs().max())
+    rep = compare(residue, dq, 2e-2, 0.9999, cf)
+    assert rep["ok"] and rep["zero_signal"]
+    assert not compare(dq + 0.05 * cf, dq, 2e-2, 0.9999, cf)["ok"]
+    assert not compare(residue, dq, 2e-2, 0.9999)["ok"]
+    # a tensor with signal keeps its own scale even with a call scale given
+    got = dv.clone()
+    got[0, 0, 0] += 0.05 * float(dv.abs().max())
+    assert not compare(got, dv, 2e-2, 0.9999, 10 * cf)["ok"]
+    # segments of a zero-signal tensor take the call scale too
+    rep = per_segment_report(residue, dq, [0, 10, 20], "dq", 2e-2, 0.9999, call_floor=cf)
+    assert all(r["ok"] and r["zero_signal"] for r in rep)
